@@ -1,0 +1,207 @@
+"""fp64 CPU oracle for the batched FFT library (numpy front end over liboracle.so).
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference leg of ``bench.py`` may import this package.  The CUDA library and its Python
+binding never import it, and it imports nothing from them.
+
+Every function takes numpy arrays holding the exact values the GPU sees (complex64 / float32
+are upcast to complex128 / float64, which is exact) and returns float64 / complex128 results.
+Conventions (readings of the pages):
+
+* ``fft``: X_k = sum_j x_j exp(s*2*pi*i*j*k/N), s = -1 forward, +1 inverse, unnormalised
+  (Mota, "High Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5, without the
+  1/N of the inverse; the WGSL fourier.ts Stockham kernels are unnormalised).
+* ``fft_shifted``: forward with fftshift = rotation of every row (or image) by N/2
+  ("The 1D fftshift in CUDA by chessboard multiplication", "What is fftshift?");
+  inverse with shift = inverse transform, then multiply by the chessboard (-1)^j.
+* ``r2c`` / ``c2r``: band-limited real analysis / synthesis of fourier.ts (header comment,
+  fftAnalysWGSL / fftSynthWGSL), 0 <= mmax < N/2, spectra row-major [rows][mmax+1] or
+  m-major [mmax+1][rows] (fourier.ts stores fm[m*NLAT + ilat]).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        ci = ctypes.c_int
+        sig = {
+            "oracle_dft": [p, i64, i64, ci, p],
+            "oracle_dft_bins": [p, i64, ci, p, i64, p],
+            "oracle_fft": [p, i64, i64, ci, p],
+            "oracle_fft2d": [p, i64, i64, ci, p],
+            "oracle_fftshift": [p, i64, i64, ci, p],
+            "oracle_chessboard": [p, i64, i64, ci, p],
+            "oracle_r2c": [p, i64, i64, i64, p],
+            "oracle_c2r": [p, i64, i64, i64, p],
+            "oracle_r2c_direct": [p, i64, i64, i64, p],
+            "oracle_c2r_direct": [p, i64, i64, i64, p],
+        }
+        for name, args in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ci
+        lib.oracle_num_threads.restype = ci
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_set_num_threads.restype = None
+        lib.oracle_set_num_threads.argtypes = [ci]
+        _LIB = lib
+    return _LIB
+
+
+def _c128(x):
+    return np.ascontiguousarray(x, dtype=np.complex128)
+
+
+def _f64(x):
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise ValueError(f"oracle: {name} rejected its arguments")
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses."""
+    return int(_lib().oracle_num_threads())
+
+
+def set_num_threads(t: int) -> None:
+    _lib().oracle_set_num_threads(int(t))
+
+
+def dft(x, sign=-1):
+    """Direct O(N^2) DFT of every row of x (last axis), any length N >= 1."""
+    x = _c128(x)
+    n = x.shape[-1]
+    out = np.empty_like(x)
+    _check(_lib().oracle_dft(_ptr(x), n, x.size // n, int(sign), _ptr(out)), "dft")
+    return out
+
+
+def dft_bins(row, bins, sign=-1):
+    """Selected bins of one row, each by the direct O(N) sum."""
+    row = _c128(row).ravel()
+    bins = np.ascontiguousarray(bins, dtype=np.int64)
+    out = np.empty(bins.shape, dtype=np.complex128)
+    _check(_lib().oracle_dft_bins(_ptr(row), row.size, int(sign), _ptr(bins), bins.size,
+                                  _ptr(out)), "dft_bins")
+    return out
+
+
+def fft(x, sign=-1):
+    """Recursive radix-2 DIT FFT of every row of x (last axis, power-of-two length)."""
+    x = _c128(x)
+    n = x.shape[-1]
+    out = np.empty_like(x)
+    _check(_lib().oracle_fft(_ptr(x), n, x.size // n, int(sign), _ptr(out)), "fft")
+    return out
+
+
+def fft2d(x, sign=-1):
+    """Row-column 2-D FFT of every n x n image (last two axes)."""
+    x = _c128(x)
+    n = x.shape[-1]
+    if x.shape[-2] != n:
+        raise ValueError("oracle.fft2d: images must be square")
+    out = np.empty_like(x)
+    _check(_lib().oracle_fft2d(_ptr(x), n, x.size // (n * n), int(sign), _ptr(out)), "fft2d")
+    return out
+
+
+def fftshift(x, dims=1):
+    """Rotate every row (dims=1) or image (dims=2) by n/2 (numpy-style fftshift, even n)."""
+    x = _c128(x)
+    n = x.shape[-1]
+    out = np.empty_like(x)
+    per = n if dims == 1 else n * n
+    _check(_lib().oracle_fftshift(_ptr(x), n, x.size // per, int(dims), _ptr(out)),
+           "fftshift")
+    return out
+
+
+def chessboard(x, dims=1):
+    """Multiply element-wise by (-1)^j (dims=1) or (-1)^(row+col) (dims=2)."""
+    x = _c128(x)
+    n = x.shape[-1]
+    out = np.empty_like(x)
+    per = n if dims == 1 else n * n
+    _check(_lib().oracle_chessboard(_ptr(x), n, x.size // per, int(dims), _ptr(out)),
+           "chessboard")
+    return out
+
+
+def transform(x, direction=-1, dims=1, shift=False):
+    """What one exec of a C2C plan computes, in fp64.
+
+    direction -1: forward; with shift, the output is fftshift(FFT(x)).
+    direction +1: inverse; with shift, the output is (-1)^j * IFFT(x) (chessboard post-multiply).
+    """
+    y = fft(x, direction) if dims == 1 else fft2d(x, direction)
+    if shift:
+        y = fftshift(y, dims) if direction == -1 else chessboard(y, dims)
+    return y
+
+
+def to_mmajor(F):
+    """Row-major spectrum [rows][mmax+1] -> m-major [mmax+1][rows] (fm[m*NLAT + ilat])."""
+    return np.ascontiguousarray(np.asarray(F).T)
+
+
+def from_mmajor(Fm):
+    """m-major [mmax+1][rows] -> row-major [rows][mmax+1]."""
+    return np.ascontiguousarray(np.asarray(Fm).T)
+
+
+def r2c(x, mmax, layout="rowmajor"):
+    """Band-limited analysis F_m, m = 0..mmax, of every real row (FFT path)."""
+    x = _f64(x)
+    n = x.shape[-1]
+    rows = x.size // n
+    F = np.empty((rows, mmax + 1), dtype=np.complex128)
+    _check(_lib().oracle_r2c(_ptr(x), n, rows, int(mmax), _ptr(F)), "r2c")
+    return to_mmajor(F) if layout == "mmajor" else F
+
+
+def c2r(F, n, layout="rowmajor"):
+    """Band-limited synthesis of real rows of length n from F_m (FFT path)."""
+    F = _c128(from_mmajor(F) if layout == "mmajor" else F)
+    rows, m1 = F.shape
+    x = np.empty((rows, n), dtype=np.float64)
+    _check(_lib().oracle_c2r(_ptr(F), n, rows, m1 - 1, _ptr(x)), "c2r")
+    return x
+
+
+def r2c_direct(x, mmax):
+    """Direct band-limited analysis sum (row-major output)."""
+    x = _f64(x)
+    n = x.shape[-1]
+    rows = x.size // n
+    F = np.empty((rows, mmax + 1), dtype=np.complex128)
+    _check(_lib().oracle_r2c_direct(_ptr(x), n, rows, int(mmax), _ptr(F)), "r2c_direct")
+    return F
+
+
+def c2r_direct(F, n):
+    """Direct band-limited synthesis sum (row-major input)."""
+    F = _c128(F)
+    rows, m1 = F.shape
+    x = np.empty((rows, n), dtype=np.float64)
+    _check(_lib().oracle_c2r_direct(_ptr(F), n, rows, m1 - 1, _ptr(x)), "c2r_direct")
+    return x

@@ -1,0 +1,270 @@
+"""Pins for the fp64 oracle, against facts the pages and the mathematics fix (CPU only).
+
+Each check is independent of the oracle's own code: a printed worked example, the closed
+4-point form, brute force on tiny sizes, numpy's FFT (a library routine), closed forms
+(delta, tone, plane wave, single real mode) and invariants (linearity, Parseval, round trip,
+chessboard = rotation, Hermitian symmetry).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+
+def crand(*shape):
+    return RNG.standard_normal(shape) + 1j * RNG.standard_normal(shape)
+
+
+def rel(a, b):
+    return np.linalg.norm(np.ravel(a - b)) / max(np.linalg.norm(np.ravel(b)), 1e-300)
+
+
+# --- Mota §2.2 worked example -----------------------------------------------------------------
+def _load_golden(name):
+    x, X = {}, {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            tag, i, re, im = line.split()
+            (x if tag == "x" else X)[int(i)] = complex(float(re), float(im))
+    n = len(x)
+    return (np.array([x[i] for i in range(n)]), np.array([X[i] for i in range(n)]))
+
+
+def test_worked_example_n8():
+    x, X = _load_golden("dft_worked_example_n8.txt")
+    for f in (oracle.fft, oracle.dft):
+        np.testing.assert_allclose(f(x[None], -1)[0], X, atol=1e-3)
+    # with the exact samples cos(2 pi n/8) the printed answer holds to rounding
+    xe = np.cos(2 * np.pi * np.arange(8) / 8)
+    np.testing.assert_allclose(oracle.fft(xe[None], -1)[0], X, atol=1e-12)
+
+
+# --- Mota §2.3 Eq. 7: the 4-point DFT written out -------------------------------------------
+@pytest.mark.parametrize("sign", [-1, 1])
+def test_four_point_closed_form(sign):
+    x = crand(16, 4)
+    x0, x1, x2, x3 = x.T
+    i = 1j * (-sign)  # Eq. 7 is the forward transform; the inverse flips i
+    X = np.stack([x0 + x1 + x2 + x3,
+                  x0 - i * x1 - x2 + i * x3,
+                  x0 - x1 + x2 - x3,
+                  x0 + i * x1 - x2 - i * x3], axis=1)
+    np.testing.assert_allclose(oracle.fft(x, sign), X, atol=1e-13)
+    np.testing.assert_allclose(oracle.dft(x, sign), X, atol=1e-13)
+
+
+# --- brute force and a library FFT ----------------------------------------------------------
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("sign", [-1, 1])
+def test_fft_matches_direct_dft(n, sign):
+    x = crand(3, n)
+    # an independent direct sum written in numpy (outer product of indices)
+    j = np.arange(n)
+    W = np.exp(sign * 2j * np.pi * np.outer(j, j) / n)
+    ref = x @ W
+    assert rel(oracle.dft(x, sign), ref) < 1e-13
+    assert rel(oracle.fft(x, sign), ref) < 1e-13
+
+
+@pytest.mark.parametrize("n", [3, 5, 6, 12])
+def test_dft_non_power_of_two_vs_numpy(n):
+    x = crand(2, n)
+    assert rel(oracle.dft(x, -1), np.fft.fft(x)) < 1e-13
+
+
+@pytest.mark.parametrize("logn", list(range(1, 17)) + [20])
+def test_fft_matches_numpy(logn):
+    n = 1 << logn
+    rows = max(1, (1 << 16) // n)
+    x = crand(rows, n)
+    assert rel(oracle.fft(x, -1), np.fft.fft(x)) < 1e-14
+    assert rel(oracle.fft(x, +1), np.fft.ifft(x) * n) < 1e-14
+
+
+def test_fft_rejects_non_power_of_two():
+    with pytest.raises(ValueError):
+        oracle.fft(crand(1, 6))
+
+
+# --- closed forms -----------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [2, 16, 1024, 1 << 15])
+def test_delta(n):
+    x = np.zeros((1, n), complex)
+    x[0, 0] = 1
+    np.testing.assert_array_equal(oracle.fft(x, -1), np.ones((1, n)))
+    j0 = 3 % n
+    x = np.zeros((1, n), complex)
+    x[0, j0] = 1
+    k = np.arange(n)
+    np.testing.assert_allclose(oracle.fft(x, -1)[0], np.exp(-2j * np.pi * j0 * k / n),
+                               atol=1e-12)
+
+
+@pytest.mark.parametrize("n", [8, 256, 4096])
+@pytest.mark.parametrize("sign", [-1, 1])
+def test_tone_gives_delta(n, sign):
+    k0 = (5 * n) // 7
+    j = np.arange(n)
+    x = np.exp(-sign * 2j * np.pi * k0 * j / n)[None]
+    X = oracle.fft(x, sign)[0]
+    ref = np.zeros(n, complex)
+    ref[k0] = n
+    assert np.max(np.abs(X - ref)) < 1e-9 * n
+
+
+def test_linearity():
+    x, y = crand(4, 512), crand(4, 512)
+    a, b = 0.3 - 1.2j, -2.0 + 0.5j
+    assert rel(oracle.fft(a * x + b * y), a * oracle.fft(x) + b * oracle.fft(y)) < 1e-14
+
+
+@pytest.mark.parametrize("n", [64, 8192])
+def test_parseval(n):
+    x = crand(2, n)
+    X = oracle.fft(x)
+    np.testing.assert_allclose(np.sum(np.abs(X) ** 2, axis=1),
+                               n * np.sum(np.abs(x) ** 2, axis=1), rtol=1e-12)
+
+
+@pytest.mark.parametrize("n", [2, 128, 1 << 14])
+def test_round_trip_is_n_times_identity(n):
+    x = crand(3, n)
+    assert rel(oracle.fft(oracle.fft(x, -1), +1), n * x) < 1e-14
+
+
+def test_dft_bins_match_fft():
+    n = 1 << 12
+    x = crand(1, n)
+    bins = np.array([0, 1, 7, n // 2, n - 1, 1234])
+    np.testing.assert_allclose(oracle.dft_bins(x[0], bins, -1), oracle.fft(x, -1)[0, bins],
+                               atol=1e-9)
+
+
+# --- chessboard fftshift ("The 1D fftshift in CUDA by chessboard multiplication") -----------
+@pytest.mark.parametrize("n", [2, 8, 4096])
+def test_fftshift_matches_numpy(n):
+    x = crand(3, n)
+    np.testing.assert_array_equal(oracle.fftshift(x, 1), np.fft.fftshift(x, axes=-1))
+    img = crand(2, 8, 8)
+    np.testing.assert_array_equal(oracle.fftshift(img, 2), np.fft.fftshift(img, axes=(-2, -1)))
+
+
+@pytest.mark.parametrize("n", [2, 16, 4096])
+def test_chessboard_premultiply_equals_shift(n):
+    x = crand(4, n)
+    lhs = oracle.fft(oracle.chessboard(x, 1), -1)
+    rhs = oracle.fftshift(oracle.fft(x, -1), 1)
+    assert rel(lhs, rhs) < 1e-14
+    # inverse with shift undoes forward with shift up to the factor N
+    y = oracle.transform(oracle.transform(x, -1, 1, True), +1, 1, True)
+    assert rel(y, n * x) < 1e-14
+
+
+def test_chessboard_values():
+    x = np.ones((1, 6), complex)
+    np.testing.assert_array_equal(oracle.chessboard(x, 1)[0], [1, -1, 1, -1, 1, -1])
+    img = np.ones((1, 2, 2), complex)
+    np.testing.assert_array_equal(oracle.chessboard(img, 2)[0], [[1, -1], [-1, 1]])
+
+
+def test_shifted_tone_lands_at_k_plus_half():
+    n, k0 = 64, 5
+    x = np.exp(2j * np.pi * k0 * np.arange(n) / n)[None]
+    X = oracle.transform(x, -1, 1, True)[0]
+    assert np.argmax(np.abs(X)) == (k0 + n // 2) % n
+
+
+# --- 2-D (Mota §2.7 Eq. 19) -------------------------------------------------------------------
+def test_fft2d_matches_numpy_and_separability():
+    n = 32
+    img = crand(2, n, n)
+    assert rel(oracle.fft2d(img, -1), np.fft.fft2(img)) < 1e-14
+    assert rel(oracle.fft2d(img, +1), np.fft.ifft2(img) * n * n) < 1e-14
+    u, v = crand(n), crand(n)
+    lhs = oracle.fft2d(np.outer(u, v)[None], -1)[0]
+    rhs = np.outer(oracle.fft(u[None])[0], oracle.fft(v[None])[0])
+    assert rel(lhs, rhs) < 1e-14
+
+
+def test_plane_wave_and_2d_shift():
+    n, a, b = 16, 3, 11
+    y, x = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+    img = np.exp(2j * np.pi * (a * x + b * y) / n)[None]
+    X = oracle.fft2d(img, -1)[0]
+    ref = np.zeros((n, n), complex)
+    ref[b, a] = n * n
+    assert np.max(np.abs(X - ref)) < 1e-10
+    Xs = oracle.transform(img, -1, 2, True)[0]
+    assert np.unravel_index(np.argmax(np.abs(Xs)), Xs.shape) == ((b + n // 2) % n,
+                                                                  (a + n // 2) % n)
+    assert rel(oracle.fft2d(oracle.chessboard(img, 2), -1), oracle.fftshift(X[None], 2)) < 1e-14
+    rt = oracle.transform(oracle.transform(img, -1, 2, True), +1, 2, True)
+    assert rel(rt, n * n * img) < 1e-14
+
+
+# --- band-limited real rows (fourier.ts) ------------------------------------------------------
+@pytest.mark.parametrize("n,mmax", [(2, 0), (8, 3), (64, 20), (4096, 1365)])
+def test_r2c_is_truncated_c2c_and_direct_sum(n, mmax):
+    x = RNG.standard_normal((3, n))
+    F = oracle.r2c(x, mmax)
+    assert rel(F, np.fft.fft(x)[:, :mmax + 1]) < 1e-14
+    if n <= 64:
+        assert rel(F, oracle.r2c_direct(x, mmax)) < 1e-13
+
+
+def test_real_row_spectrum_is_hermitian():
+    n = 256
+    X = oracle.fft(RNG.standard_normal((2, n)).astype(complex))
+    np.testing.assert_allclose(X[:, 1:], np.conj(X[:, :0:-1]), atol=1e-12)
+
+
+@pytest.mark.parametrize("n,mmax", [(2, 0), (8, 3), (64, 31), (256, 85)])
+def test_c2r_matches_direct_sum(n, mmax):
+    F = crand(3, mmax + 1)
+    assert rel(oracle.c2r(F, n), oracle.c2r_direct(F, n)) < 1e-13
+
+
+def test_c2r_single_mode_is_a_cosine():
+    n, m, A, th = 128, 9, 0.75, 0.4
+    F = np.zeros((1, 20), complex)
+    F[0, m] = A * np.exp(1j * th)
+    j = np.arange(n)
+    np.testing.assert_allclose(oracle.c2r(F, n)[0], 2 * A * np.cos(2 * np.pi * m * j / n + th),
+                               atol=1e-12)
+    F = np.zeros((1, 20), complex)
+    F[0, 0] = 1.5 + 7.0j  # only Re F_0 is used
+    np.testing.assert_allclose(oracle.c2r(F, n)[0], np.full(n, 1.5), atol=1e-13)
+
+
+def test_analysis_of_synthesis():
+    n, mmax = 512, 170
+    F = crand(4, mmax + 1)
+    G = oracle.r2c(oracle.c2r(F, n), mmax)
+    np.testing.assert_allclose(G[:, 1:], n * F[:, 1:], rtol=1e-12, atol=1e-9)
+    np.testing.assert_allclose(G[:, 0], n * F[:, 0].real, atol=1e-9)
+
+
+def test_mmajor_layout_is_fm_m_times_nlat_plus_ilat():
+    nlat, mmax = 5, 3
+    F = crand(nlat, mmax + 1)
+    flat = oracle.to_mmajor(F).ravel()
+    for ilat in range(nlat):
+        for m in range(mmax + 1):
+            assert flat[m * nlat + ilat] == F[ilat, m]
+    np.testing.assert_array_equal(oracle.from_mmajor(oracle.to_mmajor(F)), F)
+    x = RNG.standard_normal((nlat, 16))
+    np.testing.assert_array_equal(oracle.r2c(x, 5, "mmajor"), oracle.to_mmajor(oracle.r2c(x, 5)))
+
+
+@pytest.mark.parametrize("bad", [(8, 4), (8, -1), (6, 1)])
+def test_band_limit_rejected(bad):
+    n, mmax = bad
+    with pytest.raises(ValueError):
+        oracle.r2c(np.zeros((1, n)), mmax)
