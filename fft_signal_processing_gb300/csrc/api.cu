@@ -1,0 +1,492 @@
+// C ABI of the library (declared in include/gbfft.h): plan creation and validation, the
+// host-side planner, the fp64 twiddle tables, and the execution paths.
+//
+// Paths (chosen at plan creation, as the WGSL "src/sht/wgsl/fourier.ts" selects its 'fft' or
+// 'dft' implementation at plan creation):
+//   onepass   dims 1, n <= 2^14: one kernel, each row resident in one CTA.
+//   fourstep  dims 1, 2^15 <= n <= 2^24: n = N1*N2 with n = n1*N2 + n2 and k = k1 + N1*k2.
+//             Pass 1 does the N1-point transforms down the N2 columns and multiplies output
+//             (k1, n2) by w_n^{n2*k1}; pass 2 does the N2-point row transforms and writes row
+//             k1's output k2 to X[k1 + N1*k2].  This is the four-step FFT the CS598 project page
+//             ("Fast Fourier Transform on CPU and GPU") names for inputs that do not fit in
+//             fast memory; the intermediate lives in the plan's workspace.
+//   2d        n x n images: all rows, then all columns (Mota, "High Performance Fourier
+//             Transforms on GPUs with GLSL", §2.7 Eq. 19), both in place in the output.
+//   real      band-limited real rows through an n/2-point complex core (fourier.ts).
+//
+// Twiddles are computed on the host in double precision from cos/sin of 2*pi*q/M with q
+// reduced modulo M in integers, and rounded once to float (fourier.ts header comment: device
+// trigonometry is too inaccurate for the fp32 transform error).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/gbfft.h"
+#include "fft_kernel.cuh"
+#include "kernels.h"
+
+using namespace gbfft;
+
+namespace {
+
+enum Path { PATH_ONEPASS = 0, PATH_FOURSTEP = 1, PATH_2D = 2, PATH_REAL = 3 };
+
+struct PlanSpec {
+    int64_t n = 0, batch = 0;
+    int dims = 1, direction = -1, layout = 0, shift = 0;
+    int log2n = 0;
+    Path path = PATH_ONEPASS;
+    int log2n1 = 0, log2n2 = 0;  // four-step split
+    int lowbits = 0;             // four-step two-level twiddle split
+};
+
+int ilog2_exact(int64_t n) {
+    if (n < 1 || (n & (n - 1))) return -1;
+    int l = 0;
+    while ((int64_t(1) << l) < n) ++l;
+    return l;
+}
+
+// Host validation and path choice shared by fft_plan_create and fft_plan_query.
+int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int shift,
+              PlanSpec* ps) {
+    if (batch < 1) return FFT_ERR_INVALID_ARG;
+    if (dims != 1 && dims != 2) return FFT_ERR_INVALID_ARG;
+    if (direction != FFT_FORWARD && direction != FFT_INVERSE) return FFT_ERR_INVALID_ARG;
+    if (layout != FFT_LAYOUT_C2C && layout != FFT_LAYOUT_REAL_ROWMAJOR &&
+        layout != FFT_LAYOUT_REAL_MMAJOR)
+        return FFT_ERR_INVALID_ARG;
+    if (shift != 0 && shift != 1) return FFT_ERR_INVALID_ARG;
+    if (layout != FFT_LAYOUT_C2C && (dims != 1 || shift)) return FFT_ERR_INVALID_ARG;
+    const int l = ilog2_exact(n);
+    if (l < 0) return FFT_ERR_UNSUPPORTED_SIZE;
+    if (shift && (n & 1)) return FFT_ERR_INVALID_ARG;
+    PlanSpec s;
+    s.n = n;
+    s.batch = batch;
+    s.dims = dims;
+    s.direction = direction;
+    s.layout = layout;
+    s.shift = shift;
+    s.log2n = l;
+    if (layout != FFT_LAYOUT_C2C) {
+        if (l < 2 || l > kMaxLog2RealH + 1) return FFT_ERR_UNSUPPORTED_SIZE;
+        s.path = PATH_REAL;
+    } else if (dims == 2) {
+        if (l < 1 || l > FFT_MAX_LOG2N_2D) return FFT_ERR_UNSUPPORTED_SIZE;
+        s.path = PATH_2D;
+    } else {
+        if (l > FFT_MAX_LOG2N_1D) return FFT_ERR_UNSUPPORTED_SIZE;
+        if (l <= kMaxLog2OnePass) {
+            s.path = PATH_ONEPASS;
+        } else {
+            s.path = PATH_FOURSTEP;
+            s.log2n1 = l / 2;      // column pass (strided)
+            s.log2n2 = l - l / 2;  // row pass (contiguous in, transposed out)
+            s.lowbits = (l + 1) / 2;
+        }
+    }
+    // total element count must stay addressable with 64-bit byte offsets
+    const int64_t per = dims == 2 ? n * n : n;
+    if (batch > (INT64_C(1) << 58) / per) return FFT_ERR_UNSUPPORTED_SIZE;
+    *ps = s;
+    return FFT_OK;
+}
+
+// ---- host twiddle tables ------------------------------------------------------------------
+const double kTwoPi = 6.283185307179586476925286766559005768;
+
+// (cos, sin)(2*pi*q/m) in double, rounded once to float.  The angle is reduced in integers to
+// the first quadrant, and cos/sin are evaluated at the nearer of a and pi/2 - a, so quarter
+// turns are exactly 0 and +-1 and the table keeps the symmetries of the unit circle.
+float2 root_of_unity(int64_t q, int64_t m) {
+    q %= m;
+    if (q < 0) q += m;
+    if (m % 4 != 0) {  // m = 1, 2: the roots are +-1
+        const bool half = (2 * q == m);
+        return make_float2(half ? -1.f : 1.f, 0.f);
+    }
+    // first quadrant angle a (in units of 2*pi/m) and the number of quarter turns
+    const int64_t qq = m / 4;
+    const int64_t quad = q / qq, a = q % qq;
+    double c, s;
+    if (a <= qq / 2) {
+        const double th = kTwoPi * (double)a / (double)m;
+        c = std::cos(th);
+        s = std::sin(th);
+    } else {  // use the complementary angle pi/2 - th for accuracy near pi/2
+        const double th = kTwoPi * (double)(qq - a) / (double)m;
+        c = std::sin(th);
+        s = std::cos(th);
+    }
+    if (a == 0) {
+        c = 1.0;
+        s = 0.0;
+    }
+    double x, y;  // rotate by quad quarter turns
+    switch (quad & 3) {
+        case 0: x = c; y = s; break;
+        case 1: x = -s; y = c; break;
+        case 2: x = -c; y = -s; break;
+        default: x = s; y = -c; break;
+    }
+    return make_float2((float)x, (float)y);
+}
+
+void push_root(std::vector<float2>& v, int64_t q, int64_t m) { v.push_back(root_of_unity(q, m)); }
+
+void align_table(std::vector<float2>& v) {
+    while (v.size() % 32) v.push_back(make_float2(0.f, 0.f));
+}
+
+// Per-pass tables of a 2^l-point transform (layout of tw_pass_off in fft_kernel.cuh).
+size_t append_pass_tables(std::vector<float2>& v, int l) {
+    align_table(v);
+    const size_t off = v.size();
+    if (l <= 4) return off;
+    const int npass = (l + 3) / 4;
+    for (int p = 1; p < npass; ++p) {
+        const int rb = (l - 4 * p >= 4) ? 4 : l - 4 * p;
+        const int64_t R = int64_t(1) << rb, Ns = int64_t(1) << (4 * p);
+        for (int64_t m = 0; m < Ns; ++m)
+            for (int64_t r = 0; r < R; ++r) push_root(v, m * r, Ns * R);
+    }
+    if (v.size() - off != (size_t)tw_table_size(l)) std::abort();  // layout invariant
+    return off;
+}
+
+size_t append_roots(std::vector<float2>& v, int64_t count, int64_t step, int64_t m) {
+    align_table(v);
+    const size_t off = v.size();
+    for (int64_t q = 0; q < count; ++q) push_root(v, q * step, m);
+    return off;
+}
+
+std::string radix_string(int l) {
+    if (l == 0) return "1";
+    std::string s;
+    int rem = l;
+    while (rem > 0) {
+        const int rb = rem >= 4 ? 4 : rem;
+        if (!s.empty()) s += "x";
+        s += std::to_string(1 << rb);
+        rem -= rb;
+    }
+    return s;
+}
+
+struct Geo {
+    int threads, per_cta;
+    size_t smem;
+};
+Geo rows_geo(int l) {
+    const int e = rows_log2e(l), w = rows_log2w(l);
+    const int npass = l <= 4 ? 1 : (l + 3) / 4;
+    return {(1 << (l - e)) << w, 1 << w,
+            npass > 1 ? (size_t)spad_size(1 << l) * (1u << w) * 8u : 0};
+}
+Geo strided_geo(int l, int log2minw) {
+    const int e = cols_log2e(l), w = cols_log2w(l, log2minw);
+    const int npass = l <= 4 ? 1 : (l + 3) / 4;
+    return {(1 << (l - e)) << w, 1 << w,
+            npass > 1 ? (size_t)spad_size(1 << l) * (1u << w) * 8u : 0};
+}
+Geo real_geo(int lh) {
+    const int e = rows_log2e(lh), w = real_log2w(lh);
+    const int npass = lh <= 4 ? 1 : (lh + 3) / 4;
+    const int srow = npass > 1 ? spad_size(1 << lh) : 0;
+    const int sreal = std::max(srow, spad_size(1 << lh) + 1);
+    return {(1 << (lh - e)) << w, 1 << w, (size_t)sreal * (1u << w) * 8u};
+}
+
+std::string describe_spec(const PlanSpec& s, int64_t mmax) {
+    char buf[512];
+    const char* dir = s.direction < 0 ? "forward" : "inverse";
+    switch (s.path) {
+        case PATH_ONEPASS: {
+            Geo g = rows_geo(s.log2n);
+            snprintf(buf, sizeof buf,
+                     "path=onepass n=%lld batch=%lld %s shift=%d radix=%s kernels=1 "
+                     "threads=%d rows_per_cta=%d smem=%zu",
+                     (long long)s.n, (long long)s.batch, dir, s.shift,
+                     radix_string(s.log2n).c_str(), g.threads, g.per_cta, g.smem);
+            break;
+        }
+        case PATH_FOURSTEP: {
+            Geo g1 = strided_geo(s.log2n1, 0), g2 = strided_geo(s.log2n2, 2);
+            snprintf(buf, sizeof buf,
+                     "path=fourstep n=%lld batch=%lld %s shift=%d n1=%d n2=%d kernels=2 "
+                     "pass1=columns(radix=%s threads=%d cols_per_cta=%d smem=%zu) "
+                     "pass2=rows_transposed(radix=%s threads=%d rows_per_cta=%d smem=%zu)",
+                     (long long)s.n, (long long)s.batch, dir, s.shift, 1 << s.log2n1,
+                     1 << s.log2n2, radix_string(s.log2n1).c_str(), g1.threads, g1.per_cta,
+                     g1.smem, radix_string(s.log2n2).c_str(), g2.threads, g2.per_cta, g2.smem);
+            break;
+        }
+        case PATH_2D: {
+            Geo g1 = rows_geo(s.log2n), g2 = strided_geo(s.log2n, 0);
+            snprintf(buf, sizeof buf,
+                     "path=2d n=%lldx%lld batch=%lld %s shift=%d radix=%s kernels=2 "
+                     "rows(threads=%d rows_per_cta=%d smem=%zu) "
+                     "columns(threads=%d cols_per_cta=%d smem=%zu)",
+                     (long long)s.n, (long long)s.n, (long long)s.batch, dir, s.shift,
+                     radix_string(s.log2n).c_str(), g1.threads, g1.per_cta, g1.smem,
+                     g2.threads, g2.per_cta, g2.smem);
+            break;
+        }
+        default: {
+            Geo g = real_geo(s.log2n - 1);
+            snprintf(buf, sizeof buf,
+                     "path=real n=%lld batch=%lld %s mmax=%lld layout=%s core=%lld radix=%s "
+                     "kernels=1 threads=%d rows_per_cta=%d smem=%zu",
+                     (long long)s.n, (long long)s.batch,
+                     s.direction < 0 ? "analysis(r2c)" : "synthesis(c2r)", (long long)mmax,
+                     s.layout == FFT_LAYOUT_REAL_MMAJOR ? "mmajor" : "rowmajor",
+                     (long long)(s.n / 2), radix_string(s.log2n - 1).c_str(), g.threads,
+                     g.per_cta, g.smem);
+            break;
+        }
+    }
+    return buf;
+}
+
+int map_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return FFT_OK;
+    return e == cudaErrorMemoryAllocation ? FFT_ERR_OOM : FFT_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+}  // namespace
+
+struct gbfft_plan_s {
+    PlanSpec s;
+    int64_t mmax = 0;
+    int device = 0;
+    float2* d_tw = nullptr;
+    size_t tw_count = 0;
+    size_t off_a = 0, off_b = 0, off_hi = 0, off_lo = 0, off_r = 0;
+    void* d_work = nullptr;
+    size_t work_bytes = 0;
+    int* d_err = nullptr;
+};
+
+static void free_plan(gbfft_plan_s* p) {
+    if (!p) return;
+    if (p->d_tw) cudaFree(p->d_tw);
+    if (p->d_work) cudaFree(p->d_work);
+    if (p->d_err) cudaFree(p->d_err);
+    delete p;
+}
+
+extern "C" {
+
+int fft_version(void) { return 10000; }
+
+const char* fft_status_string(int status) {
+    switch (status) {
+        case FFT_OK: return "FFT_OK: success";
+        case FFT_ERR_INVALID_ARG: return "FFT_ERR_INVALID_ARG: invalid argument";
+        case FFT_ERR_UNSUPPORTED_SIZE:
+            return "FFT_ERR_UNSUPPORTED_SIZE: size is not a supported power of two";
+        case FFT_ERR_MISALIGNED: return "FFT_ERR_MISALIGNED: data pointer not 16-byte aligned";
+        case FFT_ERR_OOM: return "FFT_ERR_OOM: device allocation failed";
+        case FFT_ERR_CUDA: return "FFT_ERR_CUDA: CUDA runtime or launch error";
+        case FFT_ERR_TIMEOUT: return "FFT_ERR_TIMEOUT: a bounded device-side wait gave up";
+        default: return "unknown status";
+    }
+}
+
+int fft_plan_query(int64_t n, int64_t batch, int dims, int direction, int layout, int shift,
+                   char* buf, size_t len) {
+    PlanSpec s;
+    const int rc = plan_spec(n, batch, dims, direction, layout, shift, &s);
+    if (rc != FFT_OK) return rc;
+    if (buf && len) {
+        std::string d = describe_spec(s, s.path == PATH_REAL ? s.n / 2 - 1 : 0);
+        snprintf(buf, len, "%s", d.c_str());
+    }
+    return FFT_OK;
+}
+
+int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layout, int shift,
+                    fft_plan* out) {
+    if (!out) return FFT_ERR_INVALID_ARG;
+    *out = nullptr;
+    PlanSpec s;
+    int rc = plan_spec(n, batch, dims, direction, layout, shift, &s);
+    if (rc != FFT_OK) return rc;
+
+    gbfft_plan_s* p = new (std::nothrow) gbfft_plan_s();
+    if (!p) return FFT_ERR_OOM;
+    p->s = s;
+    p->mmax = s.path == PATH_REAL ? s.n / 2 - 1 : 0;
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+        delete p;
+        return FFT_ERR_CUDA;
+    }
+
+    std::vector<float2> tw;
+    switch (s.path) {
+        case PATH_ONEPASS:
+        case PATH_2D:
+            p->off_a = append_pass_tables(tw, s.log2n);
+            break;
+        case PATH_FOURSTEP: {
+            p->off_a = append_pass_tables(tw, s.log2n1);
+            p->off_b = append_pass_tables(tw, s.log2n2);
+            const int64_t nlo = int64_t(1) << s.lowbits, nhi = int64_t(1) << (s.log2n - s.lowbits);
+            p->off_hi = append_roots(tw, nhi, nlo, s.n);  // w_n^{qh * 2^lowbits}
+            p->off_lo = append_roots(tw, nlo, 1, s.n);    // w_n^{ql}
+            p->work_bytes = (size_t)s.batch * (size_t)s.n * sizeof(float2);
+            break;
+        }
+        case PATH_REAL:
+            p->off_a = append_pass_tables(tw, s.log2n - 1);
+            p->off_r = append_roots(tw, s.n / 2, 1, s.n);  // w_n^k, k < n/2
+            break;
+    }
+    align_table(tw);
+    if (tw.empty()) tw.resize(32, make_float2(0.f, 0.f));
+    p->tw_count = tw.size();
+
+    cudaError_t e = cudaMalloc((void**)&p->d_tw, tw.size() * sizeof(float2));
+    if (e == cudaSuccess)
+        e = cudaMemcpy(p->d_tw, tw.data(), tw.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&p->d_err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int));
+    if (e == cudaSuccess && p->work_bytes) e = cudaMalloc(&p->d_work, p->work_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error state of a failed allocation
+        free_plan(p);
+        return map_cuda(e);
+    }
+    *out = p;
+    return FFT_OK;
+}
+
+int fft_plan_set_band_limit(fft_plan p, int64_t mmax) {
+    if (!p || p->s.path != PATH_REAL) return FFT_ERR_INVALID_ARG;
+    if (mmax < 0 || mmax >= p->s.n / 2) return FFT_ERR_INVALID_ARG;
+    p->mmax = mmax;
+    return FFT_OK;
+}
+
+int fft_plan_workspace_bytes(fft_plan p, size_t* bytes) {
+    if (!p || !bytes) return FFT_ERR_INVALID_ARG;
+    *bytes = p->work_bytes;
+    return FFT_OK;
+}
+
+int fft_plan_describe(fft_plan p, char* buf, size_t len) {
+    if (!p || !buf || !len) return FFT_ERR_INVALID_ARG;
+    std::string d = describe_spec(p->s, p->mmax);
+    snprintf(buf, len, "%s", d.c_str());
+    return FFT_OK;
+}
+
+int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
+    if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
+    const PlanSpec& s = p->s;
+    if (s.layout != FFT_LAYOUT_C2C) return FFT_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(out)) return FFT_ERR_MISALIGNED;
+    const size_t bytes = (size_t)s.batch * (size_t)(s.dims == 2 ? s.n * s.n : s.n) * 8u;
+    if (in != out && ranges_overlap(in, bytes, out, bytes)) return FFT_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const float2* x = (const float2*)in;
+    float2* y = (float2*)out;
+    const bool fwd = s.direction == FFT_FORWARD;
+    cudaError_t e = cudaSuccess;
+    switch (s.path) {
+        case PATH_ONEPASS: {
+            const int flags = s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0;
+            e = run_rows(s.log2n, s.direction, x, y, s.batch, p->d_tw + p->off_a, flags, 0, st);
+            break;
+        }
+        case PATH_FOURSTEP: {
+            float2* wk = (float2*)p->d_work;
+            const int64_t n1 = int64_t(1) << s.log2n1, n2 = int64_t(1) << s.log2n2;
+            e = run_cols(s.log2n1, s.direction, x, wk, s.batch * n2, s.log2n2,
+                         p->d_tw + p->off_a, (s.shift && fwd) ? KF_CHESS_LOAD : 0, 0,
+                         p->d_tw + p->off_hi, p->d_tw + p->off_lo, s.lowbits, st);
+            if (e == cudaSuccess)
+                e = run_rows_t(s.log2n2, s.direction, wk, y, s.batch * n1, s.log2n1,
+                               p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0, st);
+            break;
+        }
+        case PATH_2D: {
+            const int64_t n = s.n;
+            e = run_rows(s.log2n, s.direction, x, y, s.batch * n, p->d_tw + p->off_a,
+                         (s.shift && fwd) ? KF_CHESS_LOAD : 0, 1, st);
+            if (e == cudaSuccess)
+                e = run_cols(s.log2n, s.direction, y, y, s.batch * n, s.log2n,
+                             p->d_tw + p->off_a, (s.shift && !fwd) ? KF_CHESS_STORE : 0, 1,
+                             nullptr, nullptr, 0, st);
+            break;
+        }
+        default:
+            return FFT_ERR_INVALID_ARG;
+    }
+    return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
+}
+
+int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
+    if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
+    const PlanSpec& s = p->s;
+    if (s.path != PATH_REAL || s.direction != FFT_FORWARD) return FFT_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(out)) return FFT_ERR_MISALIGNED;
+    const size_t in_bytes = (size_t)s.batch * (size_t)s.n * 4u;
+    const size_t out_bytes = (size_t)s.batch * (size_t)(p->mmax + 1) * 8u;
+    if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
+    cudaError_t e = run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax,
+                            s.layout == FFT_LAYOUT_REAL_MMAJOR, p->d_tw + p->off_a,
+                            p->d_tw + p->off_r, (cudaStream_t)stream);
+    return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
+}
+
+int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
+    if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
+    const PlanSpec& s = p->s;
+    if (s.path != PATH_REAL || s.direction != FFT_INVERSE) return FFT_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(out)) return FFT_ERR_MISALIGNED;
+    const size_t in_bytes = (size_t)s.batch * (size_t)(p->mmax + 1) * 8u;
+    const size_t out_bytes = (size_t)s.batch * (size_t)s.n * 4u;
+    if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
+    cudaError_t e = run_c2r(s.log2n - 1, (const float2*)in, out, s.batch, (int)p->mmax,
+                            s.layout == FFT_LAYOUT_REAL_MMAJOR, p->d_tw + p->off_a,
+                            p->d_tw + p->off_r, (cudaStream_t)stream);
+    return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
+}
+
+int fft_plan_check(fft_plan p) {
+    if (!p) return FFT_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FFT_ERR_CUDA;
+    int h = 0;
+    if (cudaMemcpy(&h, p->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FFT_ERR_CUDA;
+    if (h != 0) {
+        if (cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess) return FFT_ERR_CUDA;
+        return FFT_ERR_TIMEOUT;
+    }
+    return FFT_OK;
+}
+
+int fft_plan_destroy(fft_plan p) {
+    if (!p) return FFT_OK;
+    const cudaError_t e = cudaDeviceSynchronize();
+    free_plan(p);
+    return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
+}
+
+}  // extern "C"

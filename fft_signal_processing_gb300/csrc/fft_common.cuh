@@ -1,0 +1,152 @@
+// Device building blocks shared by every kernel of the library: complex arithmetic on
+// float2 (x = re, y = im), twiddle multiplication, the in-register radix-R butterflies and the
+// shared-memory padding used by the exchanges between radix passes.
+//
+// Convention: DIR is the sign s of the exponent, -1 forward, +1 inverse (Mota, "High
+// Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5 and §2.3.1 Algorithm 2:
+// the inverse is the same algorithm with exp(+2*pi*i/m)).  Twiddle tables always store
+// (cos t, sin t) for t >= 0; the sign is applied at use, as the WGSL Stockham kernels of
+// "src/sht/wgsl/fourier.ts" do with their (cos, sin) table.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbfft {
+
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+__device__ __forceinline__ float2 cneg(float2 a) { return make_float2(-a.x, -a.y); }
+
+// a * exp(DIR * i * t) given w = (cos t, sin t).
+template <int DIR>
+__device__ __forceinline__ float2 ctw(float2 a, float2 w) {
+    if constexpr (DIR < 0)
+        return make_float2(fmaf(a.x, w.x, a.y * w.y), fmaf(a.y, w.x, -(a.x * w.y)));
+    else
+        return make_float2(fmaf(a.x, w.x, -(a.y * w.y)), fmaf(a.x, w.y, a.y * w.x));
+}
+
+// Plain complex product a*b.
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+    return make_float2(fmaf(a.x, b.x, -(a.y * b.y)), fmaf(a.x, b.y, a.y * b.x));
+}
+
+// cos(2*pi*k/32) for any integer k, as compile-time constants (quarter-wave values of the
+// 32nd roots of unity; every butterfly radix used here divides 32).
+__host__ __device__ constexpr double cos32(int k) {
+    k = ((k % 32) + 32) % 32;
+    if (k > 16) k = 32 - k;          // cos is even
+    const bool neg = k > 8;          // cos(pi - a) = -cos(a)
+    if (neg) k = 16 - k;
+    double v = 0.0;
+    switch (k) {
+        case 0: v = 1.0; break;
+        case 1: v = 0.98078528040323044912618223613424; break;
+        case 2: v = 0.92387953251128675612818318939679; break;
+        case 3: v = 0.83146961230254523707878837761791; break;
+        case 4: v = 0.70710678118654752440084436210485; break;
+        case 5: v = 0.55557023301960222474283081394853; break;
+        case 6: v = 0.38268343236508977172845998403040; break;
+        case 7: v = 0.19509032201612826784828486847702; break;
+        default: v = 0.0; break;
+    }
+    return neg ? -v : v;
+}
+__host__ __device__ constexpr double sin32(int k) { return cos32(k - 8); }
+
+// a * exp(DIR * 2*pi*i * E / R) with E, R compile-time.  Quarter turns are exact swaps and
+// sign flips; everything else is one complex multiply by float constants.
+template <int DIR, int E, int R>
+__device__ __forceinline__ float2 crot(float2 a) {
+    constexpr int e = ((E % R) + R) % R;
+    if constexpr (e == 0) {
+        return a;
+    } else if constexpr (4 * e == R) {          // DIR * i
+        return DIR < 0 ? make_float2(a.y, -a.x) : make_float2(-a.y, a.x);
+    } else if constexpr (2 * e == R) {          // -1
+        return cneg(a);
+    } else if constexpr (4 * e == 3 * R) {      // -DIR * i
+        return DIR < 0 ? make_float2(-a.y, a.x) : make_float2(a.y, -a.x);
+    } else {
+        static_assert(32 % R == 0, "radix must divide 32");
+        constexpr int k = e * (32 / R);
+        constexpr float c = (float)cos32(k);
+        constexpr float s = (float)(DIR * sin32(k));
+        return make_float2(fmaf(a.x, c, -(a.y * s)), fmaf(a.x, s, a.y * c));
+    }
+}
+
+__host__ __device__ constexpr int ilog2c(int v) { return v <= 1 ? 0 : 1 + ilog2c(v >> 1); }
+
+__host__ __device__ constexpr int bitrev_c(int i, int bits) {
+    int r = 0;
+    for (int b = 0; b < bits; ++b) r |= ((i >> b) & 1) << (bits - 1 - b);
+    return r;
+}
+
+// In-register R-point DFT, unnormalised, sign DIR, natural order in and out:
+// v[k] <- sum_j v[j] exp(DIR*2*pi*i*j*k/R).  Radix-2 decimation in frequency over the
+// register array (every index is a compile-time constant after unrolling, so the closing
+// bit-reversal is only a renaming of registers).
+template <int R, int DIR>
+__device__ __forceinline__ void dft_reg(float2* v) {
+    constexpr int L = ilog2c(R);
+#pragma unroll
+    for (int s = 0; s < L; ++s) {
+        const int half = R >> (s + 1);
+#pragma unroll
+        for (int blk = 0; blk < R; blk += 2 * half) {
+#pragma unroll
+            for (int k = 0; k < half; ++k) {
+                float2 a = v[blk + k], b = v[blk + k + half];
+                v[blk + k] = cadd(a, b);
+                v[blk + k + half] = csub(a, b);
+            }
+        }
+        // twiddles of this DIF stage: element k of the upper half times w_{2*half}^k
+#pragma unroll
+        for (int blk = 0; blk < R; blk += 2 * half) {
+#pragma unroll
+            for (int k = 1; k < half; ++k) {
+                // exponent k/(2*half) = k*(R/(2*half))/R
+                switch (k * (R / (2 * half))) {
+#define GBFFT_ROT(EE) case EE: v[blk + k + half] = crot<DIR, EE, R>(v[blk + k + half]); break;
+                    GBFFT_ROT(1) GBFFT_ROT(2) GBFFT_ROT(3) GBFFT_ROT(4) GBFFT_ROT(5) GBFFT_ROT(6)
+                    GBFFT_ROT(7) GBFFT_ROT(8) GBFFT_ROT(9) GBFFT_ROT(10) GBFFT_ROT(11)
+                    GBFFT_ROT(12) GBFFT_ROT(13) GBFFT_ROT(14) GBFFT_ROT(15)
+#undef GBFFT_ROT
+                    default: break;
+                }
+            }
+        }
+    }
+    float2 t[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) t[i] = v[bitrev_c(i, L)];
+#pragma unroll
+    for (int i = 0; i < R; ++i) v[i] = t[i];
+}
+
+// Shared-memory index padding: one float2 of padding every 16, which makes the stride-16
+// writes of a radix-16 pass (and the stride-R writes of the smaller radices) bank-conflict
+// free for 64-bit accesses.
+__device__ __forceinline__ int spad(int i) { return i + (i >> 4); }
+__host__ __device__ constexpr int spad_size(int n) { return n + (n >> 4); }
+
+// Streaming global loads / stores (data is touched once per pass).
+__device__ __forceinline__ float2 ldg_stream(const float2* p) { return __ldcs(p); }
+__device__ __forceinline__ void stg_stream(float2* p, float2 v) { __stcs(p, v); }
+__device__ __forceinline__ float4 ldg_stream4(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ void stg_stream4(float4* p, float4 v) { __stcs(p, v); }
+
+// Flags understood by the transform kernels.
+enum : int {
+    KF_CHESS_LOAD = 1,   // multiply input element (row, j) by (-1)^j before the transform
+    KF_CHESS_STORE = 2,  // multiply output element (row, k) by (-1)^k after the transform
+    KF_CHESS_ROW = 4,    // 2-D chessboard: also multiply by (-1)^row
+};
+
+__device__ __forceinline__ float2 neg_if(float2 v, int odd) { return odd ? cneg(v) : v; }
+
+}  // namespace gbfft

@@ -1,0 +1,66 @@
+// Host-side dispatch into the kernel instantiations (one switch per kernel family), and the
+// compile-time launch geometry of every family.  Each run_* function selects the
+// instantiation for a log2 size and a direction and enqueues it on `stream`.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fft_common.cuh"
+
+namespace gbfft {
+
+// ---- launch geometry ------------------------------------------------------------------------
+// points per thread: 16 (32 from 2^12 up for the strided families, 2^14 for rows); whole
+// transform per thread below 16 points.
+__host__ __device__ constexpr int rows_log2e(int l) { return l <= 4 ? l : (l >= 14 ? 5 : 4); }
+__host__ __device__ constexpr int cols_log2e(int l) { return l <= 4 ? l : (l >= 12 ? 5 : 4); }
+
+__host__ __device__ constexpr int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+// rows per CTA of the one-pass path: at least 256 threads per CTA
+__host__ __device__ constexpr int rows_log2w(int l) {
+    return clampi(8 - (l - rows_log2e(l)), 0, 8);
+}
+// transforms per CTA of the strided families: <= 512 threads, <= 2^14 points per CTA,
+// at least `minw` transforms (coalescing width), at most 128
+__host__ __device__ constexpr int cols_log2w(int l, int log2minw) {
+    return clampi((9 - (l - cols_log2e(l))) < (14 - l) ? (9 - (l - cols_log2e(l))) : (14 - l),
+                  log2minw, 7);
+}
+// rows per CTA of the real-row path (H-point core): 256 threads, and 4 rows when the shared
+// memory allows (32-byte runs of the m-major spectrum)
+__host__ __device__ constexpr int real_log2w(int lh) {
+    return clampi(8 - (lh - rows_log2e(lh)), lh >= 13 ? 0 : (lh == 12 ? 1 : 2), 7);
+}
+
+// Largest sizes of each family.
+constexpr int kMaxLog2OnePass = 14;  // 2^14 points * 8.5 B of padded shared memory per row
+constexpr int kMaxLog2Strided = 12;  // columns of 2-D images and the four-step passes
+constexpr int kMaxLog2RealH = 14;    // real rows of up to 2^15 points
+
+// ---- dispatch -------------------------------------------------------------------------------
+// One-pass rows: nrows contiguous rows of 2^log2n points.  row_parity adds (-1)^row to the
+// chessboard (2-D row pass).
+cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t nrows,
+                     const float2* tw, int flags, int row_parity, cudaStream_t s);
+
+// Strided columns: count columns of matrices [2^log2l][2^log2s] stored back to back.
+// elem_parity: 1 for the 2-D chessboard (-1)^(row+col), 0 for the four-step one (-1)^col.
+// With hi/lo non-NULL, output k1 of column c is multiplied by w_{L*S}^{c*k1} (four-step).
+cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t count,
+                     int log2s, const float2* tw, int flags, int elem_parity, const float2* hi,
+                     const float2* lo, int lowbits, cudaStream_t s);
+
+// Four-step pass 2: count rows of 2^log2n points, row tr = k1 + N1*(tr div N1) written
+// transposed into X[k1 + N1*k2] of its 2^(log2n1+log2n)-point transform.
+cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_t count,
+                       int log2n1, const float2* tw, int flags, cudaStream_t s);
+
+// Real rows of 2^(log2h+1) points.
+cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
+                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s);
+cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
+                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s);
+
+}  // namespace gbfft

@@ -1,0 +1,202 @@
+// Band-limited real rows: analysis (R2C) and synthesis (C2R) of N = 2^(LOG2H+1) real points
+// through one H = N/2-point complex transform per row, with the two-for-one recombination
+// fused into the kernel's load (synthesis) or store (analysis) phase.
+//
+// Semantics, from "src/sht/wgsl/fourier.ts" (header comment, fftSynthWGSL / fftAnalysWGSL):
+//   analysis   F_m = sum_j x_j exp(-2*pi*i*m*j/N), m = 0..mmax, mmax < N/2;
+//   synthesis  X_0 = Re F_0, X_m = F_m, X_{N-m} = conj F_m (1 <= m <= mmax), other bins 0,
+//              x = inverse FFT of X (real), unnormalised.
+// Recombination (the N/2-point real-FFT path of the same file):
+//   analysis   z_m = x_{2m} + i x_{2m+1}, Z = FFT_H(z),
+//              X_k = (Z_k + conj Z_{H-k})/2 - i e^{-2 pi i k/N} (Z_k - conj Z_{H-k})/2;
+//   synthesis  Z_k = (X_k + conj X_{H-k}) + i e^{+2 pi i k/N} (X_k - conj X_{H-k}),
+//              z = inverse FFT_H(Z), x_{2m} = Re z_m, x_{2m+1} = Im z_m,
+// with Z_H = Z_0 and X_H = 0 (no Nyquist bin since mmax < N/2).
+#pragma once
+
+#include "fft_kernel.cuh"
+
+namespace gbfft {
+
+template <class C>
+struct RealCfg {
+    // per-row shared memory: the exchange buffer, or H+1 padded slots for the recombination
+    static constexpr int SREAL = (C::SROW > spad_size(C::N) + 1) ? C::SROW : spad_size(C::N) + 1;
+    static constexpr size_t SMEM_BYTES = (size_t)SREAL * C::W * sizeof(float2);
+};
+
+// R2C: in = real rows [nrows][2H] float32, out = spectrum (row-major [nrows][mmax+1] or
+// m-major [mmax+1][nrows]).  twr[k] = (cos, sin)(2*pi*k/N), k < H.
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    k_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
+          const float2* __restrict__ tw, const float2* __restrict__ twr) {
+    static_assert(C::TFAST, "real kernels keep each row's threads adjacent");
+    constexpr int H = C::N;
+    constexpr int SREAL = RealCfg<C>::SREAL;
+    extern __shared__ float2 smem[];
+    const int w = (int)threadIdx.x / C::T;
+    const int t = (int)threadIdx.x % C::T;
+    const int64_t row = (int64_t)blockIdx.x * C::W + w;
+    const bool active = row < nrows;
+    float2* sb = smem + w * SREAL;
+
+    constexpr int R0 = C::radix(0);
+    constexpr int B0 = C::E / R0;
+    constexpr int S0 = C::N / R0;
+    float2 v[C::E];
+    const float2* src = reinterpret_cast<const float2*>(in) + (active ? row * H : 0);
+#pragma unroll
+    for (int b = 0; b < B0; ++b) {
+        const int j = t + b * C::T;
+#pragma unroll
+        for (int r = 0; r < R0; ++r)
+            v[b * R0 + r] = active ? ldg_stream(src + j + r * S0) : make_float2(0.f, 0.f);
+    }
+    run_passes<C, -1, 0>(v, t, sb, tw);
+
+    constexpr int RL = C::radix(C::NPASS - 1);
+    constexpr int BL = C::E / RL;
+    constexpr int SL = C::N / RL;
+    if constexpr (C::NPASS > 1) __syncthreads();  // last exchange fully read
+#pragma unroll
+    for (int b = 0; b < BL; ++b) {
+        const int j = t + b * C::T;
+#pragma unroll
+        for (int r = 0; r < RL; ++r) sb[spad(j + r * SL)] = v[b * RL + r];
+    }
+    __syncthreads();
+
+    // X_k for k <= mmax; row-major: each row's threads walk k; m-major: the W rows of the CTA
+    // are adjacent lanes so that consecutive rows of one coefficient are written together.
+    const int total = C::W * (mmax + 1);
+    for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
+        int wr, k;
+        if (mmajor) {
+            wr = i % C::W;
+            k = i / C::W;
+        } else {
+            wr = i / (mmax + 1);
+            k = i % (mmax + 1);
+        }
+        const int64_t rr = (int64_t)blockIdx.x * C::W + wr;
+        if (rr >= nrows) continue;
+        const float2* s = smem + wr * SREAL;
+        const float2 zk = s[spad(k)];
+        const float2 zm = s[spad((H - k) & (H - 1))];
+        const float2 zc = make_float2(zm.x, -zm.y);                   // conj Z_{H-k}
+        const float2 xe = make_float2(0.5f * (zk.x + zc.x), 0.5f * (zk.y + zc.y));
+        const float2 d = make_float2(0.5f * (zk.x - zc.x), 0.5f * (zk.y - zc.y));
+        const float2 xo = make_float2(d.y, -d.x);                     // -i * d
+        const float2 wk = __ldg(twr + k);
+        const float2 y = cadd(xe, ctw<-1>(xo, wk));                   // xe + e^{-i th} xo
+        const int64_t o = mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k;
+        stg_stream(out + o, y);
+    }
+}
+
+// C2R: in = spectrum (layout as above), out = real rows [nrows][2H] float32.
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    k_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
+          const float2* __restrict__ tw, const float2* __restrict__ twr) {
+    static_assert(C::TFAST, "real kernels keep each row's threads adjacent");
+    constexpr int H = C::N;
+    constexpr int SREAL = RealCfg<C>::SREAL;
+    extern __shared__ float2 smem[];
+    const int w = (int)threadIdx.x / C::T;
+    const int t = (int)threadIdx.x % C::T;
+    const int64_t row = (int64_t)blockIdx.x * C::W + w;
+    const bool active = row < nrows;
+    float2* sb = smem + w * SREAL;
+
+    // gather X_0..X_H into shared memory (X_0 = Re F_0, zero above mmax, X_H = 0)
+    const int total = C::W * (H + 1);
+    for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
+        int wr, k;
+        if (mmajor) {
+            wr = i % C::W;
+            k = i / C::W;
+        } else {
+            wr = i / (H + 1);
+            k = i % (H + 1);
+        }
+        const int64_t rr = (int64_t)blockIdx.x * C::W + wr;
+        float2 x = make_float2(0.f, 0.f);
+        if (rr < nrows && k <= mmax) {
+            x = ldg_stream(in + (mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k));
+            if (k == 0) x.y = 0.f;
+        }
+        smem[wr * SREAL + spad(k)] = x;
+    }
+    __syncthreads();
+
+    constexpr int R0 = C::radix(0);
+    constexpr int B0 = C::E / R0;
+    constexpr int S0 = C::N / R0;
+    float2 v[C::E];
+#pragma unroll
+    for (int b = 0; b < B0; ++b) {
+        const int j = t + b * C::T;
+#pragma unroll
+        for (int r = 0; r < R0; ++r) {
+            const int k = j + r * S0;
+            const float2 xk = sb[spad(k)];
+            const float2 xm = sb[spad(H - k)];
+            const float2 xc = make_float2(xm.x, -xm.y);             // conj X_{H-k}
+            const float2 s = cadd(xk, xc);
+            const float2 wd = ctw<+1>(csub(xk, xc), __ldg(twr + k));  // e^{+i th} (X_k - conj X_{H-k})
+            v[b * R0 + r] = make_float2(s.x - wd.y, s.y + wd.x);     // s + i * wd
+        }
+    }
+    __syncthreads();  // the exchange buffer aliases the gathered spectrum
+
+    run_passes<C, +1, 0>(v, t, sb, tw);
+
+    constexpr int RL = C::radix(C::NPASS - 1);
+    constexpr int BL = C::E / RL;
+    constexpr int SL = C::N / RL;
+    if (active) {
+        float2* dst = reinterpret_cast<float2*>(out) + row * H;
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < RL; ++r) stg_stream(dst + j + r * SL, v[b * RL + r]);
+        }
+    }
+}
+
+template <class C>
+cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
+                       const float2* tw, const float2* twr, cudaStream_t stream) {
+    auto kern = k_r2c<C>;
+    constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t grid = (nrows + C::W - 1) / C::W;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr);
+    return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
+                       const float2* tw, const float2* twr, cudaStream_t stream) {
+    auto kern = k_c2r<C>;
+    constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
+    if (smem > 48 * 1024) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t grid = (nrows + C::W - 1) / C::W;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr);
+    return cudaGetLastError();
+}
+
+}  // namespace gbfft

@@ -1,0 +1,170 @@
+/*
+ * gbfft.h - C ABI of the batched fp32 FFT library for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The library computes, for power-of-two n,
+ *
+ *     X_k = sum_{j<n} x_j * exp(s * 2*pi*i * j*k / n),   s = -1 forward, s = +1 inverse,
+ *
+ * on batches of contiguous rows (dims = 1) or n x n images (dims = 2, row-column: all rows,
+ * then all columns), with no 1/n scaling in either direction.  This is the discrete Fourier
+ * transform of Mota, "High Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5, with
+ * the sign convention of its Eq. 5 / Algorithm 2 and the unnormalised inverse of the WGSL
+ * Stockham kernels in "src/sht/wgsl/fourier.ts"; the 2-D form is Mota §2.7 Eq. 19.
+ *
+ * Data types: complex data are complex64, interleaved (re, im) float32 pairs, 8 bytes per
+ * point; real rows are float32.  All pointers passed to exec calls are DEVICE pointers owned by
+ * the caller, contiguous and 16-byte aligned.  The stream argument is a cudaStream_t passed as
+ * void* (NULL = the legacy default stream).  Exec calls are asynchronous on that stream: they
+ * validate their arguments on the host, enqueue kernels and return; they never synchronise.
+ *
+ * Errors: every function returns FFT_OK (0) or a negative status.  Argument errors are
+ * detected on the host before anything is enqueued.  There is no CPU fallback: if the device
+ * or the kernels are unavailable the call fails with FFT_ERR_CUDA.
+ *
+ * Thread-safety: distinct plans may be used concurrently.  One plan must not be executed on
+ * two streams at the same time (its workspace is shared by its executions).
+ */
+#ifndef GBFFT_H
+#define GBFFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gbfft_plan_s* fft_plan; /* opaque; created and freed by the library */
+
+/* Direction = sign s of the exponent (Mota §2.3.1 Algorithm 2 and its inverse remark). */
+enum { FFT_FORWARD = -1, FFT_INVERSE = +1 };
+
+/* Data layouts.
+ * FFT_LAYOUT_C2C          complex rows [batch][n] (dims 1) or images [batch][n][n] (dims 2).
+ * FFT_LAYOUT_REAL_ROWMAJOR real rows [batch][n] float32 <-> spectrum [batch][mmax+1] complex64.
+ * FFT_LAYOUT_REAL_MMAJOR   real rows [batch][n] float32 <-> spectrum [mmax+1][batch] complex64,
+ *                          i.e. coefficient m of row r at index m*batch + r, the fm[m*NLAT+ilat]
+ *                          layout of fourier.ts (fftSynthWGSL / fftAnalysWGSL). */
+enum { FFT_LAYOUT_C2C = 0, FFT_LAYOUT_REAL_ROWMAJOR = 1, FFT_LAYOUT_REAL_MMAJOR = 2 };
+
+/* Status codes. */
+enum {
+    FFT_OK = 0,
+    FFT_ERR_INVALID_ARG = -1,      /* NULL pointer, bad enum, batch < 1, wrong exec kind,
+                                      shift with a real layout, band limit out of range */
+    FFT_ERR_UNSUPPORTED_SIZE = -2, /* n not a power of two, or above the maximum */
+    FFT_ERR_MISALIGNED = -3,       /* a data pointer is not 16-byte aligned */
+    FFT_ERR_OOM = -4,              /* device allocation of tables or workspace failed */
+    FFT_ERR_CUDA = -5,             /* a CUDA runtime call or kernel launch failed */
+    FFT_ERR_TIMEOUT = -6           /* a bounded device-side wait gave up (fft_plan_check) */
+};
+
+/* Largest supported transform sizes. */
+#define FFT_MAX_LOG2N_1D 24 /* n <= 2^24 for dims = 1 (complex and real rows) */
+#define FFT_MAX_LOG2N_2D 12 /* n <= 2^12 per side for dims = 2 */
+
+/*
+ * fft_plan_create - plan a batched transform on the current CUDA device.
+ *   n         transform length (dims 1) or image side (dims 2); power of two,
+ *             1 <= n <= 2^24 (dims 1, complex), 4 <= n <= 2^24 (real layouts),
+ *             2 <= n <= 2^12 (dims 2).
+ *   batch     number of rows (dims 1) or images (dims 2), >= 1.
+ *   dims      1 or 2 (2 only with FFT_LAYOUT_C2C).
+ *   direction FFT_FORWARD or FFT_INVERSE.  Real layouts: FORWARD = analysis (R2C, exec with
+ *             fft_exec_r2c), INVERSE = synthesis (C2R, exec with fft_exec_c2r).
+ *   layout    FFT_LAYOUT_*.
+ *   shift     0 or 1; C2C only, n even.  Forward: the input is pre-multiplied by the chessboard
+ *             (-1)^j (dims 1) or (-1)^(row+col) (dims 2), which for even n makes the output
+ *             fftshift(X) ("The 1D fftshift in CUDA by chessboard multiplication", the
+ *             chessboard section).  Inverse: the output is post-multiplied by the same
+ *             chessboard, so inverse-shift(forward-shift(x)) = n*x (dims 1) or n^2*x (dims 2).
+ *   out       receives the plan.
+ * The plan allocates its device twiddle tables, its workspace (large 1-D sizes only) and a
+ * device error word with cudaMalloc on the current device, and copies the tables (computed on
+ * the host in double precision and rounded once to float) synchronously.
+ * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_UNSUPPORTED_SIZE, FFT_ERR_OOM or FFT_ERR_CUDA;
+ * on error *out is set to NULL and nothing is left allocated.
+ */
+int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layout, int shift,
+                    fft_plan* out);
+
+/*
+ * fft_plan_set_band_limit - set mmax for a real-layout plan: the analysis keeps m = 0..mmax,
+ * the synthesis reads F_0..F_mmax and assembles the Hermitian spectrum X_0 = Re F_0,
+ * X_m = F_m, X_{n-m} = conj F_m (fourier.ts header comment and fftSynthWGSL).  Requires
+ * 0 <= mmax < n/2 (no Nyquist bin).  The default is n/2 - 1.  Host only.
+ * Returns FFT_OK or FFT_ERR_INVALID_ARG (NULL plan, C2C plan, mmax out of range).
+ */
+int fft_plan_set_band_limit(fft_plan plan, int64_t mmax);
+
+/* fft_plan_workspace_bytes - device bytes the plan holds besides its twiddle tables
+ * (informational).  Returns FFT_OK or FFT_ERR_INVALID_ARG. */
+int fft_plan_workspace_bytes(fft_plan plan, size_t* bytes);
+
+/*
+ * fft_plan_describe - write a one-line, NUL-terminated description of the plan's execution
+ * path (kernels, radix sequence, launch geometry) into buf (at most len bytes).  Host only.
+ * Returns FFT_OK or FFT_ERR_INVALID_ARG.
+ */
+int fft_plan_describe(fft_plan plan, char* buf, size_t len);
+
+/*
+ * fft_plan_query - host-only planning: describe the path fft_plan_create would choose for
+ * these parameters, without touching any device.  Same validation and return codes as
+ * fft_plan_create (minus the device errors).  buf may be NULL when len is 0.
+ */
+int fft_plan_query(int64_t n, int64_t batch, int dims, int direction, int layout, int shift,
+                   char* buf, size_t len);
+
+/*
+ * fft_exec_c2c - run a C2C plan: out = transform(in).
+ *   in, out  device pointers to batch*n (dims 1) or batch*n*n (dims 2) complex64 values;
+ *            in == out (in place) is allowed; otherwise the ranges must not overlap.
+ *   stream   cudaStream_t as void*.
+ * Returns FFT_OK, FFT_ERR_INVALID_ARG (NULL, real-layout plan), FFT_ERR_MISALIGNED or
+ * FFT_ERR_CUDA (launch failure).  Device faults surface at the caller's next synchronisation.
+ */
+int fft_exec_c2c(fft_plan plan, const void* in, void* out, void* stream);
+
+/*
+ * fft_exec_r2c - run a FORWARD real-layout plan (band-limited analysis, fftAnalysWGSL):
+ * F_m = sum_j x_j exp(-2*pi*i*m*j/n), m = 0..mmax, for every row.
+ *   in   device float32 [batch][n];  out  device complex64 spectrum in the plan's layout.
+ *   in and out must not overlap.
+ * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_MISALIGNED or FFT_ERR_CUDA.
+ */
+int fft_exec_r2c(fft_plan plan, const float* in, void* out, void* stream);
+
+/*
+ * fft_exec_c2r - run an INVERSE real-layout plan (band-limited synthesis, fftSynthWGSL):
+ * x_j = Re F_0 + 2 * sum_{m=1}^{mmax} Re(F_m exp(+2*pi*i*m*j/n)), for every row (Im F_0 is
+ * ignored).
+ *   in   device complex64 spectrum in the plan's layout;  out  device float32 [batch][n].
+ *   in and out must not overlap.
+ * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_MISALIGNED or FFT_ERR_CUDA.
+ */
+int fft_exec_c2r(fft_plan plan, const void* in, float* out, void* stream);
+
+/*
+ * fft_plan_check - synchronise the device, then read and clear the plan's device error word.
+ * Kernels that wait on device-side events give up after a bounded number of polls and set
+ * this word instead of hanging.  Returns FFT_OK, FFT_ERR_TIMEOUT, FFT_ERR_INVALID_ARG or
+ * FFT_ERR_CUDA (the synchronisation itself reported an error).
+ */
+int fft_plan_check(fft_plan plan);
+
+/* fft_plan_destroy - free the plan and its device memory (synchronises the device first).
+ * NULL is accepted and ignored.  Returns FFT_OK or FFT_ERR_CUDA. */
+int fft_plan_destroy(fft_plan plan);
+
+/* fft_status_string - static description of a status code (never NULL). */
+const char* fft_status_string(int status);
+
+/* fft_version - library version as major*10000 + minor*100 + patch. */
+int fft_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBFFT_H */

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every function
+declared in include/gbfft.h, and the planner validates its arguments and picks its paths."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fft_signal_processing_gb300 as fx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbfft.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from fft_signal_processing_gb300 import _build
+
+    _build.build()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fft_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(fx.ABI_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(fx.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version():
+    for st in (0, -1, -2, -3, -4, -5, -6):
+        assert fx.status_string(st).startswith("FFT_")
+    assert fx.status_string(-99) == "unknown status"
+    assert fx.lib().fft_version() >= 10000
+
+
+def test_destroy_null_is_ok():
+    assert fx.lib().fft_plan_destroy(None) == fx.FFT_OK
+
+
+def q(n, batch=1, dims=1, direction=-1, layout=0, shift=0):
+    return fx.lib().fft_plan_query(n, batch, dims, direction, layout, shift, None, 0)
+
+
+@pytest.mark.parametrize("n", [3, 6, 1000, 0, -4])
+def test_non_power_of_two_rejected(n):
+    assert q(n) == fx.FFT_ERR_UNSUPPORTED_SIZE
+
+
+def test_size_limits():
+    assert q(1 << 24) == fx.FFT_OK
+    assert q(1 << 25) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert q(1 << 12, dims=2) == fx.FFT_OK
+    assert q(1 << 13, dims=2) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert q(1, dims=2) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert q(1 << 15, layout=1) == fx.FFT_OK
+    assert q(1 << 16, layout=1) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert q(2, layout=1) == fx.FFT_ERR_UNSUPPORTED_SIZE
+
+
+@pytest.mark.parametrize("args", [
+    dict(batch=0), dict(batch=-1), dict(dims=3), dict(direction=0), dict(direction=2),
+    dict(layout=3), dict(shift=2), dict(layout=1, shift=1), dict(layout=2, dims=2),
+])
+def test_invalid_arguments(args):
+    assert q(64, **args) == fx.FFT_ERR_INVALID_ARG
+
+
+def test_shift_needs_even_n():
+    assert q(1, shift=1) == fx.FFT_ERR_INVALID_ARG
+    assert q(2, shift=1) == fx.FFT_OK
+
+
+def test_batch_overflow_rejected():
+    assert q(1 << 20, batch=1 << 40) == fx.FFT_ERR_UNSUPPORTED_SIZE
+
+
+def test_create_rejects_before_touching_the_device():
+    h = ctypes.c_void_p(1)
+    rc = fx.lib().fft_plan_create(6, 1, 1, -1, 0, 0, ctypes.byref(h))
+    assert rc == fx.FFT_ERR_UNSUPPORTED_SIZE and not h.value
+    assert fx.lib().fft_plan_create(8, 1, 1, -1, 0, 0, None) == fx.FFT_ERR_INVALID_ARG
+
+
+def test_null_plan_calls():
+    L = fx.lib()
+    assert L.fft_plan_set_band_limit(None, 1) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_plan_workspace_bytes(None, None) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_plan_describe(None, None, 0) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_exec_c2c(None, None, None, None) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_exec_r2c(None, None, None, None) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_exec_c2r(None, None, None, None) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_plan_check(None) == fx.FFT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n,path,radix", [
+    (1, "onepass", "1"), (16, "onepass", "16"), (1024, "onepass", "16x16x4"),
+    (4096, "onepass", "16x16x16"), (8192, "onepass", "16x16x16x2"),
+    (1 << 14, "onepass", "16x16x16x4"), (1 << 15, "fourstep", None), (1 << 24, "fourstep", None),
+])
+def test_path_choice(n, path, radix):
+    d = fx.query(n, 4)
+    assert f"path={path}" in d
+    if radix:
+        assert f"radix={radix} " in d
+    if path == "fourstep":
+        l = n.bit_length() - 1
+        assert f"n1={1 << (l // 2)} n2={1 << (l - l // 2)}" in d
+
+
+def test_2d_and_real_paths():
+    assert "path=2d" in fx.query(4096, 1, dims=2, shift=True)
+    d = fx.query(4096, 2048, layout=2, direction=1)
+    assert "path=real" in d and "core=2048" in d and "mmajor" in d

@@ -1,0 +1,166 @@
+"""GPU parity of the band-limited real-row path (R2C analysis / C2R synthesis, row-major and
+m-major spectra) and of the 2-D path, against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def fx():
+    import fft_signal_processing_gb300 as m
+
+    return m
+
+
+def wl():
+    from fft_signal_processing_gb300 import workloads
+
+    return workloads
+
+
+LAYOUTS = {"rowmajor": 1, "mmajor": 2}
+
+
+def gpu_c2r(F_rowmajor, n, mmax, layout):
+    m = fx()
+    rows = F_rowmajor.shape[0]
+    p = m.Plan(n, rows, 1, m.INVERSE, layout=LAYOUTS[layout], mmax=mmax)
+    Fin = oracle.to_mmajor(F_rowmajor) if layout == "mmajor" else F_rowmajor
+    Fd = torch.from_numpy(np.ascontiguousarray(Fin, dtype=np.complex64)).cuda()
+    x = p.c2r(Fd)
+    torch.cuda.synchronize()
+    return x.cpu().numpy()
+
+
+def gpu_r2c(x, mmax, layout):
+    m = fx()
+    rows, n = x.shape
+    p = m.Plan(n, rows, 1, m.FORWARD, layout=LAYOUTS[layout], mmax=mmax)
+    F = p.r2c(torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda())
+    torch.cuda.synchronize()
+    F = F.cpu().numpy()
+    return oracle.from_mmajor(F) if layout == "mmajor" else F
+
+
+def mmax_cases(n):
+    h = n // 2
+    return sorted({0, h - 1, max(0, h // 3), max(0, (2 * h) // 3)})
+
+
+@pytest.mark.parametrize("log2n", list(range(2, 16)))
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+def test_c2r_grid(log2n, layout):
+    n = 1 << log2n
+    for mmax in mmax_cases(n):
+        rows = 67 if n <= 4096 else 5
+        F = wl().spectrum(100 + log2n, rows, mmax)
+        got = gpu_c2r(F, n, mmax, layout)
+        assert_parity(got, oracle.c2r(F, n), n, f"c2r n={n} mmax={mmax} {layout}")
+
+
+@pytest.mark.parametrize("log2n", list(range(2, 16)))
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+def test_r2c_grid(log2n, layout):
+    n = 1 << log2n
+    for mmax in mmax_cases(n):
+        rows = 67 if n <= 4096 else 5
+        x = wl().real_normal(200 + log2n, rows, n)
+        got = gpu_r2c(x, mmax, layout)
+        ref = oracle.r2c(x, mmax)
+        # per-row error scale: the RMS of the row's full spectrum, ||x_row||_2 (Parseval),
+        # since few bins may be kept
+        assert_parity(got, ref, mmax + 1, f"r2c n={n} mmax={mmax} {layout}",
+                      scale=np.linalg.norm(x.astype(np.float64), axis=1))
+
+
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+def test_real_n4_bit_exact(layout):
+    """n = 4: every twiddle is 0 or +-1 and every product exact, so the Hermitian assembly,
+    the two-for-one recombination and the spectrum layout must match bit for bit."""
+    rng = np.random.default_rng(7)
+    rows, n, mmax = 131, 4, 1
+    F = (rng.integers(-8, 8, (rows, 2)) + 1j * rng.integers(-8, 8, (rows, 2))).astype(np.complex64)
+    x = gpu_c2r(F, n, mmax, layout)
+    ref = oracle.c2r(F, n)
+    np.testing.assert_array_equal(x.astype(np.float64), np.round(ref))
+    xr = rng.integers(-8, 8, (rows, n)).astype(np.float32)
+    G = gpu_r2c(xr, mmax, layout)
+    refG = oracle.r2c(xr, mmax)
+    np.testing.assert_array_equal(G.astype(np.complex128),
+                                  np.round(refG.real) + 1j * np.round(refG.imag))
+
+
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+def test_real_roundtrip(layout):
+    n, rows, mmax = 1024, 33, 341
+    F = wl().spectrum(300, rows, mmax)
+    x = gpu_c2r(F, n, mmax, layout)
+    G = gpu_r2c(x, mmax, layout)
+    ref = oracle.r2c(oracle.c2r(F, n), mmax)  # the fp64 round trip of F
+    assert_parity(G, ref, mmax + 1, f"real round trip {layout}")
+
+
+def test_real_argument_errors():
+    m = fx()
+    p = m.Plan(64, 4, 1, m.FORWARD, layout=1)
+    assert p.mmax == 31
+    L = m.lib()
+    assert L.fft_plan_set_band_limit(p.handle, 32) == m.FFT_ERR_INVALID_ARG
+    assert L.fft_plan_set_band_limit(p.handle, -1) == m.FFT_ERR_INVALID_ARG
+    x = torch.zeros((4, 64), dtype=torch.float32, device="cuda")
+    import ctypes
+
+    vp = ctypes.c_void_p
+    assert L.fft_exec_c2r(p.handle, vp(x.data_ptr()), vp(x.data_ptr()), vp(0)) == \
+        m.FFT_ERR_INVALID_ARG  # forward plan run as synthesis
+    assert L.fft_exec_r2c(p.handle, vp(x.data_ptr()), vp(x.data_ptr()), vp(0)) == \
+        m.FFT_ERR_INVALID_ARG  # in and out overlap
+    assert L.fft_exec_c2c(p.handle, vp(x.data_ptr()), vp(x.data_ptr()), vp(0)) == \
+        m.FFT_ERR_INVALID_ARG
+
+
+# ---- 2-D -------------------------------------------------------------------------------------
+def gpu_2d(img, direction, shift, inplace=False):
+    m = fx()
+    batch, n, _ = img.shape
+    p = m.Plan(n, batch, 2, direction, shift=shift)
+    xd = torch.from_numpy(np.ascontiguousarray(img, dtype=np.complex64)).cuda()
+    y = p.c2c(xd, out=xd) if inplace else p.c2c(xd)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("log2n", list(range(1, 13)))
+@pytest.mark.parametrize("direction", [-1, 1])
+@pytest.mark.parametrize("shift", [False, True])
+def test_2d_grid(log2n, direction, shift):
+    n = 1 << log2n
+    batch = 3 if n <= 512 else 1
+    img = wl().image(400 + log2n, batch, n)
+    got = gpu_2d(img, direction, shift, inplace=(log2n % 2 == 0))
+    assert_parity(got, oracle.transform(img, direction, 2, shift), n * n,
+                  f"2d n={n} dir={direction} shift={shift}")
+
+
+def test_2d_small_integer_bit_exact():
+    rng = np.random.default_rng(11)
+    for n in (2, 4):
+        img = (rng.integers(-4, 4, (7, n, n)) + 1j * rng.integers(-4, 4, (7, n, n))).astype(np.complex64)
+        for direction in (-1, 1):
+            for shift in (False, True):
+                got = gpu_2d(img, direction, shift)
+                ref = oracle.transform(img, direction, 2, shift)
+                exact = np.round(ref.real) + 1j * np.round(ref.imag)
+                np.testing.assert_array_equal(got.astype(np.complex128), exact)
