@@ -33,6 +33,7 @@ ABI_SYMBOLS = (
     "fft_plan_create", "fft_plan_set_band_limit", "fft_plan_workspace_bytes",
     "fft_plan_describe", "fft_plan_query", "fft_exec_c2c", "fft_exec_r2c", "fft_exec_c2r",
     "fft_plan_check", "fft_plan_destroy", "fft_status_string", "fft_version",
+    "fft_exec_c2c_noalloc",
 )
 
 _LIB = None
@@ -67,6 +68,7 @@ def lib():
         L.fft_status_string.argtypes = [ci]
         L.fft_status_string.restype = ctypes.c_char_p
         L.fft_version.argtypes = []
+        L.fft_exec_c2c_noalloc.argtypes = [i64, i64, ci, ci, vp, vp, vp]
         for name in ABI_SYMBOLS:
             if name != "fft_status_string":
                 getattr(L, name).restype = ci
@@ -89,6 +91,13 @@ def query(n, batch, dims=1, direction=FORWARD, layout=LAYOUT_C2C, shift=False) -
     _check(lib().fft_plan_query(int(n), int(batch), int(dims), int(direction), int(layout),
                                 int(bool(shift)), buf, len(buf)), "fft_plan_query")
     return buf.value.decode()
+
+
+def exec_c2c_noalloc(n, batch, direction, shift, in_ptr, out_ptr, stream_ptr=0):
+    """Allocation-free batched C2C transform on raw device pointers (fft_exec_c2c_noalloc)."""
+    _check(lib().fft_exec_c2c_noalloc(int(n), int(batch), int(direction), int(bool(shift)),
+                                      ctypes.c_void_p(in_ptr), ctypes.c_void_p(out_ptr),
+                                      ctypes.c_void_p(stream_ptr)), "fft_exec_c2c_noalloc")
 
 
 def _stream_ptr(stream):

@@ -1,0 +1,178 @@
+// fft_exec_c2c_noalloc: the large-n (four-step) batched C2C transform for callers that must not
+// allocate device memory.  Its intermediate buffer and its twiddle tables live in file-scope
+// __device__ arrays of fixed size instead of cudaMalloc'ed plan memory, so the call itself
+// allocates nothing.  See include/gbfft.h for the contract.
+//
+// The transform is the library's four-step path (the same two kernels as a plan of the same
+// size): n = N1*N2 with N1 = 2^(l/2) and N2 = 2^(l - l/2); pass 1 writes N1-point column
+// transforms times w_n^{n2*k1} into the scratch array, pass 2 reads it and writes the N2-point
+// row transforms transposed into the output.  Pass 1 overwrites every scratch element that pass
+// 2 reads, so the scratch never needs clearing between calls.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gbfft.h"
+#include "fft_kernel.cuh"
+#include "kernels.h"
+
+using namespace gbfft;
+
+static constexpr int kNoAllocMinLog2 = 15;  // below this the one-pass path needs no scratch
+static constexpr int kNoAllocMaxLog2 = 21;
+static constexpr int64_t kScratchPoints = int64_t(1) << 21;  // complex64 points: 16 MiB
+static constexpr int kTableFloat2 = 1 << 16;                 // 512 KiB of twiddles, all sizes
+
+// Every GPU that loads this module holds these until the process exits.
+static __device__ __align__(256) float2 g_scratch[kScratchPoints];
+static __device__ __align__(256) float2 g_tables[kTableFloat2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool ready = false;
+    float2* scratch = nullptr;  // device address of g_scratch on this device
+    float2* tables = nullptr;   // device address of g_tables on this device
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+// Offsets (in float2) into g_tables of each size's sub-tables.
+struct SizeTables {
+    size_t col = 0, row = 0, hi = 0, lo = 0;
+};
+SizeTables g_off[kNoAllocMaxLog2 + 1];
+
+const double kTwoPi = 6.283185307179586476925286766559005768;
+
+// (cos, sin)(2*pi*q/m) in double, reduced in integers to the first quadrant (quarter turns
+// exact), rounded once to float -- the same values the plan path's tables hold.
+float2 unit_root(int64_t q, int64_t m) {
+    q %= m;
+    if (q < 0) q += m;
+    if (m % 4 != 0) return make_float2(2 * q == m ? -1.f : 1.f, 0.f);
+    const int64_t qq = m / 4, quad = q / qq, a = q % qq;
+    double c, s;
+    if (a == 0) {
+        c = 1.0;
+        s = 0.0;
+    } else if (a <= qq / 2) {
+        c = std::cos(kTwoPi * (double)a / (double)m);
+        s = std::sin(kTwoPi * (double)a / (double)m);
+    } else {
+        c = std::sin(kTwoPi * (double)(qq - a) / (double)m);
+        s = std::cos(kTwoPi * (double)(qq - a) / (double)m);
+    }
+    double x, y;
+    switch (quad & 3) {
+        case 0: x = c; y = s; break;
+        case 1: x = -s; y = c; break;
+        case 2: x = -c; y = -s; break;
+        default: x = s; y = -c; break;
+    }
+    return make_float2((float)x, (float)y);
+}
+
+void pad32(std::vector<float2>& v) {
+    while (v.size() % 32) v.push_back(make_float2(0.f, 0.f));
+}
+
+size_t pass_tables(std::vector<float2>& v, int l) {
+    pad32(v);
+    const size_t off = v.size();
+    const int npass = l <= 4 ? 1 : (l + 3) / 4;
+    for (int p = 1; p < npass; ++p) {
+        const int rb = (l - 4 * p >= 4) ? 4 : l - 4 * p;
+        const int64_t R = int64_t(1) << rb, Ns = int64_t(1) << (4 * p);
+        for (int64_t m = 0; m < Ns; ++m)
+            for (int64_t r = 0; r < R; ++r) v.push_back(unit_root(m * r, Ns * R));
+    }
+    return off;
+}
+
+size_t roots(std::vector<float2>& v, int64_t count, int64_t step, int64_t m) {
+    pad32(v);
+    const size_t off = v.size();
+    for (int64_t q = 0; q < count; ++q) v.push_back(unit_root(q * step, m));
+    return off;
+}
+
+// Host tables of every supported size, laid out once (identical on every device).
+const std::vector<float2>& host_tables() {
+    static std::vector<float2> v;
+    static bool built = false;
+    if (!built) {
+        for (int l = kNoAllocMinLog2; l <= kNoAllocMaxLog2; ++l) {
+            const int l1 = l / 2, l2 = l - l / 2, lowbits = (l + 1) / 2;
+            g_off[l].col = pass_tables(v, l1);
+            g_off[l].row = pass_tables(v, l2);
+            g_off[l].hi = roots(v, int64_t(1) << (l - lowbits), int64_t(1) << lowbits,
+                                int64_t(1) << l);
+            g_off[l].lo = roots(v, int64_t(1) << lowbits, 1, int64_t(1) << l);
+        }
+        pad32(v);
+        built = true;
+    }
+    return v;
+}
+
+// Once per device, with that device current: resolve the arrays' device addresses (host code
+// must not use the array symbols themselves as pointers) and upload the twiddle tables.
+int setup_device(int dev, DeviceState** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        const std::vector<float2>& t = host_tables();
+        if (t.size() > (size_t)kTableFloat2) return FFT_ERR_UNSUPPORTED_SIZE;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) return FFT_ERR_CUDA;
+        st.scratch = (float2*)p;
+        if (cudaGetSymbolAddress(&p, g_tables) != cudaSuccess) return FFT_ERR_CUDA;
+        st.tables = (float2*)p;
+        if (cudaMemcpy(st.tables, t.data(), t.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+            cudaSuccess)
+            return FFT_ERR_CUDA;
+        st.ready = true;
+    }
+    *out = &st;
+    return FFT_OK;
+}
+
+}  // namespace
+
+extern "C" int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int shift,
+                                    const void* in, void* out, void* stream) {
+    if (!in || !out || batch < 1) return FFT_ERR_INVALID_ARG;
+    if (direction != FFT_FORWARD && direction != FFT_INVERSE) return FFT_ERR_INVALID_ARG;
+    if (shift != 0 && shift != 1) return FFT_ERR_INVALID_ARG;
+    if (n < 1 || (n & (n - 1))) return FFT_ERR_UNSUPPORTED_SIZE;
+    int l = 0;
+    while ((int64_t(1) << l) < n) ++l;
+    if (l < kNoAllocMinLog2 || l > kNoAllocMaxLog2) return FFT_ERR_UNSUPPORTED_SIZE;
+    if (batch > kScratchPoints / n) return FFT_ERR_UNSUPPORTED_SIZE;  // scratch capacity
+    if (((uintptr_t)in & 15u) || ((uintptr_t)out & 15u)) return FFT_ERR_MISALIGNED;
+    const size_t bytes = (size_t)batch * (size_t)n * sizeof(float2);
+    const uintptr_t a = (uintptr_t)in, b = (uintptr_t)out;
+    if (in != out && a < b + bytes && b < a + bytes) return FFT_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FFT_ERR_CUDA;
+    DeviceState* st = nullptr;
+    const int rc = setup_device(dev, &st);
+    if (rc != FFT_OK) return rc;
+
+    const int l1 = l / 2, l2 = l - l / 2, lowbits = (l + 1) / 2;
+    const SizeTables& o = g_off[l];
+    const bool fwd = direction == FFT_FORWARD;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = run_cols(l1, direction, (const float2*)in, st->scratch, batch << l2, l2,
+                             st->tables + o.col, (shift && fwd) ? KF_CHESS_LOAD : 0, 0,
+                             st->tables + o.hi, st->tables + o.lo, lowbits, s);
+    if (e == cudaSuccess)
+        e = run_rows_t(l2, direction, st->scratch, (float2*)out, batch << l1, l1,
+                       st->tables + o.row, (shift && !fwd) ? KF_CHESS_STORE : 0, s);
+    return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
+}

@@ -157,6 +157,37 @@ int fft_plan_check(fft_plan plan);
  * NULL is accepted and ignored.  Returns FFT_OK or FFT_ERR_CUDA. */
 int fft_plan_destroy(fft_plan plan);
 
+/*
+ * fft_exec_c2c_noalloc - the batched 1-D C2C transform for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this call; it exists for integration.
+ *
+ * Some callers may not call cudaMalloc at all: code running inside a host application or
+ * framework that owns every byte of device memory through its own allocator and forbids
+ * direct allocation, and latency-bound processing loops that cannot afford cudaMalloc's
+ * implicit device synchronisation and unbounded latency.  Plans allocate their tables and
+ * workspace, so those callers cannot create one.  This entry point needs no plan: its scratch
+ * buffer (the four-step intermediate) and its twiddle tables are fixed-size static device
+ * arrays of the library (16 MiB + 512 KiB, held by every GPU that loads them until the
+ * process exits), and the call allocates nothing.
+ *
+ *   n, batch   2^15 <= n <= 2^21 (power of two) and batch * n <= 2^21 (the scratch capacity);
+ *              anything larger returns FFT_ERR_UNSUPPORTED_SIZE.
+ *   direction, shift   as for fft_plan_create (C2C, dims 1).
+ *   in, out, stream    as for fft_exec_c2c (device pointers, 16-byte aligned, in == out
+ *              allowed); the output equals that of fft_exec_c2c on a plan of the same size.
+ * Set-up: the first call on each device (with that device current) resolves the static
+ * arrays' device addresses and uploads the twiddle tables with a synchronous copy; make that
+ * first call before any stream capture.  Later calls only enqueue two kernels.
+ * All calls share the one scratch array: calls that overlap on the GPU (on different streams
+ * or threads) race and corrupt each other's results; serialise them.  The scratch keeps the
+ * last call's contents, and nothing in it needs clearing (every element read is first
+ * written by the same call).
+ * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_UNSUPPORTED_SIZE, FFT_ERR_MISALIGNED or
+ * FFT_ERR_CUDA.
+ */
+int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int shift, const void* in,
+                         void* out, void* stream);
+
 /* fft_status_string - static description of a status code (never NULL). */
 const char* fft_status_string(int status);
 
