@@ -33,7 +33,7 @@ ABI_SYMBOLS = (
     "fft_plan_create", "fft_plan_set_band_limit", "fft_plan_workspace_bytes",
     "fft_plan_describe", "fft_plan_query", "fft_exec_c2c", "fft_exec_r2c", "fft_exec_c2r",
     "fft_plan_check", "fft_plan_destroy", "fft_status_string", "fft_version",
-    "fft_exec_c2c_noalloc",
+    "fft_exec_c2c_noalloc", "fft_plan_set_wait_timeout",
 )
 
 _LIB = None
@@ -69,6 +69,7 @@ def lib():
         L.fft_status_string.restype = ctypes.c_char_p
         L.fft_version.argtypes = []
         L.fft_exec_c2c_noalloc.argtypes = [i64, i64, ci, ci, vp, vp, vp]
+        L.fft_plan_set_wait_timeout.argtypes = [vp, ctypes.c_uint64]
         for name in ABI_SYMBOLS:
             if name != "fft_status_string":
                 getattr(L, name).restype = ci
@@ -145,6 +146,10 @@ class Plan:
 
     def check(self):
         _check(lib().fft_plan_check(self._h), "fft_plan_check")
+
+    def set_wait_timeout(self, ns: int):
+        """Limit of every device-side wait of this plan's kernels (0: give up at once)."""
+        _check(lib().fft_plan_set_wait_timeout(self._h, int(ns)), "fft_plan_set_wait_timeout")
 
     def close(self):
         if getattr(self, "_h", None):

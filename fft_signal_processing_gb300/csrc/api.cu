@@ -29,6 +29,7 @@
 
 #include "../../include/gbfft.h"
 #include "fft_kernel.cuh"
+#include "host_tables.h"
 #include "kernels.h"
 
 using namespace gbfft;
@@ -99,84 +100,15 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     return FFT_OK;
 }
 
-// ---- host twiddle tables ------------------------------------------------------------------
-const double kTwoPi = 6.283185307179586476925286766559005768;
+using host::append_pass_tables;
+using host::append_roots;
+using host::align_table;
 
-// (cos, sin)(2*pi*q/m) in double, rounded once to float.  The angle is reduced in integers to
-// the first quadrant, and cos/sin are evaluated at the nearer of a and pi/2 - a, so quarter
-// turns are exactly 0 and +-1 and the table keeps the symmetries of the unit circle.
-float2 root_of_unity(int64_t q, int64_t m) {
-    q %= m;
-    if (q < 0) q += m;
-    if (m % 4 != 0) {  // m = 1, 2: the roots are +-1
-        const bool half = (2 * q == m);
-        return make_float2(half ? -1.f : 1.f, 0.f);
-    }
-    // first quadrant angle a (in units of 2*pi/m) and the number of quarter turns
-    const int64_t qq = m / 4;
-    const int64_t quad = q / qq, a = q % qq;
-    double c, s;
-    if (a <= qq / 2) {
-        const double th = kTwoPi * (double)a / (double)m;
-        c = std::cos(th);
-        s = std::sin(th);
-    } else {  // use the complementary angle pi/2 - th for accuracy near pi/2
-        const double th = kTwoPi * (double)(qq - a) / (double)m;
-        c = std::sin(th);
-        s = std::cos(th);
-    }
-    if (a == 0) {
-        c = 1.0;
-        s = 0.0;
-    }
-    double x, y;  // rotate by quad quarter turns
-    switch (quad & 3) {
-        case 0: x = c; y = s; break;
-        case 1: x = -s; y = c; break;
-        case 2: x = -c; y = -s; break;
-        default: x = s; y = -c; break;
-    }
-    return make_float2((float)x, (float)y);
-}
-
-void push_root(std::vector<float2>& v, int64_t q, int64_t m) { v.push_back(root_of_unity(q, m)); }
-
-void align_table(std::vector<float2>& v) {
-    while (v.size() % 32) v.push_back(make_float2(0.f, 0.f));
-}
-
-// Per-pass tables of a 2^l-point transform (layout of tw_pass_off in fft_kernel.cuh).
-size_t append_pass_tables(std::vector<float2>& v, int l) {
-    align_table(v);
-    const size_t off = v.size();
-    if (l <= 4) return off;
-    const int npass = (l + 3) / 4;
-    for (int p = 1; p < npass; ++p) {
-        const int rb = (l - 4 * p >= 4) ? 4 : l - 4 * p;
-        const int64_t R = int64_t(1) << rb, Ns = int64_t(1) << (4 * p);
-        for (int64_t m = 0; m < Ns; ++m)
-            for (int64_t r = 0; r < R; ++r) push_root(v, m * r, Ns * R);
-    }
-    if (v.size() - off != (size_t)tw_table_size(l)) std::abort();  // layout invariant
-    return off;
-}
-
-size_t append_roots(std::vector<float2>& v, int64_t count, int64_t step, int64_t m) {
-    align_table(v);
-    const size_t off = v.size();
-    for (int64_t q = 0; q < count; ++q) push_root(v, q * step, m);
-    return off;
-}
-
-std::string radix_string(int l) {
-    if (l == 0) return "1";
+std::string radix_string(int l, int maxrb) {
     std::string s;
-    int rem = l;
-    while (rem > 0) {
-        const int rb = rem >= 4 ? 4 : rem;
-        if (!s.empty()) s += "x";
-        s += std::to_string(1 << rb);
-        rem -= rb;
+    for (int p = 0; p < sched_npass(l, maxrb); ++p) {
+        if (p) s += "x";
+        s += std::to_string(1 << sched_rbits(l, maxrb, p));
     }
     return s;
 }
@@ -185,24 +117,28 @@ struct Geo {
     int threads, per_cta;
     size_t smem;
 };
+size_t padded_bytes(int l, int maxrb, int w) {
+    const int lp = sched_rbits(l, maxrb, 0);
+    return sched_npass(l, maxrb) > 1 ? (size_t)spad_size(1 << l, lp) * (1u << w) * 8u : 0;
+}
 Geo rows_geo(int l) {
-    const int e = rows_log2e(l), w = rows_log2w(l);
-    const int npass = l <= 4 ? 1 : (l + 3) / 4;
-    return {(1 << (l - e)) << w, 1 << w,
-            npass > 1 ? (size_t)spad_size(1 << l) * (1u << w) * 8u : 0};
+    if (l >= kRowsTmaMinLog2 && l <= kRowsTmaMaxLog2) {  // persistent bulk-copy kernel
+        const int w = 12 - l, lp = sched_rbits(l, rows_maxrb(l), 0);
+        const size_t stage = (size_t)std::max(spad_size(1 << l, lp), 1 << l) * (1u << w) * 8u;
+        return {(1 << rows_log2t(l)) << w, 1 << w, stage * kRowsTmaStages};
+    }
+    const int w = rows_log2w(l);
+    return {(1 << rows_log2t(l)) << w, 1 << w, padded_bytes(l, rows_maxrb(l), w)};
 }
 Geo strided_geo(int l, int log2minw) {
-    const int e = cols_log2e(l), w = cols_log2w(l, log2minw);
-    const int npass = l <= 4 ? 1 : (l + 3) / 4;
-    return {(1 << (l - e)) << w, 1 << w,
-            npass > 1 ? (size_t)spad_size(1 << l) * (1u << w) * 8u : 0};
+    const int w = cols_log2w(l, log2minw);
+    return {(1 << cols_log2t(l)) << w, 1 << w, padded_bytes(l, cols_maxrb(l), w)};
 }
 Geo real_geo(int lh) {
-    const int e = rows_log2e(lh), w = real_log2w(lh);
-    const int npass = lh <= 4 ? 1 : (lh + 3) / 4;
-    const int srow = npass > 1 ? spad_size(1 << lh) : 0;
-    const int sreal = std::max(srow, spad_size(1 << lh) + 1);
-    return {(1 << (lh - e)) << w, 1 << w, (size_t)sreal * (1u << w) * 8u};
+    const int w = real_log2w(lh), lp = sched_rbits(lh, real_maxrb(lh), 0);
+    const int srow = sched_npass(lh, real_maxrb(lh)) > 1 ? spad_size(1 << lh, lp) : 0;
+    const int sreal = std::max(srow, spad_size(1 << lh, lp) + 1);
+    return {(1 << real_log2t(lh)) << w, 1 << w, (size_t)sreal * (1u << w) * 8u};
 }
 
 std::string describe_spec(const PlanSpec& s, int64_t mmax) {
@@ -215,7 +151,7 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
                      "path=onepass n=%lld batch=%lld %s shift=%d radix=%s kernels=1 "
                      "threads=%d rows_per_cta=%d smem=%zu",
                      (long long)s.n, (long long)s.batch, dir, s.shift,
-                     radix_string(s.log2n).c_str(), g.threads, g.per_cta, g.smem);
+                     radix_string(s.log2n, rows_maxrb(s.log2n)).c_str(), g.threads, g.per_cta, g.smem);
             break;
         }
         case PATH_FOURSTEP: {
@@ -225,8 +161,9 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
                      "pass1=columns(radix=%s threads=%d cols_per_cta=%d smem=%zu) "
                      "pass2=rows_transposed(radix=%s threads=%d rows_per_cta=%d smem=%zu)",
                      (long long)s.n, (long long)s.batch, dir, s.shift, 1 << s.log2n1,
-                     1 << s.log2n2, radix_string(s.log2n1).c_str(), g1.threads, g1.per_cta,
-                     g1.smem, radix_string(s.log2n2).c_str(), g2.threads, g2.per_cta, g2.smem);
+                     1 << s.log2n2, radix_string(s.log2n1, cols_maxrb(s.log2n1)).c_str(), g1.threads,
+                     g1.per_cta, g1.smem, radix_string(s.log2n2, cols_maxrb(s.log2n2)).c_str(),
+                     g2.threads, g2.per_cta, g2.smem);
             break;
         }
         case PATH_2D: {
@@ -236,8 +173,8 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
                      "rows(threads=%d rows_per_cta=%d smem=%zu) "
                      "columns(threads=%d cols_per_cta=%d smem=%zu)",
                      (long long)s.n, (long long)s.n, (long long)s.batch, dir, s.shift,
-                     radix_string(s.log2n).c_str(), g1.threads, g1.per_cta, g1.smem,
-                     g2.threads, g2.per_cta, g2.smem);
+                     radix_string(s.log2n, rows_maxrb(s.log2n)).c_str(), g1.threads, g1.per_cta,
+                     g1.smem, g2.threads, g2.per_cta, g2.smem);
             break;
         }
         default: {
@@ -248,7 +185,7 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
                      (long long)s.n, (long long)s.batch,
                      s.direction < 0 ? "analysis(r2c)" : "synthesis(c2r)", (long long)mmax,
                      s.layout == FFT_LAYOUT_REAL_MMAJOR ? "mmajor" : "rowmajor",
-                     (long long)(s.n / 2), radix_string(s.log2n - 1).c_str(), g.threads,
+                     (long long)(s.n / 2), radix_string(s.log2n - 1, real_maxrb(s.log2n - 1)).c_str(), g.threads,
                      g.per_cta, g.smem);
             break;
         }
@@ -280,6 +217,7 @@ struct gbfft_plan_s {
     void* d_work = nullptr;
     size_t work_bytes = 0;
     int* d_err = nullptr;
+    uint64_t wait_limit_ns = 2000000000ull;  // bounded device waits: 2 s
 };
 
 static void free_plan(gbfft_plan_s* p) {
@@ -340,12 +278,15 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
     std::vector<float2> tw;
     switch (s.path) {
         case PATH_ONEPASS:
+            p->off_a = append_pass_tables(tw, s.log2n, rows_maxrb(s.log2n));
+            break;
         case PATH_2D:
-            p->off_a = append_pass_tables(tw, s.log2n);
+            p->off_a = append_pass_tables(tw, s.log2n, rows_maxrb(s.log2n));  // row pass
+            p->off_b = append_pass_tables(tw, s.log2n, cols_maxrb(s.log2n));  // column pass
             break;
         case PATH_FOURSTEP: {
-            p->off_a = append_pass_tables(tw, s.log2n1);
-            p->off_b = append_pass_tables(tw, s.log2n2);
+            p->off_a = append_pass_tables(tw, s.log2n1, cols_maxrb(s.log2n1));
+            p->off_b = append_pass_tables(tw, s.log2n2, cols_maxrb(s.log2n2));
             const int64_t nlo = int64_t(1) << s.lowbits, nhi = int64_t(1) << (s.log2n - s.lowbits);
             p->off_hi = append_roots(tw, nhi, nlo, s.n);  // w_n^{qh * 2^lowbits}
             p->off_lo = append_roots(tw, nlo, 1, s.n);    // w_n^{ql}
@@ -353,7 +294,7 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
             break;
         }
         case PATH_REAL:
-            p->off_a = append_pass_tables(tw, s.log2n - 1);
+            p->off_a = append_pass_tables(tw, s.log2n - 1, real_maxrb(s.log2n - 1));
             p->off_r = append_roots(tw, s.n / 2, 1, s.n);  // w_n^k, k < n/2
             break;
     }
@@ -380,6 +321,12 @@ int fft_plan_set_band_limit(fft_plan p, int64_t mmax) {
     if (!p || p->s.path != PATH_REAL) return FFT_ERR_INVALID_ARG;
     if (mmax < 0 || mmax >= p->s.n / 2) return FFT_ERR_INVALID_ARG;
     p->mmax = mmax;
+    return FFT_OK;
+}
+
+int fft_plan_set_wait_timeout(fft_plan p, uint64_t ns) {
+    if (!p) return FFT_ERR_INVALID_ARG;
+    p->wait_limit_ns = ns;
     return FFT_OK;
 }
 
@@ -411,7 +358,8 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
     switch (s.path) {
         case PATH_ONEPASS: {
             const int flags = s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0;
-            e = run_rows(s.log2n, s.direction, x, y, s.batch, p->d_tw + p->off_a, flags, 0, st);
+            e = run_rows(s.log2n, s.direction, x, y, s.batch, p->d_tw + p->off_a, flags, 0,
+                         p->d_err, p->wait_limit_ns, st);
             break;
         }
         case PATH_FOURSTEP: {
@@ -428,10 +376,10 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
         case PATH_2D: {
             const int64_t n = s.n;
             e = run_rows(s.log2n, s.direction, x, y, s.batch * n, p->d_tw + p->off_a,
-                         (s.shift && fwd) ? KF_CHESS_LOAD : 0, 1, st);
+                         (s.shift && fwd) ? KF_CHESS_LOAD : 0, 1, p->d_err, p->wait_limit_ns, st);
             if (e == cudaSuccess)
                 e = run_cols(s.log2n, s.direction, y, y, s.batch * n, s.log2n,
-                             p->d_tw + p->off_a, (s.shift && !fwd) ? KF_CHESS_STORE : 0, 1,
+                             p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0, 1,
                              nullptr, nullptr, 0, st);
             break;
         }

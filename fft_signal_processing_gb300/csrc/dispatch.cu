@@ -1,0 +1,64 @@
+// Run-time dispatch from (family, log2 size) to the per-size entry functions.
+#include "inst_entries.h"
+#include "kernels.h"
+
+namespace gbfft {
+
+cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t nrows,
+                     const float2* tw, int flags, int rp, int* err, uint64_t lim,
+                     cudaStream_t s) {
+    switch (log2n) {
+#define GBFFT_C(L) \
+    case L: return rows_entry_##L(dir, in, out, nrows, tw, flags, rp, err, lim, s);
+        GBFFT_ROWS_SIZES(GBFFT_C)
+#undef GBFFT_C
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t count,
+                     int log2s, const float2* tw, int flags, int ep, const float2* hi,
+                     const float2* lo, int lowbits, cudaStream_t s) {
+    switch (log2l) {
+#define GBFFT_C(L) \
+    case L: return cols_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo, lowbits, s);
+        GBFFT_COLS_SIZES(GBFFT_C)
+#undef GBFFT_C
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_t count,
+                       int log2n1, const float2* tw, int flags, cudaStream_t s) {
+    switch (log2n) {
+#define GBFFT_C(L) \
+    case L: return rows_t_entry_##L(dir, in, out, count, log2n1, tw, flags, s);
+        GBFFT_ROWS_T_SIZES(GBFFT_C)
+#undef GBFFT_C
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
+                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s) {
+    switch (log2h) {
+#define GBFFT_C(L) \
+    case L: return r2c_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, s);
+        GBFFT_REAL_SIZES(GBFFT_C)
+#undef GBFFT_C
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
+                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s) {
+    switch (log2h) {
+#define GBFFT_C(L) \
+    case L: return c2r_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, s);
+        GBFFT_REAL_SIZES(GBFFT_C)
+#undef GBFFT_C
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gbfft

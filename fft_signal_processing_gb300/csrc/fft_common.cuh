@@ -32,28 +32,36 @@ __device__ __forceinline__ float2 cmul(float2 a, float2 b) {
     return make_float2(fmaf(a.x, b.x, -(a.y * b.y)), fmaf(a.x, b.y, a.y * b.x));
 }
 
-// cos(2*pi*k/32) for any integer k, as compile-time constants (quarter-wave values of the
-// 32nd roots of unity; every butterfly radix used here divides 32).
-__host__ __device__ constexpr double cos32(int k) {
-    k = ((k % 32) + 32) % 32;
-    if (k > 16) k = 32 - k;          // cos is even
-    const bool neg = k > 8;          // cos(pi - a) = -cos(a)
-    if (neg) k = 16 - k;
+// cos(2*pi*k/64) for any integer k, as compile-time constants (quarter-wave values of the
+// 64th roots of unity; every in-register butterfly radix used here divides 64).
+__host__ __device__ constexpr double cos64(int k) {
+    k = ((k % 64) + 64) % 64;
+    if (k > 32) k = 64 - k;          // cos is even
+    const bool neg = k > 16;         // cos(pi - a) = -cos(a)
+    if (neg) k = 32 - k;
     double v = 0.0;
     switch (k) {
         case 0: v = 1.0; break;
-        case 1: v = 0.98078528040323044912618223613424; break;
-        case 2: v = 0.92387953251128675612818318939679; break;
-        case 3: v = 0.83146961230254523707878837761791; break;
-        case 4: v = 0.70710678118654752440084436210485; break;
-        case 5: v = 0.55557023301960222474283081394853; break;
-        case 6: v = 0.38268343236508977172845998403040; break;
-        case 7: v = 0.19509032201612826784828486847702; break;
+        case 1: v = 0.99518472667219688624483695310948; break;
+        case 2: v = 0.98078528040323044912618223613424; break;
+        case 3: v = 0.95694033573220886493579788698027; break;
+        case 4: v = 0.92387953251128675612818318939679; break;
+        case 5: v = 0.88192126434835502971275686366039; break;
+        case 6: v = 0.83146961230254523707878837761791; break;
+        case 7: v = 0.77301045336273696081090660975847; break;
+        case 8: v = 0.70710678118654752440084436210485; break;
+        case 9: v = 0.63439328416364549821517161322549; break;
+        case 10: v = 0.55557023301960222474283081394853; break;
+        case 11: v = 0.47139673682599764855638762591373; break;
+        case 12: v = 0.38268343236508977172845998403040; break;
+        case 13: v = 0.29028467725446236763619237581740; break;
+        case 14: v = 0.19509032201612826784828486847702; break;
+        case 15: v = 0.09801714032956060199419556388864; break;
         default: v = 0.0; break;
     }
     return neg ? -v : v;
 }
-__host__ __device__ constexpr double sin32(int k) { return cos32(k - 8); }
+__host__ __device__ constexpr double sin64(int k) { return cos64(k - 16); }
 
 // a * exp(DIR * 2*pi*i * E / R) with E, R compile-time.  Quarter turns are exact swaps and
 // sign flips; everything else is one complex multiply by float constants.
@@ -69,15 +77,46 @@ __device__ __forceinline__ float2 crot(float2 a) {
     } else if constexpr (4 * e == 3 * R) {      // -DIR * i
         return DIR < 0 ? make_float2(-a.y, a.x) : make_float2(a.y, -a.x);
     } else {
-        static_assert(32 % R == 0, "radix must divide 32");
-        constexpr int k = e * (32 / R);
-        constexpr float c = (float)cos32(k);
-        constexpr float s = (float)(DIR * sin32(k));
+        static_assert(64 % R == 0, "radix must divide 64");
+        constexpr int k = e * (64 / R);
+        constexpr float c = (float)cos64(k);
+        constexpr float s = (float)(DIR * sin64(k));
         return make_float2(fmaf(a.x, c, -(a.y * s)), fmaf(a.x, s, a.y * c));
     }
 }
 
 __host__ __device__ constexpr int ilog2c(int v) { return v <= 1 ? 0 : 1 + ilog2c(v >> 1); }
+
+// ---- pass schedule ----------------------------------------------------------------------------
+// A 2^l-point transform is split into npass radix passes of at most 2^m points each, as evenly
+// as possible with the larger radices first (e.g. l = 12, m = 6: 64 x 64; l = 10, m = 4:
+// 16 x 8 x 8).  Shared by the kernels and the host twiddle-table builder.
+__host__ __device__ constexpr int sched_npass(int l, int m) { return l <= 0 ? 1 : (l + m - 1) / m; }
+__host__ __device__ constexpr int sched_rbits(int l, int m, int p) {
+    return l / sched_npass(l, m) + (p < l % sched_npass(l, m) ? 1 : 0);
+}
+__host__ __device__ constexpr int sched_span_bits(int l, int m, int p) {
+    return p <= 0 ? 0 : sched_span_bits(l, m, p - 1) + sched_rbits(l, m, p - 1);
+}
+
+// ---- twiddle tables ---------------------------------------------------------------------------
+// Pass p >= 1 (radix R = 2^rb, span Ns) multiplies element r of butterfly j by w^r, where
+// w = w_{Ns*R}^(j mod Ns).  Its table holds, for each m < Ns, the A = 2^ceil(rb/2) "low"
+// powers w^a (a < A) followed by the B = R/A "high" powers w^(A*b) (b < B), padded to an even
+// count; w^r with r = a + A*b is formed as w^a * w^(A*b).  Passes are stored back to back.
+__host__ __device__ constexpr int tw_lo_count(int rb) { return 1 << ((rb + 1) / 2); }
+__host__ __device__ constexpr int tw_hi_count(int rb) { return 1 << (rb - (rb + 1) / 2); }
+__host__ __device__ constexpr int tw_stride(int rb) {
+    return ((tw_lo_count(rb) + tw_hi_count(rb)) + 1) & ~1;
+}
+__host__ __device__ constexpr int tw_pass_off(int l, int m, int p) {
+    return p <= 1 ? 0
+                  : tw_pass_off(l, m, p - 1) +
+                        (1 << sched_span_bits(l, m, p - 1)) * tw_stride(sched_rbits(l, m, p - 1));
+}
+__host__ __device__ constexpr int tw_table_size(int l, int m) {
+    return tw_pass_off(l, m, sched_npass(l, m));
+}
 
 __host__ __device__ constexpr int bitrev_c(int i, int bits) {
     int r = 0;
@@ -114,7 +153,10 @@ __device__ __forceinline__ void dft_reg(float2* v) {
 #define GBFFT_ROT(EE) case EE: v[blk + k + half] = crot<DIR, EE, R>(v[blk + k + half]); break;
                     GBFFT_ROT(1) GBFFT_ROT(2) GBFFT_ROT(3) GBFFT_ROT(4) GBFFT_ROT(5) GBFFT_ROT(6)
                     GBFFT_ROT(7) GBFFT_ROT(8) GBFFT_ROT(9) GBFFT_ROT(10) GBFFT_ROT(11)
-                    GBFFT_ROT(12) GBFFT_ROT(13) GBFFT_ROT(14) GBFFT_ROT(15)
+                    GBFFT_ROT(12) GBFFT_ROT(13) GBFFT_ROT(14) GBFFT_ROT(15) GBFFT_ROT(16)
+                    GBFFT_ROT(17) GBFFT_ROT(18) GBFFT_ROT(19) GBFFT_ROT(20) GBFFT_ROT(21)
+                    GBFFT_ROT(22) GBFFT_ROT(23) GBFFT_ROT(24) GBFFT_ROT(25) GBFFT_ROT(26)
+                    GBFFT_ROT(27) GBFFT_ROT(28) GBFFT_ROT(29) GBFFT_ROT(30) GBFFT_ROT(31)
 #undef GBFFT_ROT
                     default: break;
                 }
@@ -128,11 +170,12 @@ __device__ __forceinline__ void dft_reg(float2* v) {
     for (int i = 0; i < R; ++i) v[i] = t[i];
 }
 
-// Shared-memory index padding: one float2 of padding every 16, which makes the stride-16
-// writes of a radix-16 pass (and the stride-R writes of the smaller radices) bank-conflict
-// free for 64-bit accesses.
-__device__ __forceinline__ int spad(int i) { return i + (i >> 4); }
-__host__ __device__ constexpr int spad_size(int n) { return n + (n >> 4); }
+// Shared-memory index padding: one float2 of padding every 2^LP slots.  With 2^LP equal to the
+// radix R0 of the first pass, the stride-R0 writes of that pass are bank-conflict free for
+// 64-bit accesses, and the unit-stride accesses of the other passes stay (nearly) so.
+template <int LP>
+__device__ __forceinline__ int spad(int i) { return i + (i >> LP); }
+__host__ __device__ constexpr int spad_size(int n, int lp) { return n + (n >> lp); }
 
 // Streaming global loads / stores (data is touched once per pass).
 __device__ __forceinline__ float2 ldg_stream(const float2* p) { return __ldcs(p); }

@@ -21,60 +21,66 @@
 
 namespace gbfft {
 
-// LOG2N: transform length; LOG2E: points per thread; LOG2W: transforms per CTA;
-// TFAST: lane order inside the CTA (true: a transform's threads are adjacent lanes, which
-// suits contiguous rows; false: the W transforms are adjacent lanes, which suits columns and
-// transposed stores because neighbouring transforms are neighbouring in memory).
-template <int LOG2N_, int LOG2E_, int LOG2W_, bool TFAST_>
+// LOG2N: transform length; MAXRB: log2 of the largest radix per pass (registers per thread
+// hold one butterfly of the first, largest radix); LOG2W: transforms per CTA; TFAST: lane order
+// inside the CTA (true: a transform's threads are adjacent lanes, which suits contiguous rows;
+// false: the W transforms are adjacent lanes, which suits columns and transposed stores
+// because neighbouring transforms are neighbouring in memory).
+template <int LOG2N_, int MAXRB_, int LOG2W_, bool TFAST_>
 struct FftCfg {
     static constexpr int LOG2N = LOG2N_;
+    static constexpr int MAXRB = MAXRB_;
     static constexpr int N = 1 << LOG2N;
-    static constexpr int LOG2E = LOG2E_ < LOG2N_ ? LOG2E_ : LOG2N_;
-    static constexpr int E = 1 << LOG2E;
-    static constexpr int T = N / E;  // threads per transform
+    static constexpr int NPASS = sched_npass(LOG2N, MAXRB);
+    static constexpr int LOG2E = sched_rbits(LOG2N, MAXRB, 0);
+    static constexpr int E = 1 << LOG2E;  // points per thread = radix of the first pass
+    static constexpr int T = N / E;       // threads per transform
     static constexpr int W = 1 << LOG2W_;
     static constexpr bool TFAST = TFAST_;
     static constexpr int THREADS = T * W;
-    static constexpr int NPASS = LOG2N <= 4 ? 1 : (LOG2N + 3) / 4;
-    static constexpr int SROW = NPASS > 1 ? spad_size(N) : 0;  // padded float2 per transform
+    static constexpr int LP = LOG2E;  // shared-memory padding granularity (one slot per E)
+    static constexpr int SROW = NPASS > 1 ? spad_size(N, LP) : 0;  // padded float2 per transform
     static constexpr size_t SMEM_BYTES = (size_t)SROW * W * sizeof(float2);
     // shared-memory element stride between consecutive (padded) indices of one transform
     static constexpr int SS = TFAST ? 1 : W;
 
-    // radix bits of pass p: greedy 16, the remainder last
-    __host__ __device__ static constexpr int rbits(int p) {
-        return LOG2N <= 4 ? LOG2N : (LOG2N - 4 * p >= 4 ? 4 : LOG2N - 4 * p);
-    }
+    __host__ __device__ static constexpr int rbits(int p) { return sched_rbits(LOG2N, MAXRB, p); }
     __host__ __device__ static constexpr int radix(int p) { return 1 << rbits(p); }
-    __host__ __device__ static constexpr int span(int p) { return 1 << (4 * p); }
-};
-
-// Twiddle tables of an N-point transform, pass p >= 1: Ns*R entries
-// [m*R + r] = (cos, sin)(2*pi*m*r/(Ns*R)), m < Ns, r < R, passes stored back to back.
-__host__ __device__ constexpr int tw_pass_off(int log2n, int p) {
-    int off = 0;
-    for (int q = 1; q < p; ++q) {
-        int rb = (log2n - 4 * q >= 4) ? 4 : log2n - 4 * q;
-        off += (1 << (4 * q)) * (1 << rb);
+    __host__ __device__ static constexpr int span(int p) {
+        return 1 << sched_span_bits(LOG2N, MAXRB, p);
     }
-    return off;
-}
-__host__ __device__ constexpr int tw_table_size(int log2n) {
-    return log2n <= 4 ? 0 : tw_pass_off(log2n, (log2n + 3) / 4);
-}
+};
 
 template <class C, int DIR, int P>
 __device__ __forceinline__ void pass_twiddle(float2* v, int j, const float2* __restrict__ tw) {
-    constexpr int R = C::radix(P);
+    constexpr int RB = C::rbits(P);
+    constexpr int R = 1 << RB;
     constexpr int Ns = C::span(P);
-    const float4* w4 =
-        reinterpret_cast<const float4*>(tw + tw_pass_off(C::LOG2N, P) + (j & (Ns - 1)) * R);
+    constexpr int A = tw_lo_count(RB);
+    constexpr int B = tw_hi_count(RB);
+    constexpr int S = tw_stride(RB);
+    const float4* w4 = reinterpret_cast<const float4*>(tw + tw_pass_off(C::LOG2N, C::MAXRB, P) +
+                                                       (j & (Ns - 1)) * S);
+    float2 w[S];
 #pragma unroll
-    for (int r2 = 0; r2 < R / 2; ++r2) {
-        float4 w = __ldg(w4 + r2);
-        if (r2 > 0) v[2 * r2] = ctw<DIR>(v[2 * r2], make_float2(w.x, w.y));
-        v[2 * r2 + 1] = ctw<DIR>(v[2 * r2 + 1], make_float2(w.z, w.w));
+    for (int i = 0; i < S / 2; ++i) {
+        const float4 q = __ldg(w4 + i);
+        w[2 * i] = make_float2(q.x, q.y);
+        w[2 * i + 1] = make_float2(q.z, q.w);
     }
+#pragma unroll
+    for (int r = 1; r < R; ++r) {
+        const int a = r % A, b = r / A;
+        float2 f;
+        if (b == 0)
+            f = w[a];
+        else if (a == 0)
+            f = w[A + b];
+        else
+            f = cmul(w[a], w[A + b]);
+        v[r] = ctw<DIR>(v[r], f);
+    }
+    (void)B;
 }
 
 // Passes P..NPASS-1 on register data v (v[b*R + r] is element r of butterfly j = t + b*T).
@@ -98,7 +104,7 @@ __device__ __forceinline__ void run_passes(float2 (&v)[C::E], int t, float2* sb,
             const int j = t + b * C::T;
             const int base = (j / Ns) * Ns * R + (j & (Ns - 1));
 #pragma unroll
-            for (int r = 0; r < R; ++r) sb[spad(base + r * Ns) * C::SS] = v[b * R + r];
+            for (int r = 0; r < R; ++r) sb[spad<C::LP>(base + r * Ns) * C::SS] = v[b * R + r];
         }
         __syncthreads();
         constexpr int R2 = C::radix(P + 1);
@@ -108,7 +114,7 @@ __device__ __forceinline__ void run_passes(float2 (&v)[C::E], int t, float2* sb,
         for (int b = 0; b < B2; ++b) {
             const int j = t + b * C::T;
 #pragma unroll
-            for (int r = 0; r < R2; ++r) v[b * R2 + r] = sb[spad(j + r * S2) * C::SS];
+            for (int r = 0; r < R2; ++r) v[b * R2 + r] = sb[spad<C::LP>(j + r * S2) * C::SS];
         }
         run_passes<C, DIR, P + 1>(v, t, sb, tw);
     }

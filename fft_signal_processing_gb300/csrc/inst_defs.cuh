@@ -1,0 +1,93 @@
+// Instantiation macros: each kernel family is instantiated per log2 size in a translation unit
+// of its own (the radix-64 kernels are large), behind a plain entry function per size that the
+// dispatcher (dispatch.cu) selects at run time.
+#pragma once
+
+#include "fft_kernel.cuh"
+#include "kernels.h"
+#include "real_kernel.cuh"
+#include "rows_tma.cuh"
+
+namespace gbfft {
+
+// One-pass rows: the persistent bulk-copy kernel from 2^5 to 2^12, the plain kernel elsewhere.
+template <int L, int DIR>
+cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2* tw, int flags,
+                      int rp, int* err, uint64_t lim, cudaStream_t s) {
+    if constexpr (L >= kRowsTmaMinLog2 && L <= kRowsTmaMaxLog2) {
+        return launch_rows_tma<RowsTmaCfg<L, rows_maxrb(L), kRowsTmaStages>, DIR>(
+            in, out, nrows, tw, flags, rp, err, lim, s);
+    } else {
+        (void)err;
+        (void)lim;
+        using C = FftCfg<L, rows_maxrb(L), rows_log2w(L), true>;
+        MapRows m{nrows, L, rp};
+        return launch_fft<C, DIR, MapRows>(in, out, m, tw, flags, s);
+    }
+}
+
+template <int L, int DIR, bool TW>
+cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, const float2* tw,
+                      int flags, int ep, const float2* hi, const float2* lo, int lowbits,
+                      cudaStream_t s) {
+    using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 0), false>;
+    MapCols<TW> m{count, log2s, L, ep, hi, lo, lowbits};
+    return launch_fft<C, DIR, MapCols<TW>>(in, out, m, tw, flags, s);
+}
+
+template <int L, int DIR>
+cudaError_t rows_t_impl(const float2* in, float2* out, int64_t count, int log2n1,
+                        const float2* tw, int flags, cudaStream_t s) {
+    using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 2), false>;
+    MapRowsT m{count, L, log2n1};
+    return launch_fft<C, DIR, MapRowsT>(in, out, m, tw, flags, s);
+}
+
+template <int LH>
+using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), true>;
+
+}  // namespace gbfft
+
+#define GBFFT_DEF_ROWS(L)                                                                      \
+    cudaError_t gbfft::rows_entry_##L(int dir, const float2* in, float2* out, int64_t nrows,    \
+                                      const float2* tw, int flags, int rp, int* err,            \
+                                      uint64_t lim, cudaStream_t s) {                           \
+        return dir < 0 ? rows_impl<L, -1>(in, out, nrows, tw, flags, rp, err, lim, s)           \
+                       : rows_impl<L, +1>(in, out, nrows, tw, flags, rp, err, lim, s);          \
+    }
+
+#define GBFFT_DEF_COLS(L)                                                                      \
+    cudaError_t gbfft::cols_entry_##L(int dir, const float2* in, float2* out, int64_t count,    \
+                                      int log2s, const float2* tw, int flags, int ep,           \
+                                      const float2* hi, const float2* lo, int lowbits,          \
+                                      cudaStream_t s) {                                         \
+        if (hi)                                                                                 \
+            return dir < 0 ? cols_impl<L, -1, true>(in, out, count, log2s, tw, flags, ep, hi,   \
+                                                    lo, lowbits, s)                             \
+                           : cols_impl<L, +1, true>(in, out, count, log2s, tw, flags, ep, hi,   \
+                                                    lo, lowbits, s);                            \
+        return dir < 0 ? cols_impl<L, -1, false>(in, out, count, log2s, tw, flags, ep, hi, lo,  \
+                                                 lowbits, s)                                    \
+                       : cols_impl<L, +1, false>(in, out, count, log2s, tw, flags, ep, hi, lo,  \
+                                                 lowbits, s);                                   \
+    }
+
+#define GBFFT_DEF_ROWS_T(L)                                                                    \
+    cudaError_t gbfft::rows_t_entry_##L(int dir, const float2* in, float2* out, int64_t count,  \
+                                        int log2n1, const float2* tw, int flags,                \
+                                        cudaStream_t s) {                                       \
+        return dir < 0 ? rows_t_impl<L, -1>(in, out, count, log2n1, tw, flags, s)               \
+                       : rows_t_impl<L, +1>(in, out, count, log2n1, tw, flags, s);              \
+    }
+
+#define GBFFT_DEF_REAL(L)                                                                      \
+    cudaError_t gbfft::r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,     \
+                                     int mmajor, const float2* tw, const float2* twr,           \
+                                     cudaStream_t s) {                                          \
+        return launch_r2c<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, s);                  \
+    }                                                                                           \
+    cudaError_t gbfft::c2r_entry_##L(const float2* in, float* out, int64_t nrows, int mmax,     \
+                                     int mmajor, const float2* tw, const float2* twr,           \
+                                     cudaStream_t s) {                                          \
+        return launch_c2r<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, s);                  \
+    }

@@ -11,27 +11,31 @@
 namespace gbfft {
 
 // ---- launch geometry ------------------------------------------------------------------------
-// points per thread: 16 (32 from 2^12 up for the strided families, 2^14 for rows); whole
-// transform per thread below 16 points.
-__host__ __device__ constexpr int rows_log2e(int l) { return l <= 4 ? l : (l >= 14 ? 5 : 4); }
-__host__ __device__ constexpr int cols_log2e(int l) { return l <= 4 ? l : (l >= 12 ? 5 : 4); }
+// Largest radix per pass (log2) of each family: radix 64 for rows of 2^9 points and more (two
+// passes up to 4096 points: 64 x 64, one shared-memory exchange), radix 16 elsewhere.
+__host__ __device__ constexpr int rows_maxrb(int l) { return l >= 9 ? 6 : 4; }
+__host__ __device__ constexpr int cols_maxrb(int) { return 4; }
+__host__ __device__ constexpr int real_maxrb(int lh) { return lh >= 9 ? 6 : 4; }
 
 __host__ __device__ constexpr int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+__host__ __device__ constexpr int mini(int a, int b) { return a < b ? a : b; }
 
-// rows per CTA of the one-pass path: at least 256 threads per CTA
-__host__ __device__ constexpr int rows_log2w(int l) {
-    return clampi(8 - (l - rows_log2e(l)), 0, 8);
-}
+// log2 of threads per transform
+__host__ __device__ constexpr int rows_log2t(int l) { return l - sched_rbits(l, rows_maxrb(l), 0); }
+__host__ __device__ constexpr int cols_log2t(int l) { return l - sched_rbits(l, cols_maxrb(l), 0); }
+__host__ __device__ constexpr int real_log2t(int lh) { return lh - sched_rbits(lh, real_maxrb(lh), 0); }
+
+// rows per CTA of the plain one-pass kernel: at least 256 threads per CTA
+__host__ __device__ constexpr int rows_log2w(int l) { return clampi(8 - rows_log2t(l), 0, 8); }
 // transforms per CTA of the strided families: <= 512 threads, <= 2^14 points per CTA,
-// at least `minw` transforms (coalescing width), at most 128
+// at least 2^log2minw transforms (coalescing width), at most 128
 __host__ __device__ constexpr int cols_log2w(int l, int log2minw) {
-    return clampi((9 - (l - cols_log2e(l))) < (14 - l) ? (9 - (l - cols_log2e(l))) : (14 - l),
-                  log2minw, 7);
+    return clampi(mini(9 - cols_log2t(l), 14 - l), log2minw, 7);
 }
-// rows per CTA of the real-row path (H-point core): 256 threads, and 4 rows when the shared
-// memory allows (32-byte runs of the m-major spectrum)
+// rows per CTA of the real-row path (H-point core): 128 threads, and 4 rows (32-byte runs of
+// the m-major spectrum) while the shared memory stays moderate
 __host__ __device__ constexpr int real_log2w(int lh) {
-    return clampi(8 - (lh - rows_log2e(lh)), lh >= 13 ? 0 : (lh == 12 ? 1 : 2), 7);
+    return clampi(7 - real_log2t(lh), lh >= 13 ? 0 : (lh == 12 ? 1 : 2), 7);
 }
 
 // Largest sizes of each family.
@@ -41,9 +45,15 @@ constexpr int kMaxLog2RealH = 14;    // real rows of up to 2^15 points
 
 // ---- dispatch -------------------------------------------------------------------------------
 // One-pass rows: nrows contiguous rows of 2^log2n points.  row_parity adds (-1)^row to the
-// chessboard (2-D row pass).
+// chessboard (2-D row pass).  Sizes 2^5..2^12 run the persistent bulk-copy kernel, whose
+// bounded waits report KERR_WAIT_TIMEOUT into *err after limit_ns nanoseconds.
 cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t nrows,
-                     const float2* tw, int flags, int row_parity, cudaStream_t s);
+                     const float2* tw, int flags, int row_parity, int* err, uint64_t limit_ns,
+                     cudaStream_t s);
+
+constexpr int kRowsTmaMinLog2 = 5;
+constexpr int kRowsTmaMaxLog2 = 12;
+constexpr int kRowsTmaStages = 2;
 
 // Strided columns: count columns of matrices [2^log2l][2^log2s] stored back to back.
 // elem_parity: 1 for the 2-D chessboard (-1)^(row+col), 0 for the four-step one (-1)^col.

@@ -10,12 +10,12 @@
 // 2 reads, so the scratch never needs clearing between calls.
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <mutex>
 #include <vector>
 
 #include "../../include/gbfft.h"
 #include "fft_kernel.cuh"
+#include "host_tables.h"
 #include "kernels.h"
 
 using namespace gbfft;
@@ -46,60 +46,6 @@ struct SizeTables {
 };
 SizeTables g_off[kNoAllocMaxLog2 + 1];
 
-const double kTwoPi = 6.283185307179586476925286766559005768;
-
-// (cos, sin)(2*pi*q/m) in double, reduced in integers to the first quadrant (quarter turns
-// exact), rounded once to float -- the same values the plan path's tables hold.
-float2 unit_root(int64_t q, int64_t m) {
-    q %= m;
-    if (q < 0) q += m;
-    if (m % 4 != 0) return make_float2(2 * q == m ? -1.f : 1.f, 0.f);
-    const int64_t qq = m / 4, quad = q / qq, a = q % qq;
-    double c, s;
-    if (a == 0) {
-        c = 1.0;
-        s = 0.0;
-    } else if (a <= qq / 2) {
-        c = std::cos(kTwoPi * (double)a / (double)m);
-        s = std::sin(kTwoPi * (double)a / (double)m);
-    } else {
-        c = std::sin(kTwoPi * (double)(qq - a) / (double)m);
-        s = std::cos(kTwoPi * (double)(qq - a) / (double)m);
-    }
-    double x, y;
-    switch (quad & 3) {
-        case 0: x = c; y = s; break;
-        case 1: x = -s; y = c; break;
-        case 2: x = -c; y = -s; break;
-        default: x = s; y = -c; break;
-    }
-    return make_float2((float)x, (float)y);
-}
-
-void pad32(std::vector<float2>& v) {
-    while (v.size() % 32) v.push_back(make_float2(0.f, 0.f));
-}
-
-size_t pass_tables(std::vector<float2>& v, int l) {
-    pad32(v);
-    const size_t off = v.size();
-    const int npass = l <= 4 ? 1 : (l + 3) / 4;
-    for (int p = 1; p < npass; ++p) {
-        const int rb = (l - 4 * p >= 4) ? 4 : l - 4 * p;
-        const int64_t R = int64_t(1) << rb, Ns = int64_t(1) << (4 * p);
-        for (int64_t m = 0; m < Ns; ++m)
-            for (int64_t r = 0; r < R; ++r) v.push_back(unit_root(m * r, Ns * R));
-    }
-    return off;
-}
-
-size_t roots(std::vector<float2>& v, int64_t count, int64_t step, int64_t m) {
-    pad32(v);
-    const size_t off = v.size();
-    for (int64_t q = 0; q < count; ++q) v.push_back(unit_root(q * step, m));
-    return off;
-}
-
 // Host tables of every supported size, laid out once (identical on every device).
 const std::vector<float2>& host_tables() {
     static std::vector<float2> v;
@@ -107,13 +53,13 @@ const std::vector<float2>& host_tables() {
     if (!built) {
         for (int l = kNoAllocMinLog2; l <= kNoAllocMaxLog2; ++l) {
             const int l1 = l / 2, l2 = l - l / 2, lowbits = (l + 1) / 2;
-            g_off[l].col = pass_tables(v, l1);
-            g_off[l].row = pass_tables(v, l2);
-            g_off[l].hi = roots(v, int64_t(1) << (l - lowbits), int64_t(1) << lowbits,
-                                int64_t(1) << l);
-            g_off[l].lo = roots(v, int64_t(1) << lowbits, 1, int64_t(1) << l);
+            g_off[l].col = host::append_pass_tables(v, l1, cols_maxrb(l1));
+            g_off[l].row = host::append_pass_tables(v, l2, cols_maxrb(l2));
+            g_off[l].hi = host::append_roots(v, int64_t(1) << (l - lowbits),
+                                             int64_t(1) << lowbits, int64_t(1) << l);
+            g_off[l].lo = host::append_roots(v, int64_t(1) << lowbits, 1, int64_t(1) << l);
         }
-        pad32(v);
+        host::align_table(v);
         built = true;
     }
     return v;

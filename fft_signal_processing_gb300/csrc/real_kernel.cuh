@@ -21,7 +21,8 @@ namespace gbfft {
 template <class C>
 struct RealCfg {
     // per-row shared memory: the exchange buffer, or H+1 padded slots for the recombination
-    static constexpr int SREAL = (C::SROW > spad_size(C::N) + 1) ? C::SROW : spad_size(C::N) + 1;
+    static constexpr int SREAL =
+        (C::SROW > spad_size(C::N, C::LP) + 1) ? C::SROW : spad_size(C::N, C::LP) + 1;
     static constexpr size_t SMEM_BYTES = (size_t)SREAL * C::W * sizeof(float2);
 };
 
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(C::THREADS)
     for (int b = 0; b < BL; ++b) {
         const int j = t + b * C::T;
 #pragma unroll
-        for (int r = 0; r < RL; ++r) sb[spad(j + r * SL)] = v[b * RL + r];
+        for (int r = 0; r < RL; ++r) sb[spad<C::LP>(j + r * SL)] = v[b * RL + r];
     }
     __syncthreads();
 
@@ -82,8 +83,8 @@ __global__ void __launch_bounds__(C::THREADS)
         const int64_t rr = (int64_t)blockIdx.x * C::W + wr;
         if (rr >= nrows) continue;
         const float2* s = smem + wr * SREAL;
-        const float2 zk = s[spad(k)];
-        const float2 zm = s[spad((H - k) & (H - 1))];
+        const float2 zk = s[spad<C::LP>(k)];
+        const float2 zm = s[spad<C::LP>((H - k) & (H - 1))];
         const float2 zc = make_float2(zm.x, -zm.y);                   // conj Z_{H-k}
         const float2 xe = make_float2(0.5f * (zk.x + zc.x), 0.5f * (zk.y + zc.y));
         const float2 d = make_float2(0.5f * (zk.x - zc.x), 0.5f * (zk.y - zc.y));
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(C::THREADS)
             x = ldg_stream(in + (mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k));
             if (k == 0) x.y = 0.f;
         }
-        smem[wr * SREAL + spad(k)] = x;
+        smem[wr * SREAL + spad<C::LP>(k)] = x;
     }
     __syncthreads();
 
@@ -141,8 +142,8 @@ __global__ void __launch_bounds__(C::THREADS)
 #pragma unroll
         for (int r = 0; r < R0; ++r) {
             const int k = j + r * S0;
-            const float2 xk = sb[spad(k)];
-            const float2 xm = sb[spad(H - k)];
+            const float2 xk = sb[spad<C::LP>(k)];
+            const float2 xm = sb[spad<C::LP>(H - k)];
             const float2 xc = make_float2(xm.x, -xm.y);             // conj X_{H-k}
             const float2 s = cadd(xk, xc);
             const float2 wd = ctw<+1>(csub(xk, xc), __ldg(twr + k));  // e^{+i th} (X_k - conj X_{H-k})

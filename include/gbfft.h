@@ -97,6 +97,17 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
  */
 int fft_plan_set_band_limit(fft_plan plan, int64_t mmax);
 
+/*
+ * fft_plan_set_wait_timeout - time limit, in nanoseconds, of every device-side wait of the
+ * plan's kernels (waits for asynchronous bulk copies into shared memory).  A wait that runs out
+ * makes its CTA record the failure in the plan's device error word, wait (for at most 1 s) for
+ * its own copies still in flight, and exit; fft_plan_check then returns FFT_ERR_TIMEOUT and the
+ * outputs of that execution are undefined.  The default is 2 s.  ns = 0 is a diagnostic setting
+ * that makes every such wait give up at once without polling, which exercises this error path
+ * without a real stall.  Host only.  Returns FFT_OK or FFT_ERR_INVALID_ARG (NULL plan).
+ */
+int fft_plan_set_wait_timeout(fft_plan plan, uint64_t ns);
+
 /* fft_plan_workspace_bytes - device bytes the plan holds besides its twiddle tables
  * (informational).  Returns FFT_OK or FFT_ERR_INVALID_ARG. */
 int fft_plan_workspace_bytes(fft_plan plan, size_t* bytes);

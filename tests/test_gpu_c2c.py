@@ -155,3 +155,24 @@ def test_exec_argument_errors():
     big = m.Plan(1 << 16, 2)
     assert big.workspace_bytes() == 2 * (1 << 16) * 8
     assert "fourstep" in big.describe()
+
+
+# ---- bounded device waits: forced timeout is reported and the context stays usable ----------
+@pytest.mark.parametrize("log2n", [5, 10, 12])
+def test_wait_timeout_reported_then_recovers(log2n):
+    m = fx()
+    n, batch = 1 << log2n, 333
+    p = m.Plan(n, batch, 1, m.FORWARD)
+    x = rng_c64(6000 + log2n, batch, n)
+    xd = torch.from_numpy(x).cuda()
+    p.set_wait_timeout(0)  # every bulk-copy wait gives up at once
+    p.c2c(xd)
+    with pytest.raises(m.GbfftError) as ei:
+        p.check()
+    assert ei.value.status == m.FFT_ERR_TIMEOUT
+    p.check()  # the error word was cleared
+    p.set_wait_timeout(2_000_000_000)
+    y = p.c2c(xd)
+    torch.cuda.synchronize()
+    p.check()
+    assert_parity(y.cpu().numpy(), oracle.transform(x, -1), n, "after timeout")
