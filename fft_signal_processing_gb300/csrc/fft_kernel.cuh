@@ -8,7 +8,7 @@
 // Algorithm: Stockham autosort (natural order in and out, no bit reversal), decimation in
 // time, as in the radix-2 / radix-4 Stockham kernels of "src/sht/wgsl/fourier.ts"
 // (stockham(), stockham4()) and Mota, "High Performance Fourier Transforms on GPUs with
-// GLSL", §2.5 (radix-4 Stockham), generalised to radix 16 per pass in registers (higher radix
+// GLSL", §2.5 (radix-4 Stockham), generalised to radix 64 per pass in registers (higher radix
 // is the direction Mota §5.2 names as future work).  Pass p has radix R and span Ns (the
 // product of the earlier radices).  Butterfly j (0 <= j < N/R) reads element j + r*N/R,
 // r < R, multiplies element r by w_{Ns*R}^{(j mod Ns)*r}, does an R-point DFT in registers and
@@ -51,50 +51,59 @@ struct FftCfg {
     }
 };
 
-template <class C, int DIR, int P>
-__device__ __forceinline__ void pass_twiddle(float2* v, int j, const float2* __restrict__ tw) {
-    constexpr int RB = C::rbits(P);
-    constexpr int R = 1 << RB;
+// Twiddles of pass P for butterfly j: the A low and B high powers of w = w_{Ns*R}^(j mod Ns).
+template <class C, int P>
+struct PassTw {
+    static constexpr int RB = C::rbits(P);
+    static constexpr int A = tw_lo_count(RB);
+    static constexpr int S = tw_stride(RB);
+    float2 w[S];
+};
+
+template <class C, int P>
+__device__ __forceinline__ void load_twiddles(PassTw<C, P>& pt, int j,
+                                              const float2* __restrict__ tw) {
     constexpr int Ns = C::span(P);
-    constexpr int A = tw_lo_count(RB);
-    constexpr int B = tw_hi_count(RB);
-    constexpr int S = tw_stride(RB);
+    constexpr int S = PassTw<C, P>::S;
     const float4* w4 = reinterpret_cast<const float4*>(tw + tw_pass_off(C::LOG2N, C::MAXRB, P) +
                                                        (j & (Ns - 1)) * S);
-    float2 w[S];
 #pragma unroll
     for (int i = 0; i < S / 2; ++i) {
         const float4 q = __ldg(w4 + i);
-        w[2 * i] = make_float2(q.x, q.y);
-        w[2 * i + 1] = make_float2(q.z, q.w);
+        pt.w[2 * i] = make_float2(q.x, q.y);
+        pt.w[2 * i + 1] = make_float2(q.z, q.w);
     }
+}
+
+// v[r] *= w^r for r < R, with w^r = w^a * w^(A*b), r = a + A*b.
+template <class C, int DIR, int P>
+__device__ __forceinline__ void apply_twiddles(float2* v, const PassTw<C, P>& pt) {
+    constexpr int R = C::radix(P);
+    constexpr int A = PassTw<C, P>::A;
 #pragma unroll
     for (int r = 1; r < R; ++r) {
         const int a = r % A, b = r / A;
         float2 f;
         if (b == 0)
-            f = w[a];
+            f = pt.w[a];
         else if (a == 0)
-            f = w[A + b];
+            f = pt.w[A + b];
         else
-            f = cmul(w[a], w[A + b]);
+            f = cmul(pt.w[a], pt.w[A + b]);
         v[r] = ctw<DIR>(v[r], f);
     }
-    (void)B;
 }
 
-// Passes P..NPASS-1 on register data v (v[b*R + r] is element r of butterfly j = t + b*T).
-// sb points at this transform's first shared-memory slot; slots are C::SS apart.
+// Passes P..NPASS-1 on register data v (v[b*R + r] is element r of butterfly j = t + b*T);
+// pass P's twiddles have already been applied.  sb points at this transform's first
+// shared-memory slot; slots are C::SS apart.  The next pass's twiddles are fetched before the
+// exchange barrier so that their latency hides behind it.
 template <class C, int DIR, int P>
 __device__ __forceinline__ void run_passes(float2 (&v)[C::E], int t, float2* sb,
                                            const float2* __restrict__ tw) {
     constexpr int R = C::radix(P);
     constexpr int B = C::E / R;
     constexpr int Ns = C::span(P);
-    if constexpr (P > 0) {
-#pragma unroll
-        for (int b = 0; b < B; ++b) pass_twiddle<C, DIR, P>(v + b * R, t + b * C::T, tw);
-    }
 #pragma unroll
     for (int b = 0; b < B; ++b) dft_reg<R, DIR>(v + b * R);
     if constexpr (P + 1 < C::NPASS) {
@@ -106,15 +115,19 @@ __device__ __forceinline__ void run_passes(float2 (&v)[C::E], int t, float2* sb,
 #pragma unroll
             for (int r = 0; r < R; ++r) sb[spad<C::LP>(base + r * Ns) * C::SS] = v[b * R + r];
         }
-        __syncthreads();
         constexpr int R2 = C::radix(P + 1);
         constexpr int B2 = C::E / R2;
         constexpr int S2 = C::N / R2;
+        PassTw<C, P + 1> pt[B2];
+#pragma unroll
+        for (int b = 0; b < B2; ++b) load_twiddles<C, P + 1>(pt[b], t + b * C::T, tw);
+        __syncthreads();
 #pragma unroll
         for (int b = 0; b < B2; ++b) {
             const int j = t + b * C::T;
 #pragma unroll
             for (int r = 0; r < R2; ++r) v[b * R2 + r] = sb[spad<C::LP>(j + r * S2) * C::SS];
+            apply_twiddles<C, DIR, P + 1>(v + b * R2, pt[b]);
         }
         run_passes<C, DIR, P + 1>(v, t, sb, tw);
     }
