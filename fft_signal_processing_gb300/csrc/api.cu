@@ -130,6 +130,15 @@ Geo rows_geo(int l) {
     const int w = rows_log2w(l);
     return {(1 << rows_log2t(l)) << w, 1 << w, padded_bytes(l, rows_maxrb(l), w)};
 }
+Geo cols_geo(int l, int log2s) {
+    if (cols_use_tma(l, log2s)) {
+        const int w = cols_tma_log2w(l), lp = sched_rbits(l, cols_tma_maxrb(l), 0);
+        const size_t stage = (size_t)std::max(spad_size(1 << l, lp), 1 << l) * (1u << w) * 8u;
+        return {(1 << (l - lp)) << w, 1 << w, stage};
+    }
+    const int w = cols_log2w(l, 0);
+    return {(1 << cols_log2t(l)) << w, 1 << w, padded_bytes(l, cols_maxrb(l), w)};
+}
 Geo strided_geo(int l, int log2minw) {
     const int w = cols_log2w(l, log2minw);
     return {(1 << cols_log2t(l)) << w, 1 << w, padded_bytes(l, cols_maxrb(l), w)};
@@ -155,19 +164,19 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
             break;
         }
         case PATH_FOURSTEP: {
-            Geo g1 = strided_geo(s.log2n1, 0), g2 = strided_geo(s.log2n2, 2);
+            Geo g1 = cols_geo(s.log2n1, s.log2n2), g2 = strided_geo(s.log2n2, 2);
             snprintf(buf, sizeof buf,
                      "path=fourstep n=%lld batch=%lld %s shift=%d n1=%d n2=%d kernels=2 "
                      "pass1=columns(radix=%s threads=%d cols_per_cta=%d smem=%zu) "
                      "pass2=rows_transposed(radix=%s threads=%d rows_per_cta=%d smem=%zu)",
                      (long long)s.n, (long long)s.batch, dir, s.shift, 1 << s.log2n1,
-                     1 << s.log2n2, radix_string(s.log2n1, cols_maxrb(s.log2n1)).c_str(), g1.threads,
+                     1 << s.log2n2, radix_string(s.log2n1, cols_pass_maxrb(s.log2n1, s.log2n2)).c_str(), g1.threads,
                      g1.per_cta, g1.smem, radix_string(s.log2n2, cols_maxrb(s.log2n2)).c_str(),
                      g2.threads, g2.per_cta, g2.smem);
             break;
         }
         case PATH_2D: {
-            Geo g1 = rows_geo(s.log2n), g2 = strided_geo(s.log2n, 0);
+            Geo g1 = rows_geo(s.log2n), g2 = cols_geo(s.log2n, s.log2n);
             snprintf(buf, sizeof buf,
                      "path=2d n=%lldx%lld batch=%lld %s shift=%d radix=%s kernels=2 "
                      "rows(threads=%d rows_per_cta=%d smem=%zu) "
@@ -282,10 +291,10 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
             break;
         case PATH_2D:
             p->off_a = append_pass_tables(tw, s.log2n, rows_maxrb(s.log2n));  // row pass
-            p->off_b = append_pass_tables(tw, s.log2n, cols_maxrb(s.log2n));  // column pass
+            p->off_b = append_pass_tables(tw, s.log2n, cols_pass_maxrb(s.log2n, s.log2n));
             break;
         case PATH_FOURSTEP: {
-            p->off_a = append_pass_tables(tw, s.log2n1, cols_maxrb(s.log2n1));
+            p->off_a = append_pass_tables(tw, s.log2n1, cols_pass_maxrb(s.log2n1, s.log2n2));
             p->off_b = append_pass_tables(tw, s.log2n2, cols_maxrb(s.log2n2));
             const int64_t nlo = int64_t(1) << s.lowbits, nhi = int64_t(1) << (s.log2n - s.lowbits);
             p->off_hi = append_roots(tw, nhi, nlo, s.n);  // w_n^{qh * 2^lowbits}
@@ -367,7 +376,8 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
             const int64_t n1 = int64_t(1) << s.log2n1, n2 = int64_t(1) << s.log2n2;
             e = run_cols(s.log2n1, s.direction, x, wk, s.batch * n2, s.log2n2,
                          p->d_tw + p->off_a, (s.shift && fwd) ? KF_CHESS_LOAD : 0, 0,
-                         p->d_tw + p->off_hi, p->d_tw + p->off_lo, s.lowbits, st);
+                         p->d_tw + p->off_hi, p->d_tw + p->off_lo, s.lowbits, p->d_err,
+                         p->wait_limit_ns, st);
             if (e == cudaSuccess)
                 e = run_rows_t(s.log2n2, s.direction, wk, y, s.batch * n1, s.log2n1,
                                p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0, st);
@@ -380,7 +390,7 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
             if (e == cudaSuccess)
                 e = run_cols(s.log2n, s.direction, y, y, s.batch * n, s.log2n,
                              p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0, 1,
-                             nullptr, nullptr, 0, st);
+                             nullptr, nullptr, 0, p->d_err, p->wait_limit_ns, st);
             break;
         }
         default:

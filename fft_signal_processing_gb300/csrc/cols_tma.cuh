@@ -1,0 +1,220 @@
+// Persistent column-tile kernel with TMA tensor staging (2-D column pass; four-step pass 1).
+//
+// The data are matrices [L rows][S columns] of complex64 stored back to back (nmat of them);
+// every column gets an L-point transform.  A tile is W adjacent columns of one matrix
+// (W*8 bytes of every row).  Each CTA walks a strided sequence of tiles; one thread loads a
+// tile with L/BH tensor copies (cp.async.bulk.tensor.3d, box W x BH x 1 of a 3-D tensor map
+// over (column, row, matrix)) into a shared-memory stage that completes on an mbarrier.  The
+// copy engine does the strided gathering, so the SM issues one instruction per box instead of
+// one load per row segment.  The stage lands dense ([row][W]), is read into registers, then
+// doubles as the padded exchange buffer of the tile's transforms (Stockham radix passes as in
+// fft_kernel.cuh, the W columns interleaved).  Results are stored from registers (W-wide runs
+// per row), optionally multiplied by the four-step twiddle w_{L*S}^{c*k1}, and the stage is
+// refilled with the next tile.  Several CTAs share an SM, so the copies of some overlap the
+// compute of others.  Every wait is bounded; on expiry the CTA records KERR_WAIT_TIMEOUT,
+// drains its copy and exits.
+#pragma once
+
+#include <cuda.h>
+
+#include "fft_kernel.cuh"
+#include "tma.cuh"
+
+namespace gbfft {
+
+// 3-D tiled tensor copy global -> shared, completing on `bar`.  Coordinates are in elements
+// (x = column, y = row, z = matrix); x * 8 bytes is a multiple of 16 by construction (x is a
+// multiple of W >= 2).
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+template <int LOG2L_, int MAXRB_, int LOG2W_>
+struct ColsTmaCfg {
+    using C = FftCfg<LOG2L_, MAXRB_, LOG2W_, false>;  // the W columns are adjacent lanes
+    static constexpr int L = C::N;
+    static constexpr int W = C::W;
+    static constexpr int BH = L < 256 ? L : 256;  // rows per tensor box
+    static constexpr int NBOX = L / BH;
+    static constexpr int STAGE = (C::SROW > L ? C::SROW : L) * W;  // float2
+    static constexpr uint32_t TILE_BYTES = (uint32_t)L * W * 8u;
+    static constexpr size_t SMEM_BYTES = (size_t)STAGE * sizeof(float2);
+    static_assert(W >= 2, "tensor boxes are at least 16 bytes wide");
+    static_assert((BH * W * 8) % 128 == 0, "boxes stay 128-byte aligned in shared memory");
+};
+
+struct ColsTwiddle {
+    const float2* hi;  // w_{L*S}^q = hi[q >> lowbits] * lo[q & lowmask]
+    const float2* lo;
+    int lowbits;
+};
+
+template <class RC, int DIR, bool TW>
+__global__ void __launch_bounds__(RC::C::THREADS)
+    k_cols_tma(const __grid_constant__ CUtensorMap tmap, float2* out, int64_t nmat, int log2s,
+               const float2* __restrict__ tw, int flags, int elem_parity, ColsTwiddle twd,
+               int* err, uint64_t limit_ns) {
+    using C = typename RC::C;
+    constexpr int L = RC::L;
+    constexpr int W = RC::W;
+    extern __shared__ __align__(128) float2 smem[];
+    __shared__ uint64_t bar;
+
+    const int tid = (int)threadIdx.x;
+    const int w = tid % W;
+    const int t = tid / W;
+    const int64_t S = int64_t(1) << log2s;
+    const int64_t tiles_per_mat = S / W;
+    const int64_t ntiles = nmat * tiles_per_mat;
+    const int64_t t0 = blockIdx.x, tstride = gridDim.x;
+
+    auto issue = [&](int64_t tile) {
+        const int z = (int)(tile / tiles_per_mat);
+        const int x = (int)((tile % tiles_per_mat) * W);
+        mbar_arrive_expect_tx(&bar, RC::TILE_BYTES);
+#pragma unroll 1
+        for (int b = 0; b < RC::NBOX; ++b)
+            tma_load_3d(smem + b * RC::BH * W, &tmap, x, b * RC::BH, z, &bar);
+    };
+
+    if (tid == 0) {
+        prefetch_tensormap(&tmap);
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && t0 < ntiles) issue(t0);
+
+    constexpr int R0 = C::radix(0);
+    constexpr int B0 = C::E / R0;
+    constexpr int S0 = C::N / R0;
+    constexpr int RL = C::radix(C::NPASS - 1);
+    constexpr int BL = C::E / RL;
+    constexpr int SL = C::N / RL;
+
+    for (int64_t it = 0;; ++it) {
+        const int64_t tile = t0 + it * tstride;
+        if (tile >= ntiles) break;
+        const bool ok = mbar_wait_bounded(&bar, (uint32_t)(it & 1), limit_ns);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                if (err) atomicExch(err, KERR_WAIT_TIMEOUT);
+                mbar_wait_bounded(&bar, (uint32_t)(it & 1), kDrainLimitNs);  // the copy in flight
+            }
+            return;
+        }
+        const int64_t mat = tile / tiles_per_mat;
+        const int64_t c = (tile % tiles_per_mat) * W + w;  // column of this thread's transform
+        const int cp = (int)(c & 1);
+
+        float2 v[C::E];
+#pragma unroll
+        for (int b = 0; b < B0; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < R0; ++r) {
+                const int e = j + r * S0;
+                float2 x = smem[e * W + w];  // dense [row][W] tile written by the copy engine
+                if (flags & KF_CHESS_LOAD) x = neg_if(x, (e * elem_parity + cp) & 1);
+                v[b * R0 + r] = x;
+            }
+        }
+        __syncthreads();  // the stage becomes the exchange buffer
+
+        run_passes<C, DIR, 0>(v, t, smem + w, tw);
+
+        float2* dst = out + (mat << (log2s + RC::C::LOG2N)) + c;
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < RL; ++r) {
+                const int k = j + r * SL;
+                float2 y = v[b * RL + r];
+                if constexpr (TW) {
+                    const uint32_t q = ((uint32_t)c * (uint32_t)k) &
+                                       ((1u << (log2s + RC::C::LOG2N)) - 1u);
+                    const float2 f = cmul(__ldg(twd.hi + (q >> twd.lowbits)),
+                                          __ldg(twd.lo + (q & ((1u << twd.lowbits) - 1u))));
+                    y = ctw<DIR>(y, f);
+                }
+                if (flags & KF_CHESS_STORE) y = neg_if(y, (k * elem_parity + cp) & 1);
+                stg_stream(dst + ((int64_t)k << log2s), y);
+            }
+        }
+        __syncthreads();  // every thread is done with the stage
+        if (tid == 0) {
+            const int64_t nt = tile + tstride;
+            if (nt < ntiles) {
+                fence_proxy_async_smem();
+                issue(nt);
+            }
+        }
+    }
+}
+
+// Encode the 3-D tensor map (column, row, matrix) of `base` and launch.  The map is encoded
+// per call on the host (it holds the global address).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();  // resolved once through the runtime (dispatch.cu)
+
+template <class RC, int DIR, bool TW>
+cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log2s,
+                            const float2* tw, int flags, int elem_parity, ColsTwiddle twd,
+                            int* err, uint64_t limit_ns, cudaStream_t stream) {
+    auto kern = k_cols_tma<RC, DIR, TW>;
+    static int configured_dev = -1;
+    static int per_sm = 0, num_sms = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_dev != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)RC::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RC::C::THREADS,
+                                                              RC::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        configured_dev = dev;
+    }
+    EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const int64_t S = int64_t(1) << log2s;
+    if (S < RC::W) return cudaErrorInvalidValue;
+    CUtensorMap map;
+    const cuuint64_t dims[3] = {(cuuint64_t)S, (cuuint64_t)RC::L, (cuuint64_t)nmat};
+    const cuuint64_t strides[2] = {(cuuint64_t)S * 8u, (cuuint64_t)S * RC::L * 8u};
+    const cuuint32_t box[3] = {(cuuint32_t)RC::W, (cuuint32_t)RC::BH, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 3, const_cast<float2*>(in), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int64_t ntiles = nmat * (S / RC::W);
+    const int64_t resident = (int64_t)per_sm * num_sms;
+    const int64_t grid = ntiles < resident ? ntiles : resident;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(
+        map, out, nmat, log2s, tw, flags, elem_parity, twd, err, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace gbfft

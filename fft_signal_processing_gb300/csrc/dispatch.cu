@@ -1,8 +1,23 @@
 // Run-time dispatch from (family, log2 size) to the per-size entry functions.
 #include "inst_entries.h"
+#include "cols_tma.cuh"
 #include "kernels.h"
 
 namespace gbfft {
+
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link against libcuda).
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
 
 cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t nrows,
                      const float2* tw, int flags, int rp, int* err, uint64_t lim,
@@ -18,10 +33,12 @@ cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t 
 
 cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t count,
                      int log2s, const float2* tw, int flags, int ep, const float2* hi,
-                     const float2* lo, int lowbits, cudaStream_t s) {
+                     const float2* lo, int lowbits, int* err, uint64_t lim, cudaStream_t s) {
     switch (log2l) {
-#define GBFFT_C(L) \
-    case L: return cols_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo, lowbits, s);
+#define GBFFT_C(L)                                                                          \
+    case L:                                                                                 \
+        return cols_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo, lowbits, err, \
+                              lim, s);
         GBFFT_COLS_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;

@@ -1,6 +1,5 @@
-// Kernel instantiations: GBFFT_DEF_COLS(11) GBFFT_DEF_COLS(12).
+// Kernel instantiations: GBFFT_DEF_COLS(11).
 #include "inst_defs.cuh"
 #include "inst_entries.h"
 
 GBFFT_DEF_COLS(11)
-GBFFT_DEF_COLS(12)

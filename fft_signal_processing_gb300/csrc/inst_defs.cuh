@@ -6,6 +6,7 @@
 #include "fft_kernel.cuh"
 #include "kernels.h"
 #include "real_kernel.cuh"
+#include "cols_tma.cuh"
 #include "rows_tma.cuh"
 
 namespace gbfft {
@@ -29,10 +30,20 @@ cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2
 template <int L, int DIR, bool TW>
 cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, const float2* tw,
                       int flags, int ep, const float2* hi, const float2* lo, int lowbits,
-                      cudaStream_t s) {
-    using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 0), false>;
-    MapCols<TW> m{count, log2s, L, ep, hi, lo, lowbits};
-    return launch_fft<C, DIR, MapCols<TW>>(in, out, m, tw, flags, s);
+                      int* err, uint64_t lim, cudaStream_t s) {
+    if constexpr (L >= kColsTmaMinLog2 && L <= kColsTmaMaxLog2) {
+        // the planners only ask for matrices at least one tile wide at these sizes
+        if (!cols_use_tma(L, log2s)) return cudaErrorInvalidValue;
+        using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
+        return launch_cols_tma<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags, ep,
+                                            ColsTwiddle{hi, lo, lowbits}, err, lim, s);
+    } else {
+        (void)err;
+        (void)lim;
+        using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 0), false>;
+        MapCols<TW> m{count, log2s, L, ep, hi, lo, lowbits};
+        return launch_fft<C, DIR, MapCols<TW>>(in, out, m, tw, flags, s);
+    }
 }
 
 template <int L, int DIR>
@@ -60,16 +71,16 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), true>;
     cudaError_t gbfft::cols_entry_##L(int dir, const float2* in, float2* out, int64_t count,    \
                                       int log2s, const float2* tw, int flags, int ep,           \
                                       const float2* hi, const float2* lo, int lowbits,          \
-                                      cudaStream_t s) {                                         \
+                                      int* err, uint64_t lim, cudaStream_t s) {                 \
         if (hi)                                                                                 \
             return dir < 0 ? cols_impl<L, -1, true>(in, out, count, log2s, tw, flags, ep, hi,   \
-                                                    lo, lowbits, s)                             \
+                                                    lo, lowbits, err, lim, s)                   \
                            : cols_impl<L, +1, true>(in, out, count, log2s, tw, flags, ep, hi,   \
-                                                    lo, lowbits, s);                            \
+                                                    lo, lowbits, err, lim, s);                  \
         return dir < 0 ? cols_impl<L, -1, false>(in, out, count, log2s, tw, flags, ep, hi, lo,  \
-                                                 lowbits, s)                                    \
+                                                 lowbits, err, lim, s)                          \
                        : cols_impl<L, +1, false>(in, out, count, log2s, tw, flags, ep, hi, lo,  \
-                                                 lowbits, s);                                   \
+                                                 lowbits, err, lim, s);                         \
     }
 
 #define GBFFT_DEF_ROWS_T(L)                                                                    \

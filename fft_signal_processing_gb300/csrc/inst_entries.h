@@ -13,8 +13,8 @@ namespace gbfft {
 #define GBFFT_X_COLS(L)                                                                    \
     cudaError_t cols_entry_##L(int dir, const float2* in, float2* out, int64_t count,       \
                                int log2s, const float2* tw, int flags, int ep,              \
-                               const float2* hi, const float2* lo, int lowbits,             \
-                               cudaStream_t s);
+                               const float2* hi, const float2* lo, int lowbits, int* err,   \
+                               uint64_t lim, cudaStream_t s);
 #define GBFFT_X_ROWS_T(L)                                                                  \
     cudaError_t rows_t_entry_##L(int dir, const float2* in, float2* out, int64_t count,     \
                                  int log2n1, const float2* tw, int flags, cudaStream_t s);

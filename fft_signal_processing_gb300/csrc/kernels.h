@@ -58,9 +58,25 @@ constexpr int kRowsTmaStages = 1;  // one stage per CTA: six CTAs per SM at 2^12
 // Strided columns: count columns of matrices [2^log2l][2^log2s] stored back to back.
 // elem_parity: 1 for the 2-D chessboard (-1)^(row+col), 0 for the four-step one (-1)^col.
 // With hi/lo non-NULL, output k1 of column c is multiplied by w_{L*S}^{c*k1} (four-step).
+// Columns of 2^7..2^12 points with at least one full tile per matrix run the persistent
+// TMA-staged tile kernel (bounded waits reporting into *err, which may be NULL).
 cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t count,
                      int log2s, const float2* tw, int flags, int elem_parity, const float2* hi,
-                     const float2* lo, int lowbits, cudaStream_t s);
+                     const float2* lo, int lowbits, int* err, uint64_t limit_ns, cudaStream_t s);
+
+// Column tiles of the TMA kernel: W = 8192/L columns (at least 2, at most 64), radix up to 64.
+__host__ __device__ constexpr int cols_tma_log2w(int l) { return clampi(13 - l, 1, 6); }
+__host__ __device__ constexpr int cols_tma_maxrb(int l) { return l >= 9 ? 6 : 4; }
+constexpr int kColsTmaMinLog2 = 7;
+constexpr int kColsTmaMaxLog2 = 12;
+// the TMA tile kernel serves a column pass iff its tile fits in one matrix row
+__host__ __device__ constexpr bool cols_use_tma(int l, int log2s) {
+    return l >= kColsTmaMinLog2 && l <= kColsTmaMaxLog2 && log2s >= cols_tma_log2w(l);
+}
+// twiddle-table schedule (largest radix) of a column pass
+__host__ __device__ constexpr int cols_pass_maxrb(int l, int log2s) {
+    return cols_use_tma(l, log2s) ? cols_tma_maxrb(l) : cols_maxrb(l);
+}
 
 // Four-step pass 2: count rows of 2^log2n points, row tr = k1 + N1*(tr div N1) written
 // transposed into X[k1 + N1*k2] of its 2^(log2n1+log2n)-point transform.

@@ -20,8 +20,6 @@
 
 namespace gbfft {
 
-constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s for draining copies after a timeout
-
 template <int LOG2N_, int MAXRB_, int NST_>
 struct RowsTmaCfg {
     static constexpr int LOG2N = LOG2N_;
@@ -87,7 +85,7 @@ __global__ void __launch_bounds__(RC::C::THREADS)
         const bool ok = mbar_wait_bounded(&bars[s], parity, limit_ns);
         if (__syncthreads_or(!ok)) {
             if (tid == 0) {
-                atomicExch(err, KERR_WAIT_TIMEOUT);
+                if (err) atomicExch(err, KERR_WAIT_TIMEOUT);
                 for (int k = 0; k < NST; ++k) {  // copies still in flight: iterations it..it+NST-1
                     const int64_t ik = it + k;
                     if (blk0 + ik * bstride < nblocks)

@@ -75,6 +75,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s for draining copies after a timeout
+
 // Error word values written by kernels (read and cleared by fft_plan_check).
 enum : int { KERR_WAIT_TIMEOUT = 1 };
 
