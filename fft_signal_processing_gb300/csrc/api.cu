@@ -139,6 +139,12 @@ Geo cols_geo(int l, int log2s) {
     const int w = cols_log2w(l, 0);
     return {(1 << cols_log2t(l)) << w, 1 << w, padded_bytes(l, cols_maxrb(l), w)};
 }
+Geo rowst_geo(int l) {
+    const int w = rowst_log2w(l), lp = sched_rbits(l, rowst_maxrb(l), 0);
+    const size_t a = (size_t)((1 << l) + (w >= 3 ? 2 : 16 >> w)) << w;
+    const size_t b = (size_t)spad_size(1 << l, lp) << w;
+    return {(1 << (l - lp)) << w, 1 << w, std::max(a, b) * 8u};
+}
 Geo strided_geo(int l, int log2minw) {
     const int w = cols_log2w(l, log2minw);
     return {(1 << cols_log2t(l)) << w, 1 << w, padded_bytes(l, cols_maxrb(l), w)};
@@ -164,14 +170,14 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
             break;
         }
         case PATH_FOURSTEP: {
-            Geo g1 = cols_geo(s.log2n1, s.log2n2), g2 = strided_geo(s.log2n2, 2);
+            Geo g1 = cols_geo(s.log2n1, s.log2n2), g2 = rowst_geo(s.log2n2);
             snprintf(buf, sizeof buf,
                      "path=fourstep n=%lld batch=%lld %s shift=%d n1=%d n2=%d kernels=2 "
                      "pass1=columns(radix=%s threads=%d cols_per_cta=%d smem=%zu) "
                      "pass2=rows_transposed(radix=%s threads=%d rows_per_cta=%d smem=%zu)",
                      (long long)s.n, (long long)s.batch, dir, s.shift, 1 << s.log2n1,
                      1 << s.log2n2, radix_string(s.log2n1, cols_pass_maxrb(s.log2n1, s.log2n2)).c_str(), g1.threads,
-                     g1.per_cta, g1.smem, radix_string(s.log2n2, cols_maxrb(s.log2n2)).c_str(),
+                     g1.per_cta, g1.smem, radix_string(s.log2n2, rowst_maxrb(s.log2n2)).c_str(),
                      g2.threads, g2.per_cta, g2.smem);
             break;
         }
@@ -295,7 +301,7 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
             break;
         case PATH_FOURSTEP: {
             p->off_a = append_pass_tables(tw, s.log2n1, cols_pass_maxrb(s.log2n1, s.log2n2));
-            p->off_b = append_pass_tables(tw, s.log2n2, cols_maxrb(s.log2n2));
+            p->off_b = append_pass_tables(tw, s.log2n2, rowst_maxrb(s.log2n2));
             const int64_t nlo = int64_t(1) << s.lowbits, nhi = int64_t(1) << (s.log2n - s.lowbits);
             p->off_hi = append_roots(tw, nhi, nlo, s.n);  // w_n^{qh * 2^lowbits}
             p->off_lo = append_roots(tw, nlo, 1, s.n);    // w_n^{ql}
@@ -380,7 +386,8 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                          p->wait_limit_ns, st);
             if (e == cudaSuccess)
                 e = run_rows_t(s.log2n2, s.direction, wk, y, s.batch * n1, s.log2n1,
-                               p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0, st);
+                               p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0,
+                               p->d_err, p->wait_limit_ns, st);
             break;
         }
         case PATH_2D: {

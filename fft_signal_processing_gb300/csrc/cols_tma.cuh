@@ -8,11 +8,12 @@
 // copy engine does the strided gathering, so the SM issues one instruction per box instead of
 // one load per row segment.  The stage lands dense ([row][W]), is read into registers, then
 // doubles as the padded exchange buffer of the tile's transforms (Stockham radix passes as in
-// fft_kernel.cuh, the W columns interleaved).  Results are stored from registers (W-wide runs
-// per row), optionally multiplied by the four-step twiddle w_{L*S}^{c*k1}, and the stage is
-// refilled with the next tile.  Several CTAs share an SM, so the copies of some overlap the
-// compute of others.  Every wait is bounded; on expiry the CTA records KERR_WAIT_TIMEOUT,
-// drains its copy and exits.
+// fft_kernel.cuh, the W columns interleaved).  Results, optionally multiplied by the four-step
+// twiddle w_{L*S}^{c*k1}, go back into the stage in the dense tile layout and leave with tensor
+// stores (the copy engine writes the W-wide row runs), after which the stage is refilled with
+// the next tile.  Several CTAs share an SM, so the copies of some overlap the compute of
+// others.  Every mbarrier wait is bounded; on expiry the CTA records KERR_WAIT_TIMEOUT, drains
+// its copy and exits.
 #pragma once
 
 #include <cuda.h>
@@ -34,6 +35,21 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* m
         : "memory");
 }
 
+// 3-D tiled tensor copy shared -> global (bulk async group of the issuing thread).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z,
+                                             const void* src_smem) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_addr(src_smem))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The issuing thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_smem_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -48,6 +64,8 @@ struct ColsTmaCfg {
     static constexpr int STAGE = (C::SROW > L ? C::SROW : L) * W;  // float2
     static constexpr uint32_t TILE_BYTES = (uint32_t)L * W * 8u;
     static constexpr size_t SMEM_BYTES = (size_t)STAGE * sizeof(float2);
+    // CTAs per SM the register allocation must allow (shared memory allows three)
+    static constexpr int MIN_CTAS = C::THREADS <= 128 ? 3 : (C::THREADS <= 256 ? 2 : 1);
     static_assert(W >= 2, "tensor boxes are at least 16 bytes wide");
     static_assert((BH * W * 8) % 128 == 0, "boxes stay 128-byte aligned in shared memory");
 };
@@ -58,16 +76,28 @@ struct ColsTwiddle {
     int lowbits;
 };
 
+// w_M^q for q reduced modulo M = 2^log2m, from the two-level table of the plan.
+__device__ __forceinline__ float2 root2(const ColsTwiddle& t, uint32_t q, uint32_t mask) {
+    q &= mask;
+    return cmul(__ldg(t.hi + (q >> t.lowbits)), __ldg(t.lo + (q & ((1u << t.lowbits) - 1u))));
+}
+
 template <class RC, int DIR, bool TW>
-__global__ void __launch_bounds__(RC::C::THREADS)
-    k_cols_tma(const __grid_constant__ CUtensorMap tmap, float2* out, int64_t nmat, int log2s,
-               const float2* __restrict__ tw, int flags, int elem_parity, ColsTwiddle twd,
-               int* err, uint64_t limit_ns) {
+__global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
+    k_cols_tma(const __grid_constant__ CUtensorMap imap, const __grid_constant__ CUtensorMap omap,
+               int64_t nmat, int log2s, const float2* __restrict__ tw, int flags, int elem_parity,
+               ColsTwiddle twd, int* err, uint64_t limit_ns) {
     using C = typename RC::C;
-    constexpr int L = RC::L;
     constexpr int W = RC::W;
+    constexpr int RBL = C::rbits(C::NPASS - 1);
+    constexpr int RL = 1 << RBL;
+    constexpr int BL = C::E / RL;
+    constexpr int SL = C::N / RL;
+    constexpr int TA = tw_lo_count(RBL);  // four-step twiddle split r = a + TA*b
+    constexpr int TB = RL / TA;
     extern __shared__ __align__(128) float2 smem[];
     __shared__ uint64_t bar;
+    __shared__ float2 fac[TW ? W * (TA + TB) : 1];  // per-column four-step twiddle factors
 
     const int tid = (int)threadIdx.x;
     const int w = tid % W;
@@ -76,6 +106,7 @@ __global__ void __launch_bounds__(RC::C::THREADS)
     const int64_t tiles_per_mat = S / W;
     const int64_t ntiles = nmat * tiles_per_mat;
     const int64_t t0 = blockIdx.x, tstride = gridDim.x;
+    const uint32_t mask = (1u << (log2s + C::LOG2N)) - 1u;
 
     auto issue = [&](int64_t tile) {
         const int z = (int)(tile / tiles_per_mat);
@@ -83,11 +114,12 @@ __global__ void __launch_bounds__(RC::C::THREADS)
         mbar_arrive_expect_tx(&bar, RC::TILE_BYTES);
 #pragma unroll 1
         for (int b = 0; b < RC::NBOX; ++b)
-            tma_load_3d(smem + b * RC::BH * W, &tmap, x, b * RC::BH, z, &bar);
+            tma_load_3d(smem + b * RC::BH * W, &imap, x, b * RC::BH, z, &bar);
     };
 
     if (tid == 0) {
-        prefetch_tensormap(&tmap);
+        prefetch_tensormap(&imap);
+        prefetch_tensormap(&omap);
         mbar_init(&bar, 1);
         fence_mbar_init();
     }
@@ -97,9 +129,6 @@ __global__ void __launch_bounds__(RC::C::THREADS)
     constexpr int R0 = C::radix(0);
     constexpr int B0 = C::E / R0;
     constexpr int S0 = C::N / R0;
-    constexpr int RL = C::radix(C::NPASS - 1);
-    constexpr int BL = C::E / RL;
-    constexpr int SL = C::N / RL;
 
     for (int64_t it = 0;; ++it) {
         const int64_t tile = t0 + it * tstride;
@@ -112,9 +141,20 @@ __global__ void __launch_bounds__(RC::C::THREADS)
             }
             return;
         }
-        const int64_t mat = tile / tiles_per_mat;
-        const int64_t c = (tile % tiles_per_mat) * W + w;  // column of this thread's transform
+        const int z = (int)(tile / tiles_per_mat);
+        const int x = (int)((tile % tiles_per_mat) * W);
+        const uint32_t c = (uint32_t)x + (uint32_t)w;  // column of this thread's transform
         const int cp = (int)(c & 1);
+        if constexpr (TW) {
+            // fac[w][a] = w_M^{c*SL*a}, fac[w][TA + b] = w_M^{c*SL*TA*b} (M = L*S); the barrier
+            // after the stage read publishes them (and orders them after the previous tile's use)
+            for (int i = tid; i < W * (TA + TB); i += C::THREADS) {
+                const uint32_t cw = (uint32_t)x + (uint32_t)(i / (TA + TB));
+                const int f = i % (TA + TB);
+                const uint32_t e = f < TA ? (uint32_t)(SL * f) : (uint32_t)(SL * TA * (f - TA));
+                fac[i] = root2(twd, cw * e, mask);
+            }
+        }
 
         float2 v[C::E];
 #pragma unroll
@@ -123,16 +163,40 @@ __global__ void __launch_bounds__(RC::C::THREADS)
 #pragma unroll
             for (int r = 0; r < R0; ++r) {
                 const int e = j + r * S0;
-                float2 x = smem[e * W + w];  // dense [row][W] tile written by the copy engine
-                if (flags & KF_CHESS_LOAD) x = neg_if(x, (e * elem_parity + cp) & 1);
-                v[b * R0 + r] = x;
+                float2 xv = smem[e * W + w];  // dense [row][W] tile written by the copy engine
+                if (flags & KF_CHESS_LOAD) xv = neg_if(xv, (e * elem_parity + cp) & 1);
+                v[b * R0 + r] = xv;
             }
         }
         __syncthreads();  // the stage becomes the exchange buffer
 
         run_passes<C, DIR, 0>(v, t, smem + w, tw);
 
-        float2* dst = out + (mat << (log2s + RC::C::LOG2N)) + c;
+        // Output k = j + r*SL of column c.  Four-step: times w_M^{c*k} (M = L*S), formed as
+        // w^{c*j} * w^{c*SL*a} * w^{c*SL*TA*b} for r = a + TA*b: one table lookup per butterfly,
+        // the per-column factors from shared memory.
+        if constexpr (TW) {
+            const float2* fw = fac + w * (TA + TB);
+#pragma unroll
+            for (int b = 0; b < BL; ++b) {
+                const uint32_t j = (uint32_t)(t + b * C::T);
+                const float2 base = root2(twd, c * j, mask);
+                float2 lb[TA];
+                lb[0] = base;
+#pragma unroll
+                for (int a = 1; a < TA; ++a) lb[a] = cmul(base, fw[a]);
+#pragma unroll
+                for (int bb = 0; bb < TB; ++bb) {
+                    const float2 hb = fw[TA + bb];
+#pragma unroll
+                    for (int a = 0; a < TA; ++a) {
+                        const float2 f = bb == 0 ? lb[a] : cmul(lb[a], hb);
+                        v[b * RL + a + TA * bb] = ctw<DIR>(v[b * RL + a + TA * bb], f);
+                    }
+                }
+            }
+        }
+        __syncthreads();  // every thread has read the last exchange
 #pragma unroll
         for (int b = 0; b < BL; ++b) {
             const int j = t + b * C::T;
@@ -140,24 +204,20 @@ __global__ void __launch_bounds__(RC::C::THREADS)
             for (int r = 0; r < RL; ++r) {
                 const int k = j + r * SL;
                 float2 y = v[b * RL + r];
-                if constexpr (TW) {
-                    const uint32_t q = ((uint32_t)c * (uint32_t)k) &
-                                       ((1u << (log2s + RC::C::LOG2N)) - 1u);
-                    const float2 f = cmul(__ldg(twd.hi + (q >> twd.lowbits)),
-                                          __ldg(twd.lo + (q & ((1u << twd.lowbits) - 1u))));
-                    y = ctw<DIR>(y, f);
-                }
                 if (flags & KF_CHESS_STORE) y = neg_if(y, (k * elem_parity + cp) & 1);
-                stg_stream(dst + ((int64_t)k << log2s), y);
+                smem[k * W + w] = y;  // dense [row][W] tile for the copy engine
             }
         }
-        __syncthreads();  // every thread is done with the stage
+        fence_proxy_async_smem();  // make this thread's tile writes visible to the copy engine
+        __syncthreads();
         if (tid == 0) {
+#pragma unroll 1
+            for (int b = 0; b < RC::NBOX; ++b)
+                tma_store_3d(&omap, x, b * RC::BH, z, smem + b * RC::BH * W);
+            bulk_commit();
+            bulk_wait_smem_read();  // the stage may be refilled once the stores have read it
             const int64_t nt = tile + tstride;
-            if (nt < ntiles) {
-                fence_proxy_async_smem();
-                issue(nt);
-            }
+            if (nt < ntiles) issue(nt);
         }
     }
 }
@@ -198,22 +258,25 @@ cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log
     if (!encode) return cudaErrorNotSupported;
     const int64_t S = int64_t(1) << log2s;
     if (S < RC::W) return cudaErrorInvalidValue;
-    CUtensorMap map;
+    CUtensorMap imap, omap;
     const cuuint64_t dims[3] = {(cuuint64_t)S, (cuuint64_t)RC::L, (cuuint64_t)nmat};
     const cuuint64_t strides[2] = {(cuuint64_t)S * 8u, (cuuint64_t)S * RC::L * 8u};
     const cuuint32_t box[3] = {(cuuint32_t)RC::W, (cuuint32_t)RC::BH, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 3, const_cast<float2*>(in), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    for (int k = 0; k < 2; ++k) {
+        if (encode(k == 0 ? &imap : &omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 3,
+                   k == 0 ? const_cast<float2*>(in) : out, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     const int64_t ntiles = nmat * (S / RC::W);
     const int64_t resident = (int64_t)per_sm * num_sms;
     const int64_t grid = ntiles < resident ? ntiles : resident;
     if (grid <= 0) return cudaSuccess;
     kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(
-        map, out, nmat, log2s, tw, flags, elem_parity, twd, err, limit_ns);
+        imap, omap, nmat, log2s, tw, flags, elem_parity, twd, err, limit_ns);
     return cudaGetLastError();
 }
 

@@ -35,10 +35,12 @@ cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t 
                      int log2s, const float2* tw, int flags, int ep, const float2* hi,
                      const float2* lo, int lowbits, int* err, uint64_t lim, cudaStream_t s) {
     switch (log2l) {
-#define GBFFT_C(L)                                                                          \
-    case L:                                                                                 \
-        return cols_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo, lowbits, err, \
-                              lim, s);
+#define GBFFT_C(L)                                                                           \
+    case L:                                                                                  \
+        return hi ? cols_tw_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo,     \
+                                      lowbits, err, lim, s)                                  \
+                  : cols_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo, lowbits, \
+                                   err, lim, s);
         GBFFT_COLS_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;
@@ -46,10 +48,11 @@ cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t 
 }
 
 cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_t count,
-                       int log2n1, const float2* tw, int flags, cudaStream_t s) {
+                       int log2n1, const float2* tw, int flags, int* err, uint64_t lim,
+                       cudaStream_t s) {
     switch (log2n) {
 #define GBFFT_C(L) \
-    case L: return rows_t_entry_##L(dir, in, out, count, log2n1, tw, flags, s);
+    case L: return rows_t_entry_##L(dir, in, out, count, log2n1, tw, flags, err, lim, s);
         GBFFT_ROWS_T_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;

@@ -1,0 +1,5 @@
+// Kernel instantiations: GBFFT_DEF_COLS_TW(9).
+#include "inst_defs.cuh"
+#include "inst_entries.h"
+
+GBFFT_DEF_COLS_TW(9)

@@ -8,6 +8,7 @@
 #include "real_kernel.cuh"
 #include "cols_tma.cuh"
 #include "rows_tma.cuh"
+#include "rowst_tma.cuh"
 
 namespace gbfft {
 
@@ -48,10 +49,9 @@ cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, c
 
 template <int L, int DIR>
 cudaError_t rows_t_impl(const float2* in, float2* out, int64_t count, int log2n1,
-                        const float2* tw, int flags, cudaStream_t s) {
-    using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 2), false>;
-    MapRowsT m{count, L, log2n1};
-    return launch_fft<C, DIR, MapRowsT>(in, out, m, tw, flags, s);
+                        const float2* tw, int flags, int* err, uint64_t lim, cudaStream_t s) {
+    using RC = RowsTTmaCfg<L, rowst_maxrb(L), rowst_log2w(L)>;
+    return launch_rowst_tma<RC, DIR>(in, out, count, log2n1, tw, flags, err, lim, s);
 }
 
 template <int LH>
@@ -67,28 +67,27 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), true>;
                        : rows_impl<L, +1>(in, out, nrows, tw, flags, rp, err, lim, s);          \
     }
 
-#define GBFFT_DEF_COLS(L)                                                                      \
-    cudaError_t gbfft::cols_entry_##L(int dir, const float2* in, float2* out, int64_t count,    \
-                                      int log2s, const float2* tw, int flags, int ep,           \
-                                      const float2* hi, const float2* lo, int lowbits,          \
-                                      int* err, uint64_t lim, cudaStream_t s) {                 \
-        if (hi)                                                                                 \
-            return dir < 0 ? cols_impl<L, -1, true>(in, out, count, log2s, tw, flags, ep, hi,   \
-                                                    lo, lowbits, err, lim, s)                   \
-                           : cols_impl<L, +1, true>(in, out, count, log2s, tw, flags, ep, hi,   \
-                                                    lo, lowbits, err, lim, s);                  \
-        return dir < 0 ? cols_impl<L, -1, false>(in, out, count, log2s, tw, flags, ep, hi, lo,  \
-                                                 lowbits, err, lim, s)                          \
-                       : cols_impl<L, +1, false>(in, out, count, log2s, tw, flags, ep, hi, lo,  \
-                                                 lowbits, err, lim, s);                         \
+// Column passes: the four-step variant (with the inter-pass twiddle) and the plain one (2-D)
+// are separate entry points so that they can live in separate translation units.
+#define GBFFT_DEF_COLS_VARIANT(L, NAME, TWV)                                                   \
+    cudaError_t gbfft::NAME##_##L(int dir, const float2* in, float2* out, int64_t count,        \
+                                  int log2s, const float2* tw, int flags, int ep,               \
+                                  const float2* hi, const float2* lo, int lowbits, int* err,    \
+                                  uint64_t lim, cudaStream_t s) {                               \
+        return dir < 0 ? cols_impl<L, -1, TWV>(in, out, count, log2s, tw, flags, ep, hi, lo,    \
+                                               lowbits, err, lim, s)                            \
+                       : cols_impl<L, +1, TWV>(in, out, count, log2s, tw, flags, ep, hi, lo,    \
+                                               lowbits, err, lim, s);                           \
     }
+#define GBFFT_DEF_COLS_PLAIN(L) GBFFT_DEF_COLS_VARIANT(L, cols_entry, false)
+#define GBFFT_DEF_COLS_TW(L) GBFFT_DEF_COLS_VARIANT(L, cols_tw_entry, true)
 
 #define GBFFT_DEF_ROWS_T(L)                                                                    \
     cudaError_t gbfft::rows_t_entry_##L(int dir, const float2* in, float2* out, int64_t count,  \
-                                        int log2n1, const float2* tw, int flags,                \
-                                        cudaStream_t s) {                                       \
-        return dir < 0 ? rows_t_impl<L, -1>(in, out, count, log2n1, tw, flags, s)               \
-                       : rows_t_impl<L, +1>(in, out, count, log2n1, tw, flags, s);              \
+                                        int log2n1, const float2* tw, int flags, int* err,      \
+                                        uint64_t lim, cudaStream_t s) {                         \
+        return dir < 0 ? rows_t_impl<L, -1>(in, out, count, log2n1, tw, flags, err, lim, s)     \
+                       : rows_t_impl<L, +1>(in, out, count, log2n1, tw, flags, err, lim, s);    \
     }
 
 #define GBFFT_DEF_REAL(L)                                                                      \

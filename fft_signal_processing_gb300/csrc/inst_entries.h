@@ -10,14 +10,16 @@ namespace gbfft {
     cudaError_t rows_entry_##L(int dir, const float2* in, float2* out, int64_t nrows,       \
                                const float2* tw, int flags, int rp, int* err, uint64_t lim, \
                                cudaStream_t s);
-#define GBFFT_X_COLS(L)                                                                    \
-    cudaError_t cols_entry_##L(int dir, const float2* in, float2* out, int64_t count,       \
+#define GBFFT_X_COLS(L) GBFFT_X_COLS_NAMED(L, cols_entry) GBFFT_X_COLS_NAMED(L, cols_tw_entry)
+#define GBFFT_X_COLS_NAMED(L, NAME)                                                        \
+    cudaError_t NAME##_##L(int dir, const float2* in, float2* out, int64_t count,           \
                                int log2s, const float2* tw, int flags, int ep,              \
                                const float2* hi, const float2* lo, int lowbits, int* err,   \
                                uint64_t lim, cudaStream_t s);
 #define GBFFT_X_ROWS_T(L)                                                                  \
     cudaError_t rows_t_entry_##L(int dir, const float2* in, float2* out, int64_t count,     \
-                                 int log2n1, const float2* tw, int flags, cudaStream_t s);
+                                 int log2n1, const float2* tw, int flags, int* err,         \
+                                 uint64_t lim, cudaStream_t s);
 #define GBFFT_X_REAL(L)                                                                    \
     cudaError_t r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,        \
                               int mmajor, const float2* tw, const float2* twr,              \

@@ -79,9 +79,15 @@ __host__ __device__ constexpr int cols_pass_maxrb(int l, int log2s) {
 }
 
 // Four-step pass 2: count rows of 2^log2n points, row tr = k1 + N1*(tr div N1) written
-// transposed into X[k1 + N1*k2] of its 2^(log2n1+log2n)-point transform.
+// transposed into X[k1 + N1*k2] of its 2^(log2n1+log2n)-point transform (persistent kernel,
+// bulk copies in, tensor stores out; bounded waits report into *err, which may be NULL).
 cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_t count,
-                       int log2n1, const float2* tw, int flags, cudaStream_t s);
+                       int log2n1, const float2* tw, int flags, int* err, uint64_t limit_ns,
+                       cudaStream_t s);
+// blocks of W = 8192/N2 rows (at least 2, at most 64; W <= N1 always holds for the four-step
+// splits), radix up to 64
+__host__ __device__ constexpr int rowst_log2w(int l) { return clampi(13 - l, 1, 6); }
+__host__ __device__ constexpr int rowst_maxrb(int l) { return l >= 9 ? 6 : 4; }
 
 // Real rows of 2^(log2h+1) points.
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,

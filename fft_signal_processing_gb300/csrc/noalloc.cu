@@ -54,7 +54,7 @@ const std::vector<float2>& host_tables() {
         for (int l = kNoAllocMinLog2; l <= kNoAllocMaxLog2; ++l) {
             const int l1 = l / 2, l2 = l - l / 2, lowbits = (l + 1) / 2;
             g_off[l].col = host::append_pass_tables(v, l1, cols_pass_maxrb(l1, l - l1));
-            g_off[l].row = host::append_pass_tables(v, l2, cols_maxrb(l2));
+            g_off[l].row = host::append_pass_tables(v, l2, rowst_maxrb(l2));
             g_off[l].hi = host::append_roots(v, int64_t(1) << (l - lowbits),
                                              int64_t(1) << lowbits, int64_t(1) << l);
             g_off[l].lo = host::append_roots(v, int64_t(1) << lowbits, 1, int64_t(1) << l);
@@ -120,6 +120,7 @@ extern "C" int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int
                              2000000000ull, s);
     if (e == cudaSuccess)
         e = run_rows_t(l2, direction, st->scratch, (float2*)out, batch << l1, l1,
-                       st->tables + o.row, (shift && !fwd) ? KF_CHESS_STORE : 0, s);
+                       st->tables + o.row, (shift && !fwd) ? KF_CHESS_STORE : 0, nullptr,
+                       2000000000ull, s);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
