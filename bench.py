@@ -96,7 +96,7 @@ class Workload:
             per = 5.0 * n * self.log2n * (2 if self.dims == 2 else 1) * (n if self.dims == 2 else 1)
             ntr = 2 if self.kind == "c2c_rt" else 1
             self.flops = ntr * per * self.batch
-            passes = 2 if (self.dims == 2 or n > (1 << 14)) else 1
+            passes = 1 if (self.dims == 1 and n <= (1 << 14)) else (3 if n >= (1 << 23) else 2)
             self.min_bytes = ntr * 16 * self.points  # one-pass minimum per transform
             self.pass_bytes = ntr * 16 * self.points * passes
         self.large = self.points * 8 > 2 * L2_BYTES
@@ -370,11 +370,12 @@ def main():
         flush = None if w.large else torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
     kernels_per_step = sum(1 for _ in launches())
-    launch_kernels = {"onepass": 1, "fourstep": 2, "2d": 2, "real": 1}
-    kper = 0
-    for p in plans:
-        d = p.describe()
-        kper += launch_kernels[d.split()[0].split("=")[1]]
+
+    def kernels_of(plan):
+        d = plan.describe()
+        return int(d.split("kernels=")[1].split()[0])
+
+    kper = sum(kernels_of(p) for p in plans)
 
     def one_step(ev=None):
         if flush is not None:
@@ -427,7 +428,7 @@ def main():
         dom_bytes = (w.batch * (w.mmax + 1) * 8 + w.batch * w.n * 4)
         dom_kernels = 1
     else:
-        dom_kernels = 2 if (w.dims == 2 or w.n > (1 << 14)) else 1
+        dom_kernels = kernels_of(plans[min(dom, len(plans) - 1)])
         dom_bytes = 16 * w.points * dom_kernels  # read + write per kernel pass
     achieved = dom_bytes / (launch_ms[dom] * 1e-3) / 1e9
     key = f"{w.name}:launch{dom}"
@@ -436,7 +437,7 @@ def main():
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peak_src,
                 "kernel": plans[min(dom, len(plans) - 1)].describe().split(" ")[0] +
-                          (" (two kernels)" if dom_kernels == 2 else ""),
+                          (f" ({dom_kernels} kernels)" if dom_kernels > 1 else ""),
                 "launch_ms": round(launch_ms[dom], 4),
                 "algorithmic_bytes_per_launch": dom_bytes}
 

@@ -104,16 +104,19 @@ def test_null_plan_calls():
 @pytest.mark.parametrize("n,path,radix", [
     (1, "onepass", "1"), (16, "onepass", "16"), (64, "onepass", "8x8"), (1024, "onepass", "32x32"),
     (2048, "onepass", "64x32"), (4096, "onepass", "64x64"), (8192, "onepass", "32x16x16"),
-    (1 << 14, "onepass", "32x32x16"), (1 << 15, "fourstep", None), (1 << 24, "fourstep", None),
+    (1 << 14, "onepass", "32x32x16"), (1 << 15, "fourstep", None), (1 << 22, "fourstep", None),
+    (1 << 23, "threestep", None), (1 << 24, "threestep", None),
 ])
 def test_path_choice(n, path, radix):
     d = fx.query(n, 4)
     assert f"path={path}" in d
     if radix:
         assert f"radix={radix} " in d
+    l = n.bit_length() - 1
     if path == "fourstep":
-        l = n.bit_length() - 1
         assert f"n1={1 << (l // 2)} n2={1 << (l - l // 2)}" in d
+    if path == "threestep":
+        assert f"a=256 b={1 << (l - 16)} c=256 kernels=3" in d
 
 
 def test_2d_and_real_paths():
