@@ -2,7 +2,7 @@
 //
 // The data are matrices [L rows][S columns] of complex64 stored back to back (nmat of them);
 // every column gets an L-point transform.  A tile is W adjacent columns of one matrix
-// (W*8 bytes of every row).  Each CTA walks a strided sequence of tiles; one thread loads a
+// (W*8 bytes of every row; W*L = 4096 points, at least 2 columns).  Each CTA walks a strided sequence of tiles; one thread loads a
 // tile with L/BH tensor copies (cp.async.bulk.tensor.3d, box W x BH x 1 of a 3-D tensor map
 // over (column, row, matrix)) into a shared-memory stage that completes on an mbarrier.  The
 // copy engine does the strided gathering, so the SM issues one instruction per box instead of
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     constexpr int TB = RL / TA;
     extern __shared__ __align__(128) float2 smem[];
     __shared__ uint64_t bar;
-    __shared__ float2 fac[TW ? W * (TA + TB) : 1];  // per-column four-step twiddle factors
+    __shared__ float2 fac[TW ? W * (TA + TB) : 1];  // four-step twiddle factors, [f][W]
 
     const int tid = (int)threadIdx.x;
     const int w = tid % W;
@@ -157,11 +157,11 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         const uint32_t c = (uint32_t)x + (uint32_t)w;  // column of this thread's transform
         const int cp = (int)(c & 1);
         if constexpr (TW) {
-            // fac[w][a] = w_M^{c*SL*a}, fac[w][TA + b] = w_M^{c*SL*TA*b} (M = L*S); the barrier
+            // fac[a][w] = w_M^{c*SL*a}, fac[TA + b][w] = w_M^{c*SL*TA*b} (M = L*S); the barrier
             // after the stage read publishes them (and orders them after the previous tile's use)
             for (int i = tid; i < W * (TA + TB); i += C::THREADS) {
-                const uint32_t cw = (uint32_t)x + (uint32_t)(i / (TA + TB));
-                const int f = i % (TA + TB);
+                const uint32_t cw = (uint32_t)x + (uint32_t)(i % W);
+                const int f = i / W;
                 const uint32_t e = f < TA ? (uint32_t)(SL * f) : (uint32_t)(SL * TA * (f - TA));
                 fac[i] = root2(twd, cw * e, mask);
             }
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         // w^{c*j} * w^{c*SL*a} * w^{c*SL*TA*b} for r = a + TA*b: one table lookup per butterfly,
         // the per-column factors from shared memory.
         if constexpr (TW) {
-            const float2* fw = fac + w * (TA + TB);
+            const float2* fw = fac + w;
 #pragma unroll
             for (int b = 0; b < BL; ++b) {
                 const uint32_t j = (uint32_t)(t + b * C::T);
@@ -195,10 +195,10 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
                 float2 lb[TA];
                 lb[0] = base;
 #pragma unroll
-                for (int a = 1; a < TA; ++a) lb[a] = cmul(base, fw[a]);
+                for (int a = 1; a < TA; ++a) lb[a] = cmul(base, fw[a * W]);
 #pragma unroll
                 for (int bb = 0; bb < TB; ++bb) {
-                    const float2 hb = fw[TA + bb];
+                    const float2 hb = fw[(TA + bb) * W];
 #pragma unroll
                     for (int a = 0; a < TA; ++a) {
                         const float2 f = bb == 0 ? lb[a] : cmul(lb[a], hb);

@@ -3,7 +3,8 @@
 // Same transform as k_fft over contiguous rows (Stockham radix-64 passes in registers, padded
 // shared-memory exchanges), restructured so that HBM reads never wait for compute: the grid is
 // a whole number of CTAs per SM, each CTA walks a strided sequence of row blocks (W rows of N
-// points, W*N = 4096, 32 KiB), and one thread keeps NST blocks in flight with cp.async.bulk
+// points, W*N = 4096, 32 KiB; one row from 4096 points up), and one thread keeps NST blocks in
+// flight with cp.async.bulk
 // copies into NST shared-memory stages, each completing on its own mbarrier.  A stage that has
 // been read into registers doubles as the exchange buffer of its block, and is refilled with
 // the block NST iterations ahead once the block's results have been stored.  With one stage
@@ -23,7 +24,7 @@ namespace gbfft {
 template <int LOG2N_, int MAXRB_, int NST_>
 struct RowsTmaCfg {
     static constexpr int LOG2N = LOG2N_;
-    static constexpr int LOG2W = 12 - LOG2N_;  // W*N = 4096 points per block
+    static constexpr int LOG2W = LOG2N_ < 12 ? 12 - LOG2N_ : 0;  // W*N = 4096 points per block
     using C = FftCfg<LOG2N_, MAXRB_, LOG2W, true>;
     static constexpr int NST = NST_;
     static constexpr int N = C::N;

@@ -164,3 +164,24 @@ def test_2d_small_integer_bit_exact():
                 ref = oracle.transform(img, direction, 2, shift)
                 exact = np.round(ref.real) + 1j * np.round(ref.imag)
                 np.testing.assert_array_equal(got.astype(np.complex128), exact)
+
+
+# ---- bounded waits of the 2-D and large-N kernels: forced timeout, then a correct run -----
+@pytest.mark.parametrize("n,dims,batch", [(1024, 2, 1), (1 << 16, 1, 2), (1 << 23, 1, 1)])
+def test_wait_timeout_column_and_transposed_kernels(n, dims, batch):
+    m = fx()
+    p = m.Plan(n, batch, dims, m.FORWARD)
+    shape = (batch, n, n) if dims == 2 else (batch, n)
+    x = wl().normal(900 + dims, batch * (n if dims == 2 else 1), n).reshape(shape)
+    xd = torch.from_numpy(x).cuda()
+    p.set_wait_timeout(0)
+    p.c2c(xd)
+    with pytest.raises(m.GbfftError) as ei:
+        p.check()
+    assert ei.value.status == m.FFT_ERR_TIMEOUT
+    p.set_wait_timeout(2_000_000_000)
+    y = p.c2c(xd)
+    torch.cuda.synchronize()
+    p.check()
+    ref = oracle.transform(x, -1, dims, False)
+    assert_parity(y.cpu().numpy(), ref, n * n if dims == 2 else n, "after timeout")
