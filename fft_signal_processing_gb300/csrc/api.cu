@@ -132,6 +132,7 @@ size_t padded_bytes(int l, int maxrb, int w) {
     return sched_npass(l, maxrb) > 1 ? (size_t)spad_size(1 << l, lp) * (1u << w) * 8u : 0;
 }
 Geo rows_geo(int l) {
+    if (l <= 4) return {256, 256, (size_t)256 * ((1 << l) + 1) * 8u};  // small-row kernel
     if (l >= kRowsTmaMinLog2 && l <= kRowsTmaMaxLog2) {  // persistent bulk-copy kernel
         const int w = 12 - l, lp = sched_rbits(l, rows_maxrb(l), 0);
         const size_t stage = (size_t)std::max(spad_size(1 << l, lp), 1 << l) * (1u << w) * 8u;
@@ -162,8 +163,8 @@ Geo strided_geo(int l, int log2minw) {
 Geo real_geo(int lh) {
     const int w = real_log2w(lh), lp = sched_rbits(lh, real_maxrb(lh), 0);
     const int srow = sched_npass(lh, real_maxrb(lh)) > 1 ? spad_size(1 << lh, lp) : 0;
-    const int sreal = std::max(srow, spad_size(1 << lh, lp) + 1);
-    return {(1 << real_log2t(lh)) << w, 1 << w, (size_t)sreal * (1u << w) * 8u};
+    const int slots = std::max(srow, (1 << lh) + 1);
+    return {(1 << real_log2t(lh)) << w, 1 << w, (size_t)slots * (1u << w) * 8u};
 }
 
 std::string describe_spec(const PlanSpec& s, int64_t mmax) {

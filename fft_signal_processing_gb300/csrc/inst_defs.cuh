@@ -9,14 +9,21 @@
 #include "cols_tma.cuh"
 #include "rows_tma.cuh"
 #include "rowst_tma.cuh"
+#include "small_kernel.cuh"
 
 namespace gbfft {
 
-// One-pass rows: the persistent bulk-copy kernel from 2^5 to 2^12, the plain kernel elsewhere.
+// One-pass rows: the small-row kernel up to 2^4, the persistent bulk-copy kernel from 2^5 to
+// 2^12, the plain kernel above.
 template <int L, int DIR>
 cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2* tw, int flags,
                       int rp, int* err, uint64_t lim, cudaStream_t s) {
-    if constexpr (L >= kRowsTmaMinLog2 && L <= kRowsTmaMaxLog2) {
+    if constexpr (L <= 4) {
+        (void)tw;
+        (void)err;
+        (void)lim;
+        return launch_small<L, DIR>(in, out, nrows, flags, rp, s);
+    } else if constexpr (L >= kRowsTmaMinLog2 && L <= kRowsTmaMaxLog2) {
         return launch_rows_tma<RowsTmaCfg<L, rows_maxrb(L), kRowsTmaStages>, DIR>(
             in, out, nrows, tw, flags, rp, err, lim, s);
     } else {
@@ -55,7 +62,7 @@ cudaError_t rows_t_impl(const float2* in, float2* out, int64_t count, int log2n1
 }
 
 template <int LH>
-using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), true>;
+using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
 
 }  // namespace gbfft
 

@@ -18,12 +18,16 @@
 
 namespace gbfft {
 
+// The W rows of a CTA are adjacent lanes (thread = (w, t), w fastest) and interleaved in
+// shared memory (slot i of row w at i*W + w), so spectrum gathers and scatters, the
+// recombination and the radix exchanges all touch consecutive shared-memory words.
 template <class C>
 struct RealCfg {
-    // per-row shared memory: the exchange buffer, or H+1 padded slots for the recombination
-    static constexpr int SREAL =
-        (C::SROW > spad_size(C::N, C::LP) + 1) ? C::SROW : spad_size(C::N, C::LP) + 1;
-    static constexpr size_t SMEM_BYTES = (size_t)SREAL * C::W * sizeof(float2);
+    static_assert(!C::TFAST, "real kernels interleave their W rows");
+    static constexpr int H = C::N;
+    // per-row shared memory: the padded exchange, or H+1 slots for the recombination
+    static constexpr int SLOTS = C::SROW > H + 1 ? C::SROW : H + 1;
+    static constexpr size_t SMEM_BYTES = (size_t)SLOTS * C::W * sizeof(float2);
 };
 
 // R2C: in = real rows [nrows][2H] float32, out = spectrum (row-major [nrows][mmax+1] or
@@ -32,16 +36,16 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS)
     k_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
           const float2* __restrict__ tw, const float2* __restrict__ twr) {
-    static_assert(C::TFAST, "real kernels keep each row's threads adjacent");
     constexpr int H = C::N;
-    constexpr int SREAL = RealCfg<C>::SREAL;
+    constexpr int W = C::W;
     extern __shared__ float2 smem[];
-    const int w = (int)threadIdx.x / C::T;
-    const int t = (int)threadIdx.x % C::T;
-    const int64_t row = (int64_t)blockIdx.x * C::W + w;
+    const int w = (int)threadIdx.x % W;
+    const int t = (int)threadIdx.x / W;
+    const int64_t row0 = (int64_t)blockIdx.x * W;
+    const int64_t row = row0 + w;
     const bool active = row < nrows;
-    float2* sb = smem + w * SREAL;
 
+    // z_m = x_{2m} + i x_{2m+1}: the real row read as H complex points
     constexpr int R0 = C::radix(0);
     constexpr int B0 = C::E / R0;
     constexpr int S0 = C::N / R0;
@@ -54,7 +58,7 @@ __global__ void __launch_bounds__(C::THREADS)
         for (int r = 0; r < R0; ++r)
             v[b * R0 + r] = active ? ldg_stream(src + j + r * S0) : make_float2(0.f, 0.f);
     }
-    run_passes<C, -1, 0>(v, t, sb, tw);
+    run_passes<C, -1, 0>(v, t, smem + w, tw);
 
     constexpr int RL = C::radix(C::NPASS - 1);
     constexpr int BL = C::E / RL;
@@ -64,33 +68,24 @@ __global__ void __launch_bounds__(C::THREADS)
     for (int b = 0; b < BL; ++b) {
         const int j = t + b * C::T;
 #pragma unroll
-        for (int r = 0; r < RL; ++r) sb[spad<C::LP>(j + r * SL)] = v[b * RL + r];
+        for (int r = 0; r < RL; ++r) smem[(j + r * SL) * W + w] = v[b * RL + r];  // Z_k
     }
     __syncthreads();
 
-    // X_k for k <= mmax; row-major: each row's threads walk k; m-major: the W rows of the CTA
-    // are adjacent lanes so that consecutive rows of one coefficient are written together.
-    const int total = C::W * (mmax + 1);
+    // X_k = (Z_k + conj Z_{H-k})/2 - i e^{-i th_k} (Z_k - conj Z_{H-k})/2, k <= mmax
+    const int total = W * (mmax + 1);
+#pragma unroll 4
     for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
-        int wr, k;
-        if (mmajor) {
-            wr = i % C::W;
-            k = i / C::W;
-        } else {
-            wr = i / (mmax + 1);
-            k = i % (mmax + 1);
-        }
-        const int64_t rr = (int64_t)blockIdx.x * C::W + wr;
+        const int wr = i % W, k = i / W;
+        const int64_t rr = row0 + wr;
         if (rr >= nrows) continue;
-        const float2* s = smem + wr * SREAL;
-        const float2 zk = s[spad<C::LP>(k)];
-        const float2 zm = s[spad<C::LP>((H - k) & (H - 1))];
+        const float2 zk = smem[k * W + wr];
+        const float2 zm = smem[((H - k) & (H - 1)) * W + wr];
         const float2 zc = make_float2(zm.x, -zm.y);                   // conj Z_{H-k}
         const float2 xe = make_float2(0.5f * (zk.x + zc.x), 0.5f * (zk.y + zc.y));
         const float2 d = make_float2(0.5f * (zk.x - zc.x), 0.5f * (zk.y - zc.y));
         const float2 xo = make_float2(d.y, -d.x);                     // -i * d
-        const float2 wk = __ldg(twr + k);
-        const float2 y = cadd(xe, ctw<-1>(xo, wk));                   // xe + e^{-i th} xo
+        const float2 y = cadd(xe, ctw<-1>(xo, __ldg(twr + k)));       // xe + e^{-i th} xo
         const int64_t o = mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k;
         stg_stream(out + o, y);
     }
@@ -101,37 +96,31 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS)
     k_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
           const float2* __restrict__ tw, const float2* __restrict__ twr) {
-    static_assert(C::TFAST, "real kernels keep each row's threads adjacent");
     constexpr int H = C::N;
-    constexpr int SREAL = RealCfg<C>::SREAL;
+    constexpr int W = C::W;
     extern __shared__ float2 smem[];
-    const int w = (int)threadIdx.x / C::T;
-    const int t = (int)threadIdx.x % C::T;
-    const int64_t row = (int64_t)blockIdx.x * C::W + w;
+    const int w = (int)threadIdx.x % W;
+    const int t = (int)threadIdx.x / W;
+    const int64_t row0 = (int64_t)blockIdx.x * W;
+    const int64_t row = row0 + w;
     const bool active = row < nrows;
-    float2* sb = smem + w * SREAL;
 
-    // gather X_0..X_H into shared memory (X_0 = Re F_0, zero above mmax, X_H = 0)
-    const int total = C::W * (H + 1);
+    // gather X_0..X_H (X_0 = Re F_0, zero above mmax, X_H = 0) as slots k*W + w
+    const int total = W * (H + 1);
+#pragma unroll 8
     for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
-        int wr, k;
-        if (mmajor) {
-            wr = i % C::W;
-            k = i / C::W;
-        } else {
-            wr = i / (H + 1);
-            k = i % (H + 1);
-        }
-        const int64_t rr = (int64_t)blockIdx.x * C::W + wr;
+        const int wr = i % W, k = i / W;
+        const int64_t rr = row0 + wr;
         float2 x = make_float2(0.f, 0.f);
         if (rr < nrows && k <= mmax) {
             x = ldg_stream(in + (mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k));
             if (k == 0) x.y = 0.f;
         }
-        smem[wr * SREAL + spad<C::LP>(k)] = x;
+        smem[k * W + wr] = x;
     }
     __syncthreads();
 
+    // Z_k = (X_k + conj X_{H-k}) + i e^{+i th_k} (X_k - conj X_{H-k}) for the first pass
     constexpr int R0 = C::radix(0);
     constexpr int B0 = C::E / R0;
     constexpr int S0 = C::N / R0;
@@ -142,23 +131,23 @@ __global__ void __launch_bounds__(C::THREADS)
 #pragma unroll
         for (int r = 0; r < R0; ++r) {
             const int k = j + r * S0;
-            const float2 xk = sb[spad<C::LP>(k)];
-            const float2 xm = sb[spad<C::LP>(H - k)];
+            const float2 xk = smem[k * W + w];
+            const float2 xm = smem[(H - k) * W + w];
             const float2 xc = make_float2(xm.x, -xm.y);             // conj X_{H-k}
-            const float2 s = cadd(xk, xc);
+            const float2 sum = cadd(xk, xc);
             const float2 wd = ctw<+1>(csub(xk, xc), __ldg(twr + k));  // e^{+i th} (X_k - conj X_{H-k})
-            v[b * R0 + r] = make_float2(s.x - wd.y, s.y + wd.x);     // s + i * wd
+            v[b * R0 + r] = make_float2(sum.x - wd.y, sum.y + wd.x);  // sum + i * wd
         }
     }
     __syncthreads();  // the exchange buffer aliases the gathered spectrum
 
-    run_passes<C, +1, 0>(v, t, sb, tw);
+    run_passes<C, +1, 0>(v, t, smem + w, tw);
 
     constexpr int RL = C::radix(C::NPASS - 1);
     constexpr int BL = C::E / RL;
     constexpr int SL = C::N / RL;
     if (active) {
-        float2* dst = reinterpret_cast<float2*>(out) + row * H;
+        float2* dst = reinterpret_cast<float2*>(out) + row * H;  // x_{2m}, x_{2m+1} = z_m
 #pragma unroll
         for (int b = 0; b < BL; ++b) {
             const int j = t + b * C::T;
@@ -168,16 +157,29 @@ __global__ void __launch_bounds__(C::THREADS)
     }
 }
 
+// Kernel attributes (dynamic shared memory above 48 KiB, maximum carveout) are set once per
+// device and instantiation: Tag (the launch configuration) keeps one record per kernel.
+template <class Tag, class K>
+cudaError_t configure_once(K kern, size_t smem) {
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || configured_dev == dev) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess) configured_dev = dev;
+    return e;
+}
+
 template <class C>
 cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
                        const float2* tw, const float2* twr, cudaStream_t stream) {
     auto kern = k_r2c<C>;
     constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
-    if (smem > 48 * 1024) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    struct Tag {};
+    cudaError_t e = configure_once<Tag>(kern, smem);
+    if (e != cudaSuccess) return e;
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr);
@@ -189,11 +191,9 @@ cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, in
                        const float2* tw, const float2* twr, cudaStream_t stream) {
     auto kern = k_c2r<C>;
     constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
-    if (smem > 48 * 1024) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    struct Tag {};
+    cudaError_t e = configure_once<Tag>(kern, smem);
+    if (e != cudaSuccess) return e;
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr);
