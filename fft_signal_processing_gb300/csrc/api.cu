@@ -33,6 +33,7 @@
 #include "fft_kernel.cuh"
 #include "host_tables.h"
 #include "kernels.h"
+#include "tma.cuh"
 
 using namespace gbfft;
 
@@ -484,7 +485,7 @@ int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
     if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
     cudaError_t e = run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax,
                             s.layout == FFT_LAYOUT_REAL_MMAJOR, p->d_tw + p->off_a,
-                            p->d_tw + p->off_r, (cudaStream_t)stream);
+                            p->d_tw + p->off_r, p->d_err, (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
 
@@ -498,7 +499,7 @@ int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
     if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
     cudaError_t e = run_c2r(s.log2n - 1, (const float2*)in, out, s.batch, (int)p->mmax,
                             s.layout == FFT_LAYOUT_REAL_MMAJOR, p->d_tw + p->off_a,
-                            p->d_tw + p->off_r, (cudaStream_t)stream);
+                            p->d_tw + p->off_r, p->d_err, p->wait_limit_ns, (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
 
@@ -510,7 +511,7 @@ int fft_plan_check(fft_plan p) {
         return FFT_ERR_CUDA;
     if (h != 0) {
         if (cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess) return FFT_ERR_CUDA;
-        return FFT_ERR_TIMEOUT;
+        return h == KERR_WAIT_TIMEOUT ? FFT_ERR_TIMEOUT : FFT_ERR_CUDA;
     }
     return FFT_OK;
 }

@@ -59,6 +59,24 @@ __device__ __forceinline__ void bulk_wait_smem_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// 2-D tiled tensor copies (global -> shared on an mbarrier; shared -> global in a bulk group).
+__device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y,
+                                             const void* src_smem) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(smem_addr(src_smem))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -128,6 +146,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
             tma_load_3d(smem + b * RC::BH * W, &imap, x, b * RC::BH, z, &bar);
     };
 
+    if (!tma_stage_aligned(smem, err)) return;
     if (tid == 0) {
         prefetch_tensormap(&imap);
         prefetch_tensormap(&omap);

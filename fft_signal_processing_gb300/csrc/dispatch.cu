@@ -74,10 +74,10 @@ cudaError_t run_cols_slab(int log2l, int dir, const float2* in, float2* out, int
 }
 
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s) {
+                    int mmajor, const float2* tw, const float2* twr, int* err, cudaStream_t s) {
     switch (log2h) {
 #define GBFFT_C(L) \
-    case L: return r2c_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, s);
+    case L: return r2c_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, err, s);
         GBFFT_REAL_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;
@@ -85,10 +85,11 @@ cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int 
 }
 
 cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s) {
+                    int mmajor, const float2* tw, const float2* twr, int* err, uint64_t lim,
+                    cudaStream_t s) {
     switch (log2h) {
 #define GBFFT_C(L) \
-    case L: return c2r_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, s);
+    case L: return c2r_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, err, lim, s);
         GBFFT_REAL_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;

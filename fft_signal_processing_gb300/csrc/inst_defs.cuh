@@ -126,12 +126,12 @@ cudaError_t cols_slab_impl(const float2* in, float2* out, int64_t count, int log
 
 #define GBFFT_DEF_REAL(L)                                                                      \
     cudaError_t gbfft::r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,     \
-                                     int mmajor, const float2* tw, const float2* twr,           \
+                                     int mmajor, const float2* tw, const float2* twr, int* err, \
                                      cudaStream_t s) {                                          \
-        return launch_r2c<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, s);                  \
+        return launch_r2c<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, err, s);             \
     }                                                                                           \
     cudaError_t gbfft::c2r_entry_##L(const float2* in, float* out, int64_t nrows, int mmax,     \
-                                     int mmajor, const float2* tw, const float2* twr,           \
-                                     cudaStream_t s) {                                          \
-        return launch_c2r<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, s);                  \
+                                     int mmajor, const float2* tw, const float2* twr, int* err, \
+                                     uint64_t lim, cudaStream_t s) {                            \
+        return launch_c2r<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, err, lim, s);        \
     }

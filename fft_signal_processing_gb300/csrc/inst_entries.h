@@ -22,11 +22,11 @@ namespace gbfft {
                                  uint64_t lim, cudaStream_t s);
 #define GBFFT_X_REAL(L)                                                                    \
     cudaError_t r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,        \
-                              int mmajor, const float2* tw, const float2* twr,              \
+                              int mmajor, const float2* tw, const float2* twr, int* err,    \
                               cudaStream_t s);                                              \
     cudaError_t c2r_entry_##L(const float2* in, float* out, int64_t nrows, int mmax,        \
-                              int mmajor, const float2* tw, const float2* twr,              \
-                              cudaStream_t s);
+                              int mmajor, const float2* tw, const float2* twr, int* err,    \
+                              uint64_t lim, cudaStream_t s);
 
 #define GBFFT_X_COLS_SLAB(L)                                                               \
     cudaError_t cols_slab_entry_##L(int dir, const float2* in, float2* out, int64_t count,  \

@@ -103,8 +103,9 @@ __host__ __device__ constexpr int rowst_maxrb(int l) { return l >= 9 ? 6 : 4; }
 
 // Real rows of 2^(log2h+1) points.
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s);
+                    int mmajor, const float2* tw, const float2* twr, int* err, cudaStream_t s);
 cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, cudaStream_t s);
+                    int mmajor, const float2* tw, const float2* twr, int* err, uint64_t limit_ns,
+                    cudaStream_t s);
 
 }  // namespace gbfft

@@ -14,6 +14,9 @@
 // with Z_H = Z_0 and X_H = 0 (no Nyquist bin since mmax < N/2).
 #pragma once
 
+#include <cstring>
+
+#include "cols_tma.cuh"
 #include "fft_kernel.cuh"
 
 namespace gbfft {
@@ -32,13 +35,17 @@ struct RealCfg {
 
 // R2C: in = real rows [nrows][2H] float32, out = spectrum (row-major [nrows][mmax+1] or
 // m-major [mmax+1][nrows]).  twr[k] = (cos, sin)(2*pi*k/N), k < H.
-template <class C>
+// TMA = true (m-major spectrum, even row count): the spectrum tile [k][W] leaves through
+// tensor stores of a 2-D map over (row, coefficient); coefficients above mmax are clipped by
+// the map's extent.
+template <class C, bool TMA>
 __global__ void __launch_bounds__(C::THREADS)
     k_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
-          const float2* __restrict__ tw, const float2* __restrict__ twr) {
+          const float2* __restrict__ tw, const float2* __restrict__ twr,
+          const __grid_constant__ CUtensorMap fmap, int* err) {
     constexpr int H = C::N;
     constexpr int W = C::W;
-    extern __shared__ float2 smem[];
+    extern __shared__ __align__(128) float2 smem[];
     const int w = (int)threadIdx.x % W;
     const int t = (int)threadIdx.x / W;
     const int64_t row0 = (int64_t)blockIdx.x * W;
@@ -73,32 +80,60 @@ __global__ void __launch_bounds__(C::THREADS)
     __syncthreads();
 
     // X_k = (Z_k + conj Z_{H-k})/2 - i e^{-i th_k} (Z_k - conj Z_{H-k})/2, k <= mmax
-    const int total = W * (mmax + 1);
-#pragma unroll 4
-    for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
-        const int wr = i % W, k = i / W;
-        const int64_t rr = row0 + wr;
-        if (rr >= nrows) continue;
-        const float2 zk = smem[k * W + wr];
-        const float2 zm = smem[((H - k) & (H - 1)) * W + wr];
+    auto recombine = [&](float2 zk, float2 zm, int k) {
         const float2 zc = make_float2(zm.x, -zm.y);                   // conj Z_{H-k}
         const float2 xe = make_float2(0.5f * (zk.x + zc.x), 0.5f * (zk.y + zc.y));
         const float2 d = make_float2(0.5f * (zk.x - zc.x), 0.5f * (zk.y - zc.y));
         const float2 xo = make_float2(d.y, -d.x);                     // -i * d
-        const float2 y = cadd(xe, ctw<-1>(xo, __ldg(twr + k)));       // xe + e^{-i th} xo
-        const int64_t o = mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k;
-        stg_stream(out + o, y);
+        return cadd(xe, ctw<-1>(xo, __ldg(twr + k)));                 // xe + e^{-i th} xo
+    };
+    if constexpr (TMA) {
+        if (!tma_stage_aligned(smem, err)) return;
+        // pairs {k, H-k}: one thread reads both Z's and writes both X's in place
+        constexpr int NB = H < 256 ? 1 : H / 256;
+        constexpr int BK = H / NB;
+        const int npair = W * (H / 2 + 1);
+        for (int i = (int)threadIdx.x; i < npair; i += C::THREADS) {
+            const int wr = i % W, k = i / W;
+            const int km = (H - k) & (H - 1);
+            const float2 zk = smem[k * W + wr], zm = smem[km * W + wr];
+            smem[k * W + wr] = recombine(zk, zm, k);
+            if (km != k) smem[km * W + wr] = recombine(zm, zk, km);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int b = 0; b < NB && b * BK <= mmax; ++b)
+                tma_store_2d(&fmap, (int)row0, b * BK, smem + b * BK * W);
+            bulk_commit();
+            bulk_wait_smem_read();  // shared memory stays valid until the stores have read it
+        }
+    } else {
+        const int total = W * (mmax + 1);
+#pragma unroll 4
+        for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
+            const int wr = i % W, k = i / W;
+            const int64_t rr = row0 + wr;
+            if (rr >= nrows) continue;
+            const float2 y = recombine(smem[k * W + wr], smem[((H - k) & (H - 1)) * W + wr], k);
+            const int64_t o = mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k;
+            stg_stream(out + o, y);
+        }
     }
 }
 
 // C2R: in = spectrum (layout as above), out = real rows [nrows][2H] float32.
-template <class C>
+// TMA = true (m-major spectrum, even row count): the spectrum tile [k][W] (k < H) arrives by
+// tensor loads of a 2-D map over (row, coefficient); coefficients above mmax are filled with
+// zeros by the copy engine.  The wait is bounded (limit_ns), reporting into *err.
+template <class C, bool TMA>
 __global__ void __launch_bounds__(C::THREADS)
     k_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
-          const float2* __restrict__ tw, const float2* __restrict__ twr) {
+          const float2* __restrict__ tw, const float2* __restrict__ twr,
+          const __grid_constant__ CUtensorMap fmap, int* err, uint64_t limit_ns) {
     constexpr int H = C::N;
     constexpr int W = C::W;
-    extern __shared__ float2 smem[];
+    extern __shared__ __align__(128) float2 smem[];
     const int w = (int)threadIdx.x % W;
     const int t = (int)threadIdx.x / W;
     const int64_t row0 = (int64_t)blockIdx.x * W;
@@ -106,17 +141,46 @@ __global__ void __launch_bounds__(C::THREADS)
     const bool active = row < nrows;
 
     // gather X_0..X_H (X_0 = Re F_0, zero above mmax, X_H = 0) as slots k*W + w
-    const int total = W * (H + 1);
-#pragma unroll 8
-    for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
-        const int wr = i % W, k = i / W;
-        const int64_t rr = row0 + wr;
-        float2 x = make_float2(0.f, 0.f);
-        if (rr < nrows && k <= mmax) {
-            x = ldg_stream(in + (mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k));
-            if (k == 0) x.y = 0.f;
+    if constexpr (TMA) {
+        __shared__ uint64_t bar;
+        constexpr int NB = H < 256 ? 1 : H / 256;
+        constexpr int BK = H / NB;
+        if (!tma_stage_aligned(smem, err)) return;
+        if (threadIdx.x == 0) {
+            prefetch_tensormap(&fmap);
+            mbar_init(&bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&bar, (uint32_t)(H * W * 8));
+            for (int b = 0; b < NB; ++b) tma_load_2d(smem + b * BK * W, &fmap, (int)row0, b * BK, &bar);
         }
-        smem[k * W + wr] = x;
+        __syncthreads();
+        const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+        if (__syncthreads_or(!ok)) {
+            if (threadIdx.x == 0) {
+                if (err) atomicExch(err, KERR_WAIT_TIMEOUT);
+                mbar_wait_bounded(&bar, 0, kDrainLimitNs);
+            }
+            return;
+        }
+        if (threadIdx.x < W) {
+            smem[threadIdx.x].y = 0.f;                      // X_0 = Re F_0
+            smem[H * W + threadIdx.x] = make_float2(0.f, 0.f);  // X_H = 0
+        }
+    } else {
+        (void)err;
+        (void)limit_ns;
+        const int total = W * (H + 1);
+#pragma unroll 8
+        for (int i = (int)threadIdx.x; i < total; i += C::THREADS) {
+            const int wr = i % W, k = i / W;
+            const int64_t rr = row0 + wr;
+            float2 x = make_float2(0.f, 0.f);
+            if (rr < nrows && k <= mmax) {
+                x = ldg_stream(in + (mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k));
+                if (k == 0) x.y = 0.f;
+            }
+            smem[k * W + wr] = x;
+        }
     }
     __syncthreads();
 
@@ -172,31 +236,83 @@ cudaError_t configure_once(K kern, size_t smem) {
     return e;
 }
 
+// 2-D tensor map over an m-major spectrum [mmax+1][nrows]: (row, coefficient), box W x BK.
+template <class C>
+cudaError_t encode_spectrum_map(CUtensorMap* map, const void* base, int64_t nrows, int mmax) {
+    constexpr int H = C::N;
+    constexpr int NB = H < 256 ? 1 : H / 256;
+    constexpr int BK = H / NB;
+    EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)nrows, (cuuint64_t)(mmax + 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)nrows * 8u};
+    const cuuint32_t box[2] = {(cuuint32_t)C::W, (cuuint32_t)BK};
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+template <class C>
+bool real_use_tma(int64_t nrows, int mmajor) {
+    return mmajor && C::W >= 2 && (nrows % 2) == 0 && nrows >= C::W;
+}
+
 template <class C>
 cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
-                       const float2* tw, const float2* twr, cudaStream_t stream) {
-    auto kern = k_r2c<C>;
+                       const float2* tw, const float2* twr, int* err, cudaStream_t stream) {
     constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
-    struct Tag {};
-    cudaError_t e = configure_once<Tag>(kern, smem);
-    if (e != cudaSuccess) return e;
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr);
+    CUtensorMap map;
+    std::memset(&map, 0, sizeof map);
+    if (real_use_tma<C>(nrows, mmajor)) {
+        auto kern = k_r2c<C, true>;
+        struct Tag {};
+        cudaError_t e = configure_once<Tag>(kern, smem);
+        if (e == cudaSuccess) e = encode_spectrum_map<C>(&map, out, nrows, mmax);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr,
+                                                            map, err);
+    } else {
+        auto kern = k_r2c<C, false>;
+        struct Tag {};
+        cudaError_t e = configure_once<Tag>(kern, smem);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr,
+                                                            map, err);
+    }
     return cudaGetLastError();
 }
 
 template <class C>
 cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
-                       const float2* tw, const float2* twr, cudaStream_t stream) {
-    auto kern = k_c2r<C>;
+                       const float2* tw, const float2* twr, int* err, uint64_t limit_ns,
+                       cudaStream_t stream) {
     constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
-    struct Tag {};
-    cudaError_t e = configure_once<Tag>(kern, smem);
-    if (e != cudaSuccess) return e;
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr);
+    CUtensorMap map;
+    std::memset(&map, 0, sizeof map);
+    if (real_use_tma<C>(nrows, mmajor)) {
+        auto kern = k_c2r<C, true>;
+        struct Tag {};
+        cudaError_t e = configure_once<Tag>(kern, smem);
+        if (e == cudaSuccess) e = encode_spectrum_map<C>(&map, in, nrows, mmax);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr,
+                                                            map, err, limit_ns);
+    } else {
+        auto kern = k_c2r<C, false>;
+        struct Tag {};
+        cudaError_t e = configure_once<Tag>(kern, smem);
+        if (e != cudaSuccess) return e;
+        kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr,
+                                                            map, err, limit_ns);
+    }
     return cudaGetLastError();
 }
 

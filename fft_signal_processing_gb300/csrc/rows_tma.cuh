@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(RC::C::THREADS)
         bulk_load(smem + s * RC::STAGE, in + blk * RC::W * N, bytes, &bars[s]);
     };
 
+    if (!tma_stage_aligned(smem, err)) return;
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();

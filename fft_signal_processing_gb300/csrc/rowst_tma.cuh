@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
             bulk_load(smem + r * RC::INROW, in + (blk * W + r) * N, (uint32_t)N * 8u, &bar);
     };
 
+    if (!tma_stage_aligned(smem, err)) return;
     if (tid == 0) {
         prefetch_tensormap(&omap);
         mbar_init(&bar, 1);

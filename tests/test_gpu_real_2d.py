@@ -64,7 +64,8 @@ def mmax_cases(n):
 def test_c2r_grid(log2n, layout):
     n = 1 << log2n
     for mmax in mmax_cases(n):
-        rows = 67 if n <= 4096 else 5
+        # odd row counts take the direct-load path, even ones the tensor-copy path (m-major)
+        rows = (67 if mmax % 2 else 64) if n <= 4096 else (5 if mmax % 2 else 6)
         F = wl().spectrum(100 + log2n, rows, mmax)
         got = gpu_c2r(F, n, mmax, layout)
         assert_parity(got, oracle.c2r(F, n), n, f"c2r n={n} mmax={mmax} {layout}")
@@ -75,7 +76,7 @@ def test_c2r_grid(log2n, layout):
 def test_r2c_grid(log2n, layout):
     n = 1 << log2n
     for mmax in mmax_cases(n):
-        rows = 67 if n <= 4096 else 5
+        rows = (67 if mmax % 2 else 64) if n <= 4096 else (5 if mmax % 2 else 6)
         x = wl().real_normal(200 + log2n, rows, n)
         got = gpu_r2c(x, mmax, layout)
         ref = oracle.r2c(x, mmax)
@@ -185,3 +186,21 @@ def test_wait_timeout_column_and_transposed_kernels(n, dims, batch):
     p.check()
     ref = oracle.transform(x, -1, dims, False)
     assert_parity(y.cpu().numpy(), ref, n * n if dims == 2 else n, "after timeout")
+
+
+def test_wait_timeout_real_synthesis():
+    m = fx()
+    n, rows, mmax = 4096, 64, 1365
+    p = m.Plan(n, rows, 1, m.INVERSE, layout=LAYOUTS["mmajor"], mmax=mmax)
+    F = wl().spectrum(950, rows, mmax)
+    Fd = torch.from_numpy(np.ascontiguousarray(oracle.to_mmajor(F))).cuda()
+    p.set_wait_timeout(0)
+    p.c2r(Fd)
+    with pytest.raises(m.GbfftError) as ei:
+        p.check()
+    assert ei.value.status == m.FFT_ERR_TIMEOUT
+    p.set_wait_timeout(2_000_000_000)
+    x = p.c2r(Fd)
+    torch.cuda.synchronize()
+    p.check()
+    assert_parity(x.cpu().numpy(), oracle.c2r(F, n), n, "after timeout")
