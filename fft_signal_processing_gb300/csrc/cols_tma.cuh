@@ -146,14 +146,16 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
             tma_load_3d(smem + b * RC::BH * W, &imap, x, b * RC::BH, z, &bar);
     };
 
-    if (!tma_stage_aligned(smem, err)) return;
+    __shared__ int stage_bad;
     if (tid == 0) {
+        stage_bad = stage_misaligned(smem, err);
         prefetch_tensormap(&imap);
         prefetch_tensormap(&omap);
         mbar_init(&bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
+    if (stage_bad) return;  // uniform: never copy into a misaligned stage
     if (tid == 0 && t0 < ntiles) issue(t0);
 
     constexpr int R0 = C::radix(0);

@@ -52,19 +52,21 @@ __global__ void __launch_bounds__(RC::C::THREADS)
     const int64_t nblocks = (nrows + RC::W - 1) / RC::W;
     const int64_t blk0 = blockIdx.x, bstride = gridDim.x;
 
-    auto issue = [&](int s, int64_t blk) {
+    auto issue = [&](int s, int64_t blk) {  // never copy into a misaligned stage; the waits will give up
         const int64_t rows = nrows - blk * RC::W < RC::W ? nrows - blk * RC::W : RC::W;
         const uint32_t bytes = (uint32_t)rows * N * 8u;
         mbar_arrive_expect_tx(&bars[s], bytes);
         bulk_load(smem + s * RC::STAGE, in + blk * RC::W * N, bytes, &bars[s]);
     };
 
-    if (!tma_stage_aligned(smem, err)) return;
+    __shared__ int stage_bad;
     if (tid == 0) {
+        stage_bad = stage_misaligned(smem, err);
         for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
+    if (stage_bad) return;  // uniform: never copy into a misaligned stage
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             const int64_t blk = blk0 + s * bstride;
@@ -116,6 +118,15 @@ __global__ void __launch_bounds__(RC::C::THREADS)
         }
         __syncthreads();  // the stage becomes this block's exchange buffer
 
+        auto refill = [&]() {
+            if (tid == 0) {
+                const int64_t nb = blk0 + (it + NST) * bstride;
+                if (nb < nblocks) {
+                    fence_proxy_async_smem();
+                    issue(s, nb);
+                }
+            }
+        };
         run_passes<C, DIR, 0>(v, t, sbuf + w * RC::SROW, tw);
 
         if (active) {
@@ -133,13 +144,7 @@ __global__ void __launch_bounds__(RC::C::THREADS)
             }
         }
         __syncthreads();  // every thread is done with the stage
-        if (tid == 0) {
-            const int64_t nb = blk0 + (it + NST) * bstride;
-            if (nb < nblocks) {
-                fence_proxy_async_smem();
-                issue(s, nb);
-            }
-        }
+        refill();
     }
 }
 

@@ -61,13 +61,15 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
             bulk_load(smem + r * RC::INROW, in + (blk * W + r) * N, (uint32_t)N * 8u, &bar);
     };
 
-    if (!tma_stage_aligned(smem, err)) return;
+    __shared__ int stage_bad;
     if (tid == 0) {
+        stage_bad = stage_misaligned(smem, err);
         prefetch_tensormap(&omap);
         mbar_init(&bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
+    if (stage_bad) return;  // uniform: never copy into a misaligned stage
     if (tid == 0 && b0 < nblocks) issue(b0);
 
     constexpr int R0 = C::radix(0);

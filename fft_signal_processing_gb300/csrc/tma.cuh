@@ -80,13 +80,20 @@ constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s for draining copies af
 // Error word values written by kernels (read and cleared by fft_plan_check).
 enum : int { KERR_WAIT_TIMEOUT = 1, KERR_STAGE_ALIGN = 2 };
 
-// Self-check run by every CTA before its first asynchronous copy: the shared-memory stage must
+// Self-check run once per CTA before its first asynchronous copy: the shared-memory stage must
 // start on a 128-byte boundary (copies need 16).  On failure the CTA records KERR_STAGE_ALIGN
-// (err may be NULL) and issues nothing.  The result is uniform across the CTA.
+// (err may be NULL) and issues nothing.  tma_stage_aligned is the uniform form (every thread
+// evaluates it); stage_misaligned is the single-thread form whose result the kernel publishes
+// through shared memory across its prologue barrier.
 __device__ __forceinline__ bool tma_stage_aligned(const void* stage, int* err) {
     const bool ok = (smem_addr(stage) & 127u) == 0;
     if (!ok && threadIdx.x == 0 && err) atomicExch(err, KERR_STAGE_ALIGN);
     return ok;
+}
+__device__ __forceinline__ int stage_misaligned(const void* stage, int* err) {
+    const bool bad = (smem_addr(stage) & 127u) != 0;
+    if (bad && err) atomicExch(err, KERR_STAGE_ALIGN);
+    return bad ? 1 : 0;
 }
 
 }  // namespace gbfft
