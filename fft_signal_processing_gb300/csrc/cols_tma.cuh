@@ -91,8 +91,9 @@ struct ColsTmaCfg {
     static constexpr int STAGE = (C::SROW > L ? C::SROW : L) * W;  // float2
     static constexpr uint32_t TILE_BYTES = (uint32_t)L * W * 8u;
     static constexpr size_t SMEM_BYTES = (size_t)STAGE * sizeof(float2);
-    // CTAs per SM the register allocation must allow (shared memory allows three)
-    static constexpr int MIN_CTAS = C::THREADS <= 128 ? 3 : (C::THREADS <= 256 ? 2 : 1);
+    // CTAs per SM the register allocation must allow: as many as the shared memory allows
+    static constexpr int MIN_CTAS =
+        SMEM_BYTES > 113 * 1024 ? 1 : (C::THREADS <= 128 ? 3 : (C::THREADS <= 256 ? 2 : 1));
     static_assert(W >= 2, "tensor boxes are at least 16 bytes wide");
     static_assert((BH * W * 8) % 128 == 0, "boxes stay 128-byte aligned in shared memory");
 };

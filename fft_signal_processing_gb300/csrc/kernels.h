@@ -64,9 +64,11 @@ cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t 
                      int log2s, const float2* tw, int flags, int elem_parity, const float2* hi,
                      const float2* lo, int lowbits, int* err, uint64_t limit_ns, cudaStream_t s);
 
-// Column tiles of the TMA kernel: W = 4096/L columns (at least 2, at most 64: tiles of 32 KiB,
-// 64 KiB at 4096 points), radix up to 64.
-__host__ __device__ constexpr int cols_tma_log2w(int l) { return clampi(12 - l, 1, 6); }
+// Column tiles of the TMA kernel: W = 4096/L columns up to 512 points (at most 64), 8 columns
+// at 1024 points and 4 above.  Wide row runs (32-64 bytes) were measured to matter more than
+// CTAs per SM at these lengths.  Radix up to 64.
+__host__ __device__ constexpr int tile_log2w(int l) { return l <= 9 ? clampi(12 - l, 3, 6) : (l == 10 ? 3 : 2); }
+__host__ __device__ constexpr int cols_tma_log2w(int l) { return tile_log2w(l); }
 __host__ __device__ constexpr int cols_tma_maxrb(int l) { return l >= 9 ? 6 : 4; }
 constexpr int kColsTmaMinLog2 = 7;
 constexpr int kColsTmaMaxLog2 = 12;
@@ -96,9 +98,9 @@ __host__ __device__ constexpr int threepass_log2a(int l) { return 8; }
 __host__ __device__ constexpr int threepass_log2b(int l) { return l - 16; }  // 7 or 8
 __host__ __device__ constexpr int threepass_log2c(int l) { return 8; }
 
-// blocks of W = 4096/N2 rows (at least 2, at most 64; W <= N1 always holds for the four-step
-// splits), radix up to 64
-__host__ __device__ constexpr int rowst_log2w(int l) { return clampi(12 - l, 1, 6); }
+// blocks of W rows as for the column tiles (W <= N1 always holds for the four-step splits),
+// radix up to 64
+__host__ __device__ constexpr int rowst_log2w(int l) { return tile_log2w(l); }
 __host__ __device__ constexpr int rowst_maxrb(int l) { return l >= 9 ? 6 : 4; }
 
 // Real rows of 2^(log2h+1) points.

@@ -32,7 +32,9 @@ struct RowsTTmaCfg {
     static constexpr int STAGE = ((A1 > A2 ? A1 : A2) > A3 ? (A1 > A2 ? A1 : A2) : A3);
     static constexpr uint32_t BLOCK_BYTES = (uint32_t)W * N * 8u;
     static constexpr size_t SMEM_BYTES = (size_t)STAGE * sizeof(float2);
-    static constexpr int MIN_CTAS = C::THREADS <= 128 ? 3 : (C::THREADS <= 256 ? 2 : 1);
+    // CTAs per SM the register allocation must allow: as many as the shared memory allows
+    static constexpr int MIN_CTAS =
+        SMEM_BYTES > 113 * 1024 ? 1 : (C::THREADS <= 128 ? 3 : (C::THREADS <= 256 ? 2 : 1));
     static_assert(W >= 2, "tensor boxes are at least 16 bytes wide");
 };
 
