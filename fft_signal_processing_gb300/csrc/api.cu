@@ -139,8 +139,10 @@ Geo rows_geo(int l) {
         const size_t stage = (size_t)std::max(spad_size(1 << l, lp), 1 << l) * (1u << w) * 8u;
         return {(1 << rows_log2t(l)) << w, 1 << w, stage * kRowsTmaStages};
     }
-    const int w = rows_log2w(l);
-    return {(1 << rows_log2t(l)) << w, 1 << w, padded_bytes(l, rows_maxrb(l), w)};
+    // long rows: full-row stage + half-row exchange buffer
+    const int lp = sched_rbits(l, rows_maxrb(l), 0);
+    return {1 << rows_log2t(l), 1,
+            ((size_t)(1 << l) + (size_t)spad_size(1 << (l - 1), lp)) * 8u};
 }
 Geo cols_geo(int l, int log2s) {
     if (cols_use_tma(l, log2s)) {

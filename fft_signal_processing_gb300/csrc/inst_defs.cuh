@@ -7,6 +7,7 @@
 #include "kernels.h"
 #include "real_kernel.cuh"
 #include "cols_tma.cuh"
+#include "rows_big.cuh"
 #include "rows_tma.cuh"
 #include "rowst_tma.cuh"
 #include "small_kernel.cuh"
@@ -14,7 +15,7 @@
 namespace gbfft {
 
 // One-pass rows: the small-row kernel up to 2^4, the persistent bulk-copy kernel from 2^5 to
-// 2^12, the plain kernel above.
+// 2^12, the persistent long-row kernel at 2^13 and 2^14.
 template <int L, int DIR>
 cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2* tw, int flags,
                       int rp, int* err, uint64_t lim, cudaStream_t s) {
@@ -27,11 +28,9 @@ cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2
         return launch_rows_tma<RowsTmaCfg<L, rows_maxrb(L), kRowsTmaStages>, DIR>(
             in, out, nrows, tw, flags, rp, err, lim, s);
     } else {
-        (void)err;
-        (void)lim;
-        using C = FftCfg<L, rows_maxrb(L), rows_log2w(L), true>;
-        MapRows m{nrows, L, rp};
-        return launch_fft<C, DIR, MapRows>(in, out, m, tw, flags, s);
+        // 2^13, 2^14: full-row stage for the next row plus a half-row exchange buffer
+        using RC = RowsBigCfg<L, rows_maxrb(L), (L == 13 ? 2 : 1)>;
+        return launch_rows_big<RC, DIR>(in, out, nrows, tw, flags, rp, err, lim, s);
     }
 }
 
