@@ -224,17 +224,22 @@ def profile_traffic(kernel_key):
     except Exception:
         return None, None
     ent = data.get(kernel_key)
-    if not ent or ent.get("source_sha") != kernel_source_sha():
+    if not ent or ent.get("source_sha") != kernel_source_sha(ent.get("source_files")):
         return None, None
     return ent.get("dram_bytes_per_launch"), ent.get("summary")
 
 
-def kernel_source_sha():
+def kernel_source_sha(files=None):
+    """Hash of the sources a kernel is built from (all of csrc/ when files is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fft_signal_processing_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+    names = sorted(files) if files else sorted(
+        f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in names:
+        try:
             h.update(open(os.path.join(csrc, f), "rb").read())
+        except OSError:
+            return "missing:" + f
     return h.hexdigest()[:16]
 
 
