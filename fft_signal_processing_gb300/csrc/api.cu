@@ -145,6 +145,11 @@ Geo rows_geo(int l) {
             ((size_t)(1 << l) + (size_t)spad_size(1 << (l - 1), lp)) * 8u};
 }
 Geo cols_geo(int l, int log2s) {
+    if (cols_use_big(l, log2s)) {  // tile stage + half-length exchange buffer
+        const int w = cols_tma_log2w(l), lp = sched_rbits(l, cols_tma_maxrb(l), 0);
+        const size_t b = ((size_t)(1 << l) + (size_t)spad_size(1 << (l - 1), lp)) << w;
+        return {(1 << (l - lp)) << w, 1 << w, b * 8u};
+    }
     if (cols_use_tma(l, log2s)) {
         const int w = cols_tma_log2w(l), lp = sched_rbits(l, cols_tma_maxrb(l), 0);
         const size_t stage = (size_t)std::max(spad_size(1 << l, lp), 1 << l) * (1u << w) * 8u;
@@ -156,6 +161,9 @@ Geo cols_geo(int l, int log2s) {
 Geo rowst_geo(int l) {
     const int w = rowst_log2w(l), lp = sched_rbits(l, rowst_maxrb(l), 0);
     const size_t a = (size_t)((1 << l) + (w >= 3 ? 2 : 16 >> w)) << w;
+    if (rowst_use_big(l))  // row slots + half-length exchange buffer
+        return {(1 << (l - lp)) << w, 1 << w,
+                (a + ((size_t)spad_size(1 << (l - 1), lp) << w)) * 8u};
     const size_t b = (size_t)spad_size(1 << l, lp) << w;
     return {(1 << (l - lp)) << w, 1 << w, std::max(a, b) * 8u};
 }

@@ -11,6 +11,7 @@
 #include "rows_tma.cuh"
 #include "rowst_tma.cuh"
 #include "small_kernel.cuh"
+#include "tiles_big.cuh"
 
 namespace gbfft {
 
@@ -41,9 +42,16 @@ cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, c
     if constexpr (L >= kColsTmaMinLog2 && L <= kColsTmaMaxLog2) {
         // the planners only ask for matrices at least one tile wide at these sizes
         if (!cols_use_tma(L, log2s)) return cudaErrorInvalidValue;
-        using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
-        return launch_cols_tma<RC, DIR, TW, false>(in, out, count >> log2s, log2s, tw, flags, ep,
-                                                   ColsTwiddle{hi, lo, lowbits}, -1, err, lim, s);
+        if constexpr (L >= kBigTileMinLog2) {
+            using RC = ColsBigCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
+            return launch_cols_big<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags, ep,
+                                                ColsTwiddle{hi, lo, lowbits}, err, lim, s);
+        } else {
+            using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
+            return launch_cols_tma<RC, DIR, TW, false>(in, out, count >> log2s, log2s, tw, flags,
+                                                       ep, ColsTwiddle{hi, lo, lowbits}, -1, err,
+                                                       lim, s);
+        }
     } else {
         (void)err;
         (void)lim;
@@ -56,8 +64,13 @@ cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, c
 template <int L, int DIR>
 cudaError_t rows_t_impl(const float2* in, float2* out, int64_t count, int log2n1,
                         const float2* tw, int flags, int* err, uint64_t lim, cudaStream_t s) {
-    using RC = RowsTTmaCfg<L, rowst_maxrb(L), rowst_log2w(L)>;
-    return launch_rowst_tma<RC, DIR>(in, out, count, log2n1, tw, flags, err, lim, s);
+    if constexpr (rowst_use_big(L)) {
+        using RC = RowsTBigCfg<L, rowst_maxrb(L), rowst_log2w(L)>;
+        return launch_rowst_big<RC, DIR>(in, out, count, log2n1, tw, flags, err, lim, s);
+    } else {
+        using RC = RowsTTmaCfg<L, rowst_maxrb(L), rowst_log2w(L)>;
+        return launch_rowst_tma<RC, DIR>(in, out, count, log2n1, tw, flags, err, lim, s);
+    }
 }
 
 template <int LH>

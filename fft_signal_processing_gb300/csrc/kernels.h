@@ -81,6 +81,15 @@ __host__ __device__ constexpr int cols_pass_maxrb(int l, int log2s) {
     return cols_use_tma(l, log2s) ? cols_tma_maxrb(l) : cols_maxrb(l);
 }
 
+// From 2^12 points a tile of W transforms fills most of an SM's shared memory, and the strided
+// passes run the tile kernels that keep the stage apart from a half-length exchange buffer, so
+// that the next tile's copy overlaps the transform of the current one.
+constexpr int kBigTileMinLog2 = 12;
+__host__ __device__ constexpr bool cols_use_big(int l, int log2s) {
+    return l >= kBigTileMinLog2 && cols_use_tma(l, log2s);
+}
+__host__ __device__ constexpr bool rowst_use_big(int l) { return l >= kBigTileMinLog2; }
+
 // Four-step pass 2: count rows of 2^log2n points, row tr = k1 + N1*(tr div N1) written
 // transposed into X[k1 + N1*k2] of its 2^(log2n1+log2n)-point transform (persistent kernel,
 // bulk copies in, tensor stores out; bounded waits report into *err, which may be NULL).
@@ -93,7 +102,7 @@ cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_
 cudaError_t run_cols_slab(int log2l, int dir, const float2* in, float2* out, int64_t count,
                           int log2s, const float2* tw, const float2* hi, const float2* lo,
                           int lowbits, int log2a, int* err, uint64_t limit_ns, cudaStream_t s);
-constexpr int kThreePassMinLog2 = 23;  // from here the 2-pass tiles would be 32 bytes or less
+constexpr int kThreePassMinLog2 = 25;  // above every supported size: two passes up to 2^24
 __host__ __device__ constexpr int threepass_log2a(int l) { return 8; }
 __host__ __device__ constexpr int threepass_log2b(int l) { return l - 16; }  // 7 or 8
 __host__ __device__ constexpr int threepass_log2c(int l) { return 8; }

@@ -29,9 +29,11 @@ struct RowsBigCfg {
     static_assert(STAGE_BYTES % 128 == 0, "the exchange buffer stays 128-byte aligned");
 };
 
-// Passes P..NPASS-1 with two-phase exchanges through the half-row buffer xb.
+// Passes P..NPASS-1 with two-phase exchanges through a half-length exchange buffer.  sb points
+// at this transform's first slot; slots are C::SS apart (1 for a single row, W when W
+// transforms are interleaved lane by lane).
 template <class C, int DIR, int P>
-__device__ __forceinline__ void run_passes_split(float2 (&v)[C::E], int t, float2* xb,
+__device__ __forceinline__ void run_passes_split(float2 (&v)[C::E], int t, float2* sb,
                                                  const float2* __restrict__ tw) {
     constexpr int R = C::radix(P);
     constexpr int B = C::E / R;
@@ -58,7 +60,7 @@ __device__ __forceinline__ void run_passes_split(float2 (&v)[C::E], int t, float
                 if ((base >= HN) == (h == 1)) {  // all R outputs of j land in half h
 #pragma unroll
                     for (int r = 0; r < R; ++r)
-                        xb[spad<C::LP>(base + r * Ns - h * HN)] = v[b * R + r];
+                        sb[spad<C::LP>(base + r * Ns - h * HN) * C::SS] = v[b * R + r];
                 }
             }
             __syncthreads();
@@ -67,7 +69,7 @@ __device__ __forceinline__ void run_passes_split(float2 (&v)[C::E], int t, float
                 const int j = t + b * C::T;
 #pragma unroll
                 for (int r = 0; r < R2 / 2; ++r) {
-                    const float2 x = xb[spad<C::LP>(j + (r + h * (R2 / 2)) * S2 - h * HN)];
+                    const float2 x = sb[spad<C::LP>(j + (r + h * (R2 / 2)) * S2 - h * HN) * C::SS];
                     if (h == 0)
                         lo[b][r] = x;
                     else
@@ -82,7 +84,7 @@ __device__ __forceinline__ void run_passes_split(float2 (&v)[C::E], int t, float
         }
 #pragma unroll
         for (int b = 0; b < B2; ++b) apply_twiddles<C, DIR, P + 1>(v + b * R2, pt[b]);
-        run_passes_split<C, DIR, P + 1>(v, t, xb, tw);
+        run_passes_split<C, DIR, P + 1>(v, t, sb, tw);
     }
 }
 

@@ -105,7 +105,7 @@ def test_null_plan_calls():
     (1, "onepass", "1"), (16, "onepass", "16"), (64, "onepass", "8x8"), (1024, "onepass", "32x32"),
     (2048, "onepass", "64x32"), (4096, "onepass", "64x64"), (8192, "onepass", "32x16x16"),
     (1 << 14, "onepass", "32x32x16"), (1 << 15, "fourstep", None), (1 << 22, "fourstep", None),
-    (1 << 23, "threestep", None), (1 << 24, "threestep", None),
+    (1 << 23, "fourstep", None), (1 << 24, "fourstep", None),
 ])
 def test_path_choice(n, path, radix):
     d = fx.query(n, 4)

@@ -168,7 +168,8 @@ def test_2d_small_integer_bit_exact():
 
 
 # ---- bounded waits of the 2-D and large-N kernels: forced timeout, then a correct run -----
-@pytest.mark.parametrize("n,dims,batch", [(1024, 2, 1), (1 << 16, 1, 2), (1 << 23, 1, 1)])
+@pytest.mark.parametrize("n,dims,batch", [(1024, 2, 1), (4096, 2, 1), (1 << 16, 1, 2),
+                                          (1 << 23, 1, 1)])
 def test_wait_timeout_column_and_transposed_kernels(n, dims, batch):
     m = fx()
     p = m.Plan(n, batch, dims, m.FORWARD)
