@@ -10,8 +10,6 @@
 //             k1's output k2 to X[k1 + N1*k2].  This is the four-step FFT the CS598 project page
 //             ("Fast Fourier Transform on CPU and GPU") names for inputs that do not fit in
 //             fast memory; the intermediate lives in the plan's workspace.
-//   threestep dims 1, n = 2^23, 2^24: n = A*B*C (2^8 x 2^7..8 x 2^8), three passes whose tiles
-//             are all at least 128 bytes wide (the 2-pass tiles would be 16-32 bytes).
 //   2d        n x n images: all rows, then all columns (Mota, "High Performance Fourier
 //             Transforms on GPUs with GLSL", §2.7 Eq. 19), both in place in the output.
 //   real      band-limited real rows through an n/2-point complex core (fourier.ts).
@@ -39,7 +37,7 @@ using namespace gbfft;
 
 namespace {
 
-enum Path { PATH_ONEPASS = 0, PATH_FOURSTEP = 1, PATH_2D = 2, PATH_REAL = 3, PATH_THREESTEP = 4 };
+enum Path { PATH_ONEPASS = 0, PATH_FOURSTEP = 1, PATH_2D = 2, PATH_REAL = 3 };
 
 struct PlanSpec {
     int64_t n = 0, batch = 0;
@@ -48,7 +46,6 @@ struct PlanSpec {
     Path path = PATH_ONEPASS;
     int log2n1 = 0, log2n2 = 0;  // four-step split
     int lowbits = 0;             // four-step two-level twiddle split
-    int log2a = 0, log2b = 0, log2c = 0, lowbits2 = 0;  // three-pass split
 };
 
 int ilog2_exact(int64_t n) {
@@ -90,13 +87,6 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
         if (l > FFT_MAX_LOG2N_1D) return FFT_ERR_UNSUPPORTED_SIZE;
         if (l <= kMaxLog2OnePass) {
             s.path = PATH_ONEPASS;
-        } else if (l >= kThreePassMinLog2) {
-            s.path = PATH_THREESTEP;
-            s.log2a = threepass_log2a(l);
-            s.log2b = threepass_log2b(l);
-            s.log2c = threepass_log2c(l);
-            s.lowbits = (l + 1) / 2;
-            s.lowbits2 = (s.log2b + s.log2c + 1) / 2;
         } else {
             s.path = PATH_FOURSTEP;
             s.log2n1 = l / 2;      // column pass (strided)
@@ -203,24 +193,6 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
                      g2.threads, g2.per_cta, g2.smem);
             break;
         }
-        case PATH_THREESTEP: {
-            Geo g1 = cols_geo(s.log2a, s.log2b + s.log2c), g2 = cols_geo(s.log2b, s.log2c),
-                g3 = rowst_geo(s.log2c);
-            snprintf(buf, sizeof buf,
-                     "path=threestep n=%lld batch=%lld %s shift=%d a=%d b=%d c=%d kernels=3 "
-                     "pass1=columns(radix=%s threads=%d cols_per_cta=%d smem=%zu) "
-                     "pass2=slab_columns(radix=%s threads=%d cols_per_cta=%d smem=%zu) "
-                     "pass3=rows_transposed(radix=%s threads=%d rows_per_cta=%d smem=%zu)",
-                     (long long)s.n, (long long)s.batch, dir, s.shift, 1 << s.log2a,
-                     1 << s.log2b, 1 << s.log2c,
-                     radix_string(s.log2a, cols_pass_maxrb(s.log2a, s.log2b + s.log2c)).c_str(),
-                     g1.threads, g1.per_cta, g1.smem,
-                     radix_string(s.log2b, cols_pass_maxrb(s.log2b, s.log2c)).c_str(),
-                     g2.threads, g2.per_cta, g2.smem,
-                     radix_string(s.log2c, rowst_maxrb(s.log2c)).c_str(), g3.threads,
-                     g3.per_cta, g3.smem);
-            break;
-        }
         case PATH_2D: {
             Geo g1 = rows_geo(s.log2n), g2 = cols_geo(s.log2n, s.log2n);
             snprintf(buf, sizeof buf,
@@ -268,8 +240,7 @@ struct gbfft_plan_s {
     int device = 0;
     float2* d_tw = nullptr;
     size_t tw_count = 0;
-    size_t off_a = 0, off_b = 0, off_c = 0, off_hi = 0, off_lo = 0, off_hi2 = 0, off_lo2 = 0,
-           off_r = 0;
+    size_t off_a = 0, off_b = 0, off_hi = 0, off_lo = 0, off_r = 0;
     void* d_work = nullptr;
     size_t work_bytes = 0;
     int* d_err = nullptr;
@@ -346,21 +317,6 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
             const int64_t nlo = int64_t(1) << s.lowbits, nhi = int64_t(1) << (s.log2n - s.lowbits);
             p->off_hi = append_roots(tw, nhi, nlo, s.n);  // w_n^{qh * 2^lowbits}
             p->off_lo = append_roots(tw, nlo, 1, s.n);    // w_n^{ql}
-            p->work_bytes = (size_t)s.batch * (size_t)s.n * sizeof(float2);
-            break;
-        }
-        case PATH_THREESTEP: {
-            const int bc = s.log2b + s.log2c;
-            p->off_a = append_pass_tables(tw, s.log2a, cols_pass_maxrb(s.log2a, bc));
-            p->off_b = append_pass_tables(tw, s.log2b, cols_pass_maxrb(s.log2b, s.log2c));
-            p->off_c = append_pass_tables(tw, s.log2c, rowst_maxrb(s.log2c));
-            const int64_t nlo = int64_t(1) << s.lowbits, nhi = int64_t(1) << (s.log2n - s.lowbits);
-            p->off_hi = append_roots(tw, nhi, nlo, s.n);  // w_n^q, two levels
-            p->off_lo = append_roots(tw, nlo, 1, s.n);
-            const int64_t m2 = int64_t(1) << bc;
-            const int64_t nlo2 = int64_t(1) << s.lowbits2, nhi2 = int64_t(1) << (bc - s.lowbits2);
-            p->off_hi2 = append_roots(tw, nhi2, nlo2, m2);  // w_{BC}^q, two levels
-            p->off_lo2 = append_roots(tw, nlo2, 1, m2);
             p->work_bytes = (size_t)s.batch * (size_t)s.n * sizeof(float2);
             break;
         }
@@ -444,29 +400,6 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                 e = run_rows_t(s.log2n2, s.direction, wk, y, s.batch * n1, s.log2n1,
                                p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0,
                                p->d_err, p->wait_limit_ns, st);
-            break;
-        }
-        case PATH_THREESTEP: {
-            // n = a*BC + b*C + c, k = ka + A*kb + AB*kc:
-            // pass 1 in -> out: A-point columns of [A][BC], times w_n^{(bC + c)*ka};
-            // pass 2 out -> workspace: B-point columns of each [B][C] slab ka, times
-            //   w_{BC}^{c*kb}, written as row kb*A + ka;
-            // pass 3 workspace -> out: C-point rows, row r written to X[r + AB*kc].
-            float2* wk = (float2*)p->d_work;
-            const int bc = s.log2b + s.log2c;
-            e = run_cols(s.log2a, s.direction, x, y, s.batch << bc, bc, p->d_tw + p->off_a,
-                         (s.shift && fwd) ? KF_CHESS_LOAD : 0, 0, p->d_tw + p->off_hi,
-                         p->d_tw + p->off_lo, s.lowbits, p->d_err, p->wait_limit_ns, st);
-            if (e == cudaSuccess)
-                e = run_cols_slab(s.log2b, s.direction, y, wk, s.batch << (s.log2a + s.log2c),
-                                  s.log2c, p->d_tw + p->off_b, p->d_tw + p->off_hi2,
-                                  p->d_tw + p->off_lo2, s.lowbits2, s.log2a, p->d_err,
-                                  p->wait_limit_ns, st);
-            if (e == cudaSuccess)
-                e = run_rows_t(s.log2c, s.direction, wk, y, s.batch << (s.log2a + s.log2b),
-                               s.log2a + s.log2b, p->d_tw + p->off_c,
-                               (s.shift && !fwd) ? KF_CHESS_STORE : 0, p->d_err,
-                               p->wait_limit_ns, st);
             break;
         }
         case PATH_2D: {

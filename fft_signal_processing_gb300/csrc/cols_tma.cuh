@@ -44,15 +44,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int 
         "r"(x), "r"(y), "r"(z), "r"(smem_addr(src_smem))
         : "memory");
 }
-// 4-D tiled tensor copy shared -> global (bulk async group of the issuing thread).
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int x, int y, int z, int q,
-                                             const void* src_smem) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y), "r"(z), "r"(q), "r"(smem_addr(src_smem))
-        : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // The issuing thread's bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_smem_read() {
@@ -110,13 +101,11 @@ __device__ __forceinline__ float2 root2(const ColsTwiddle& t, uint32_t q, uint32
     return cmul(__ldg(t.hi + (q >> t.lowbits)), __ldg(t.lo + (q & ((1u << t.lowbits) - 1u))));
 }
 
-// OUT4D: the output map is 4-D (column, row, z mod 2^log2a, z div 2^log2a), which lets the
-// three-pass path write the slab ka's row kb to row kb*A + ka of its transform.
-template <class RC, int DIR, bool TW, bool OUT4D>
+template <class RC, int DIR, bool TW>
 __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     k_cols_tma(const __grid_constant__ CUtensorMap imap, const __grid_constant__ CUtensorMap omap,
                int64_t nmat, int log2s, const float2* __restrict__ tw, int flags, int elem_parity,
-               ColsTwiddle twd, int log2a, int* err, uint64_t limit_ns) {
+               ColsTwiddle twd, int* err, uint64_t limit_ns) {
     using C = typename RC::C;
     constexpr int W = RC::W;
     constexpr int RBL = C::rbits(C::NPASS - 1);
@@ -245,13 +234,8 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         __syncthreads();
         if (tid == 0) {
 #pragma unroll 1
-            for (int b = 0; b < RC::NBOX; ++b) {
-                if constexpr (OUT4D)
-                    tma_store_4d(&omap, x, b * RC::BH, z & ((1 << log2a) - 1), z >> log2a,
-                                 smem + b * RC::BH * W);
-                else
-                    tma_store_3d(&omap, x, b * RC::BH, z, smem + b * RC::BH * W);
-            }
+            for (int b = 0; b < RC::NBOX; ++b)
+                tma_store_3d(&omap, x, b * RC::BH, z, smem + b * RC::BH * W);
             bulk_commit();
             bulk_wait_smem_read();  // the stage may be refilled once the stores have read it
             const int64_t nt = tile + tstride;
@@ -268,13 +252,11 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn tensor_map_encoder();  // resolved once through the runtime (dispatch.cu)
 
-// log2a < 0: the output has the input's layout; log2a >= 0: the slab z = t*A + ka (A = 2^log2a)
-// of transform t is written with rows kb*A + ka (4-D output map).
-template <class RC, int DIR, bool TW, bool OUT4D>
+template <class RC, int DIR, bool TW>
 cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log2s,
                             const float2* tw, int flags, int elem_parity, ColsTwiddle twd,
-                            int log2a, int* err, uint64_t limit_ns, cudaStream_t stream) {
-    auto kern = k_cols_tma<RC, DIR, TW, OUT4D>;
+                            int* err, uint64_t limit_ns, cudaStream_t stream) {
+    auto kern = k_cols_tma<RC, DIR, TW>;
     static int configured_dev = -1;
     static int per_sm = 0, num_sms = 0;
     int dev = 0;
@@ -311,28 +293,12 @@ cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    if constexpr (OUT4D) {
-        const int64_t A = int64_t(1) << log2a;
-        if (log2a < 0 || nmat % A) return cudaErrorInvalidValue;
-        // (c, kb, ka, t) -> t*A*L*S + (kb*A + ka)*S + c
-        const cuuint64_t d4[4] = {(cuuint64_t)S, (cuuint64_t)RC::L, (cuuint64_t)A,
-                                  (cuuint64_t)(nmat / A)};
-        const cuuint64_t s4[3] = {(cuuint64_t)(A * S * 8), (cuuint64_t)(S * 8),
-                                  (cuuint64_t)(A * S * RC::L * 8)};
-        const cuuint32_t b4[4] = {(cuuint32_t)RC::W, (cuuint32_t)RC::BH, 1u, 1u};
-        const cuuint32_t e4[4] = {1u, 1u, 1u, 1u};
-        if (encode(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 4, out, d4, s4, b4, e4,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
     const int64_t ntiles = nmat * (S / RC::W);
     const int64_t resident = (int64_t)per_sm * num_sms;
     const int64_t grid = ntiles < resident ? ntiles : resident;
     if (grid <= 0) return cudaSuccess;
     kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(
-        imap, omap, nmat, log2s, tw, flags, elem_parity, twd, log2a, err, limit_ns);
+        imap, omap, nmat, log2s, tw, flags, elem_parity, twd, err, limit_ns);
     return cudaGetLastError();
 }
 

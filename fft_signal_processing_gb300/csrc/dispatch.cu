@@ -59,20 +59,6 @@ cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_
     }
 }
 
-cudaError_t run_cols_slab(int log2l, int dir, const float2* in, float2* out, int64_t count,
-                          int log2s, const float2* tw, const float2* hi, const float2* lo,
-                          int lowbits, int log2a, int* err, uint64_t lim, cudaStream_t s) {
-    switch (log2l) {
-#define GBFFT_C(L)                                                                           \
-    case L:                                                                                  \
-        return cols_slab_entry_##L(dir, in, out, count, log2s, tw, hi, lo, lowbits, log2a,   \
-                                   err, lim, s);
-        GBFFT_COLS_SLAB_SIZES(GBFFT_C)
-#undef GBFFT_C
-        default: return cudaErrorInvalidValue;
-    }
-}
-
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
                     int mmajor, const float2* tw, const float2* twr, int* err, cudaStream_t s) {
     switch (log2h) {

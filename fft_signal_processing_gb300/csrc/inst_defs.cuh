@@ -48,9 +48,8 @@ cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, c
                                                 ColsTwiddle{hi, lo, lowbits}, err, lim, s);
         } else {
             using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
-            return launch_cols_tma<RC, DIR, TW, false>(in, out, count >> log2s, log2s, tw, flags,
-                                                       ep, ColsTwiddle{hi, lo, lowbits}, -1, err,
-                                                       lim, s);
+            return launch_cols_tma<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags, ep,
+                                                ColsTwiddle{hi, lo, lowbits}, err, lim, s);
         }
     } else {
         (void)err;
@@ -100,33 +99,6 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
     }
 #define GBFFT_DEF_COLS_PLAIN(L) GBFFT_DEF_COLS_VARIANT(L, cols_entry, false)
 #define GBFFT_DEF_COLS_TW(L) GBFFT_DEF_COLS_VARIANT(L, cols_tw_entry, true)
-
-namespace gbfft {
-
-// Three-pass pass 2: column pass with twiddle whose output slab rows are interleaved.
-template <int L, int DIR>
-cudaError_t cols_slab_impl(const float2* in, float2* out, int64_t count, int log2s,
-                           const float2* tw, const float2* hi, const float2* lo, int lowbits,
-                           int log2a, int* err, uint64_t lim, cudaStream_t s) {
-    static_assert(L >= kColsTmaMinLog2 && L <= kColsTmaMaxLog2, "TMA column sizes only");
-    if (!cols_use_tma(L, log2s)) return cudaErrorInvalidValue;
-    using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
-    return launch_cols_tma<RC, DIR, true, true>(in, out, count >> log2s, log2s, tw, 0, 0,
-                                                ColsTwiddle{hi, lo, lowbits}, log2a, err, lim, s);
-}
-
-}  // namespace gbfft
-
-#define GBFFT_DEF_COLS_SLAB(L)                                                                 \
-    cudaError_t gbfft::cols_slab_entry_##L(int dir, const float2* in, float2* out,              \
-                                           int64_t count, int log2s, const float2* tw,          \
-                                           const float2* hi, const float2* lo, int lowbits,     \
-                                           int log2a, int* err, uint64_t lim, cudaStream_t s) { \
-        return dir < 0 ? cols_slab_impl<L, -1>(in, out, count, log2s, tw, hi, lo, lowbits,      \
-                                               log2a, err, lim, s)                              \
-                       : cols_slab_impl<L, +1>(in, out, count, log2s, tw, hi, lo, lowbits,      \
-                                               log2a, err, lim, s);                             \
-    }
 
 #define GBFFT_DEF_ROWS_T(L)                                                                    \
     cudaError_t gbfft::rows_t_entry_##L(int dir, const float2* in, float2* out, int64_t count,  \

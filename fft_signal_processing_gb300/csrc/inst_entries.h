@@ -28,22 +28,14 @@ namespace gbfft {
                               int mmajor, const float2* tw, const float2* twr, int* err,    \
                               uint64_t lim, cudaStream_t s);
 
-#define GBFFT_X_COLS_SLAB(L)                                                               \
-    cudaError_t cols_slab_entry_##L(int dir, const float2* in, float2* out, int64_t count,  \
-                                    int log2s, const float2* tw, const float2* hi,          \
-                                    const float2* lo, int lowbits, int log2a, int* err,     \
-                                    uint64_t lim, cudaStream_t s);
-
 #define GBFFT_ROWS_SIZES(X) X(0) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14)
 #define GBFFT_COLS_SIZES(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12)
 #define GBFFT_ROWS_T_SIZES(X) X(8) X(9) X(10) X(11) X(12)
-#define GBFFT_COLS_SLAB_SIZES(X) X(7) X(8)
 #define GBFFT_REAL_SIZES(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14)
 
 GBFFT_ROWS_SIZES(GBFFT_X_ROWS)
 GBFFT_COLS_SIZES(GBFFT_X_COLS)
 GBFFT_ROWS_T_SIZES(GBFFT_X_ROWS_T)
-GBFFT_COLS_SLAB_SIZES(GBFFT_X_COLS_SLAB)
 GBFFT_REAL_SIZES(GBFFT_X_REAL)
 
 }  // namespace gbfft

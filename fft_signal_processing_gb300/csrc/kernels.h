@@ -96,16 +96,6 @@ __host__ __device__ constexpr bool rowst_use_big(int l) { return l >= kBigTileMi
 cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_t count,
                        int log2n1, const float2* tw, int flags, int* err, uint64_t limit_ns,
                        cudaStream_t s);
-// Three-pass pass 2: count columns of slabs [2^log2l][2^log2s] (slab z = t*A + ka,
-// A = 2^log2a), each output multiplied by w_M^{c*kb} (M = 2^(log2l+log2s)) and written as row
-// kb*A + ka of transform t.
-cudaError_t run_cols_slab(int log2l, int dir, const float2* in, float2* out, int64_t count,
-                          int log2s, const float2* tw, const float2* hi, const float2* lo,
-                          int lowbits, int log2a, int* err, uint64_t limit_ns, cudaStream_t s);
-constexpr int kThreePassMinLog2 = 25;  // above every supported size: two passes up to 2^24
-__host__ __device__ constexpr int threepass_log2a(int l) { return 8; }
-__host__ __device__ constexpr int threepass_log2b(int l) { return l - 16; }  // 7 or 8
-__host__ __device__ constexpr int threepass_log2c(int l) { return 8; }
 
 // blocks of W rows as for the column tiles (W <= N1 always holds for the four-step splits),
 // radix up to 64

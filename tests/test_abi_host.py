@@ -115,8 +115,6 @@ def test_path_choice(n, path, radix):
     l = n.bit_length() - 1
     if path == "fourstep":
         assert f"n1={1 << (l // 2)} n2={1 << (l - l // 2)}" in d
-    if path == "threestep":
-        assert f"a=256 b={1 << (l - 16)} c=256 kernels=3" in d
 
 
 def test_2d_and_real_paths():
