@@ -84,7 +84,7 @@ __host__ __device__ constexpr int cols_pass_maxrb(int l, int log2s) {
 // From 2^12 points a tile of W transforms fills most of an SM's shared memory, and the strided
 // passes run the tile kernels that keep the stage apart from a half-length exchange buffer, so
 // that the next tile's copy overlaps the transform of the current one.
-constexpr int kBigTileMinLog2 = 12;
+constexpr int kBigTileMinLog2 = 11;
 __host__ __device__ constexpr bool cols_use_big(int l, int log2s) {
     return l >= kBigTileMinLog2 && cols_use_tma(l, log2s);
 }
