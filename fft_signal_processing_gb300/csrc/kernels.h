@@ -81,9 +81,9 @@ __host__ __device__ constexpr int cols_pass_maxrb(int l, int log2s) {
     return cols_use_tma(l, log2s) ? cols_tma_maxrb(l) : cols_maxrb(l);
 }
 
-// From 2^12 points a tile of W transforms fills most of an SM's shared memory, and the strided
-// passes run the tile kernels that keep the stage apart from a half-length exchange buffer, so
-// that the next tile's copy overlaps the transform of the current one.
+// From 2^11 points (tiles of 64 and 128 KB) the strided passes run the tile kernels that keep
+// the stage apart from a half-length exchange buffer, so that the next tile's copy overlaps the
+// transform of the current one (measured faster than sharing one buffer at 2^11 and 2^12).
 constexpr int kBigTileMinLog2 = 11;
 __host__ __device__ constexpr bool cols_use_big(int l, int log2s) {
     return l >= kBigTileMinLog2 && cols_use_tma(l, log2s);

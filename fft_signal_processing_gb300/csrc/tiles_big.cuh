@@ -1,7 +1,8 @@
 // Persistent tile kernels for long strided transforms (column pass and transposed-row pass of
-// 4096-point transforms): the next tile's copy overlaps the whole transform of the current one.
+// 2048- and 4096-point transforms): the next tile's copy overlaps the whole transform of the
+// current one.
 //
-// A tile of W transforms of 4096 points is 128 KB, so one CTA fills most of an SM's shared
+// A tile of W = 4 transforms of 4096 points is 128 KB, so one CTA fills most of an SM's shared
 // memory and a design in which the stage doubles as the exchange buffer (cols_tma.cuh,
 // rowst_tma.cuh) leaves the SM idle while each tile is copied in and out.  Here the CTA keeps
 // the stage and a half-length exchange buffer apart (the two-phase exchange of rows_big.cuh,
