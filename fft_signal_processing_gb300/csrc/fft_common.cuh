@@ -125,44 +125,55 @@ __host__ __device__ constexpr int bitrev_c(int i, int bits) {
 }
 
 // In-register R-point DFT, unnormalised, sign DIR, natural order in and out:
-// v[k] <- sum_j v[j] exp(DIR*2*pi*i*j*k/R).  Radix-2 decimation in frequency over the
-// register array (every index is a compile-time constant after unrolling, so the closing
-// bit-reversal is only a renaming of registers).
+// v[k] <- sum_j v[j] exp(DIR*2*pi*i*j*k/R).  Decimation in frequency over the register array
+// (every index is a compile-time constant after unrolling, so the closing bit-reversal is only
+// a renaming of registers).  Stages go two bits at a time as radix-4 butterflies, with one
+// twiddle-free radix-2 stage last when log2 R is odd.  A radix-4 DIF butterfly on
+// a_n = v[k + n*q] (k < q, block of 4q) writes
+//   v[k]      = Y0,            v[k + q]  = Y2 * w^{2k},
+//   v[k + 2q] = Y1 * w^{k},    v[k + 3q] = Y3 * w^{3k},       w = exp(DIR*2*pi*i/(4q)),
+// Y_m = sum_n a_n (DIR*i)^{n*m}: exactly the positions two radix-2 DIF stages give, with one
+// complex multiplication fewer.
+template <int DIR, int R, int Q, int K>
+__device__ __forceinline__ void dif4_bfly(float2* v) {
+    const float2 a0 = v[K], a1 = v[K + Q], a2 = v[K + 2 * Q], a3 = v[K + 3 * Q];
+    const float2 t0 = cadd(a0, a2), t1 = csub(a0, a2), t2 = cadd(a1, a3);
+    const float2 d = csub(a1, a3);
+    const float2 t3 = DIR < 0 ? make_float2(d.y, -d.x) : make_float2(-d.y, d.x);  // DIR*i*d
+    constexpr int U = R / (4 * Q);  // w = exp(DIR*2*pi*i*U/R)
+    v[K] = cadd(t0, t2);
+    v[K + Q] = crot<DIR, 2 * K * U, R>(csub(t0, t2));
+    v[K + 2 * Q] = crot<DIR, K * U, R>(cadd(t1, t3));
+    v[K + 3 * Q] = crot<DIR, 3 * K * U, R>(csub(t1, t3));
+}
+template <int DIR, int R, int Q, int K = 0>
+__device__ __forceinline__ void dif4_block(float2* v) {
+    if constexpr (K < Q) {
+        dif4_bfly<DIR, R, Q, K>(v);
+        dif4_block<DIR, R, Q, K + 1>(v);
+    }
+}
+// stages covering bits S.. of the index (radix-2 stage s has half-size R >> (s+1))
+template <int DIR, int R, int S, int L>
+__device__ __forceinline__ void dif_stages(float2* v) {
+    if constexpr (S + 2 <= L) {
+        constexpr int Q = R >> (S + 2);
+#pragma unroll
+        for (int blk = 0; blk < R; blk += 4 * Q) dif4_block<DIR, R, Q>(v + blk);
+        dif_stages<DIR, R, S + 2, L>(v);
+    } else if constexpr (S + 1 == L) {  // radix 2 with half-size 1: no twiddles
+#pragma unroll
+        for (int blk = 0; blk < R; blk += 2) {
+            const float2 a = v[blk], b = v[blk + 1];
+            v[blk] = cadd(a, b);
+            v[blk + 1] = csub(a, b);
+        }
+    }
+}
 template <int R, int DIR>
 __device__ __forceinline__ void dft_reg(float2* v) {
     constexpr int L = ilog2c(R);
-#pragma unroll
-    for (int s = 0; s < L; ++s) {
-        const int half = R >> (s + 1);
-#pragma unroll
-        for (int blk = 0; blk < R; blk += 2 * half) {
-#pragma unroll
-            for (int k = 0; k < half; ++k) {
-                float2 a = v[blk + k], b = v[blk + k + half];
-                v[blk + k] = cadd(a, b);
-                v[blk + k + half] = csub(a, b);
-            }
-        }
-        // twiddles of this DIF stage: element k of the upper half times w_{2*half}^k
-#pragma unroll
-        for (int blk = 0; blk < R; blk += 2 * half) {
-#pragma unroll
-            for (int k = 1; k < half; ++k) {
-                // exponent k/(2*half) = k*(R/(2*half))/R
-                switch (k * (R / (2 * half))) {
-#define GBFFT_ROT(EE) case EE: v[blk + k + half] = crot<DIR, EE, R>(v[blk + k + half]); break;
-                    GBFFT_ROT(1) GBFFT_ROT(2) GBFFT_ROT(3) GBFFT_ROT(4) GBFFT_ROT(5) GBFFT_ROT(6)
-                    GBFFT_ROT(7) GBFFT_ROT(8) GBFFT_ROT(9) GBFFT_ROT(10) GBFFT_ROT(11)
-                    GBFFT_ROT(12) GBFFT_ROT(13) GBFFT_ROT(14) GBFFT_ROT(15) GBFFT_ROT(16)
-                    GBFFT_ROT(17) GBFFT_ROT(18) GBFFT_ROT(19) GBFFT_ROT(20) GBFFT_ROT(21)
-                    GBFFT_ROT(22) GBFFT_ROT(23) GBFFT_ROT(24) GBFFT_ROT(25) GBFFT_ROT(26)
-                    GBFFT_ROT(27) GBFFT_ROT(28) GBFFT_ROT(29) GBFFT_ROT(30) GBFFT_ROT(31)
-#undef GBFFT_ROT
-                    default: break;
-                }
-            }
-        }
-    }
+    dif_stages<DIR, R, 0, L>(v);
     float2 t[R];
 #pragma unroll
     for (int i = 0; i < R; ++i) t[i] = v[bitrev_c(i, L)];

@@ -33,11 +33,14 @@ struct RowsTmaCfg {
     static constexpr int STAGE = SROW * W;                          // float2 per stage
     static constexpr uint32_t BLOCK_BYTES = (uint32_t)W * N * 8u;
     static constexpr size_t SMEM_BYTES = (size_t)NST * STAGE * sizeof(float2);
+    // CTAs per SM the register allocation must allow: at 4096 points the shared memory holds
+    // six CTAs of 64 threads, and the registers must not allow fewer
+    static constexpr int MIN_CTAS = LOG2N_ == 12 ? 6 : 1;
     static_assert((STAGE * sizeof(float2)) % 128 == 0, "stages stay 128-byte aligned");
 };
 
 template <class RC, int DIR>
-__global__ void __launch_bounds__(RC::C::THREADS)
+__global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     k_rows_tma(const float2* in, float2* out, int64_t nrows, const float2* __restrict__ tw,
                int flags, int row_parity, int* err, uint64_t limit_ns) {
     using C = typename RC::C;
