@@ -78,7 +78,8 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     s.shift = shift;
     s.log2n = l;
     if (layout != FFT_LAYOUT_C2C) {
-        if (l < 2 || l > kMaxLog2RealH + 1) return FFT_ERR_UNSUPPORTED_SIZE;
+        static_assert(FFT_MAX_LOG2N_REAL == kMaxLog2RealH + 1, "header and kernels agree");
+        if (l < 2 || l > FFT_MAX_LOG2N_REAL) return FFT_ERR_UNSUPPORTED_SIZE;
         s.path = PATH_REAL;
     } else if (dims == 2) {
         if (l < 1 || l > FFT_MAX_LOG2N_2D) return FFT_ERR_UNSUPPORTED_SIZE;

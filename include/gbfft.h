@@ -60,13 +60,14 @@ enum {
 };
 
 /* Largest supported transform sizes. */
-#define FFT_MAX_LOG2N_1D 24 /* n <= 2^24 for dims = 1 (complex and real rows) */
-#define FFT_MAX_LOG2N_2D 12 /* n <= 2^12 per side for dims = 2 */
+#define FFT_MAX_LOG2N_1D 24   /* n <= 2^24 for dims = 1, complex rows */
+#define FFT_MAX_LOG2N_REAL 15 /* n <= 2^15 for the real layouts (one-pass n/2-point core) */
+#define FFT_MAX_LOG2N_2D 12   /* n <= 2^12 per side for dims = 2 */
 
 /*
  * fft_plan_create - plan a batched transform on the current CUDA device.
  *   n         transform length (dims 1) or image side (dims 2); power of two,
- *             1 <= n <= 2^24 (dims 1, complex), 4 <= n <= 2^24 (real layouts),
+ *             1 <= n <= 2^24 (dims 1, complex), 4 <= n <= 2^15 (real layouts),
  *             2 <= n <= 2^12 (dims 2).
  *   batch     number of rows (dims 1) or images (dims 2), >= 1.
  *   dims      1 or 2 (2 only with FFT_LAYOUT_C2C).
