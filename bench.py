@@ -205,6 +205,12 @@ def barrier(pg):
         pg.barrier()
 
 
+def job_rates(w, world, step_ms):
+    """Whole-job GFLOP/s and minimum-traffic GB/s: every rank transforms its own batch of the
+    workload (weak scaling), timed by the slowest rank's step."""
+    return (w.flops * world / (step_ms * 1e-3) / 1e9, w.min_bytes * world / (step_ms * 1e-3) / 1e9)
+
+
 def max_over_ranks(pg, v):
     if pg is None:
         return v
@@ -416,8 +422,7 @@ def main():
     step_ms = max_over_ranks(pg, step_ms_local)
     launch_ms = [statistics.mean(pl[i] for pl in per_launch) for i in range(kernels_per_step)]
 
-    gflops = w.flops * world / (step_ms * 1e-3) / 1e9
-    gbs_min = w.min_bytes * world / (step_ms * 1e-3) / 1e9
+    gflops, gbs_min = job_rates(w, world, step_ms)
 
     # roofline of the dominant launch (one library call = one or two kernels)
     peaks = {}
