@@ -152,8 +152,13 @@ def transform(x, direction=-1, dims=1, shift=False):
 
     direction -1: forward; with shift, the output is fftshift(FFT(x)).
     direction +1: inverse; with shift, the output is (-1)^j * IFFT(x) (chessboard post-multiply).
+    Rows whose length is not a power of two (dims 1) take the direct sum of Mota §2.2 Eq. 5.
     """
-    y = fft(x, direction) if dims == 1 else fft2d(x, direction)
+    n = np.shape(x)[-1]
+    if dims == 1:
+        y = fft(x, direction) if (n & (n - 1)) == 0 else dft(x, direction)
+    else:
+        y = fft2d(x, direction)
     if shift:
         y = fftshift(y, dims) if direction == -1 else chessboard(y, dims)
     return y

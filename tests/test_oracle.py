@@ -167,6 +167,25 @@ def test_chessboard_premultiply_equals_shift(n):
     assert rel(y, n * x) < 1e-14
 
 
+@pytest.mark.parametrize("n", [6, 12, 1000])
+def test_any_length_transform_and_shift(n):
+    """Lengths that are not powers of two: the direct sum against a brute-force outer product
+    written here (small n) or numpy's FFT; the chessboard identity still holds for even n."""
+    x = crand(3, n)
+    if n <= 64:
+        j = np.arange(n)
+        ref = x @ np.exp(-2j * np.pi * np.outer(j, j) / n)
+    else:
+        ref = np.fft.fft(x)
+    assert rel(oracle.transform(x, -1), ref) < 1e-12
+    assert rel(oracle.transform(x, +1), np.fft.ifft(x) * n) < 1e-12
+    lhs = oracle.dft(oracle.chessboard(x, 1), -1)
+    assert rel(lhs, oracle.transform(x, -1, 1, True)) < 1e-12
+    assert rel(lhs, np.fft.fftshift(ref, axes=-1)) < 1e-12
+    y = oracle.transform(oracle.transform(x, -1, 1, True), +1, 1, True)
+    assert rel(y, n * x) < 1e-12
+
+
 def test_chessboard_values():
     x = np.ones((1, 6), complex)
     np.testing.assert_array_equal(oracle.chessboard(x, 1)[0], [1, -1, 1, -1, 1, -1])
