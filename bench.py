@@ -7,7 +7,8 @@ resident in HBM.  The default workload is the batched 1-D C2C round trip: N = 40
 16384 rows (512 MiB of complex64), a forward transform with the fftshift folded in as the
 (-1)^j chessboard on its load, then the inverse transform (chessboard on its store) -- two
 kernel launches per step.  Other workloads (--workload): c2c_1024 (N = 1024 x 64 rows, forward),
-sweep_<log2n> (batch*N = 2^26 rows of 3 tones + noise, forward), real (2048 rows x 4096,
+sweep_<log2n> (batch*N = 2^26 rows of 3 tones + noise, forward), any_<n> (the same for a
+length n <= 8192 that is not a power of two: the chirp-z path), real (2048 rows x 4096,
 mmax = 1365, synthesis then analysis, m-major spectrum), 2d (4096 x 4096, forward with the 2-D
 chessboard then inverse).
 
@@ -73,6 +74,11 @@ class Workload:
             l = int(name.split("_")[1])
             self.kind, self.n, self.batch, self.dims, self.shift = "c2c_fwd", 1 << l, (1 << 26) >> l, 1, False
             self.desc = f"1-D C2C fp32 forward N=2^{l} x {(1 << 26) >> l} rows (3 tones + noise)"
+        elif name.startswith("any_"):
+            n = int(name.split("_")[1])
+            self.kind, self.n, self.batch, self.dims, self.shift = "c2c_fwd", n, (1 << 26) // n, 1, False
+            self.desc = (f"1-D C2C fp32 forward N={n} (not a power of two: chirp-z path) x "
+                         f"{(1 << 26) // n} rows (3 tones + noise)")
         elif name == "real":
             self.kind, self.n, self.batch, self.dims, self.shift = "real_rt", 4096, 2048, 1, False
             self.mmax = 1365
@@ -86,7 +92,7 @@ class Workload:
             raise SystemExit(f"unknown workload {name}")
         n = self.n
         self.points = self.batch * (n * n if self.dims == 2 else n)
-        self.log2n = int(math.log2(n))
+        self.log2n = math.log2(n)  # flop count 5*N*log2(N) for any N (CS598 metric)
         if self.kind == "real_rt":
             m1 = self.mmax + 1
             self.flops = 2 * 2.5 * n * self.log2n * self.batch

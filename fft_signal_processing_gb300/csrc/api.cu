@@ -13,6 +13,9 @@
 //   2d        n x n images: all rows, then all columns (Mota, "High Performance Fourier
 //             Transforms on GPUs with GLSL", §2.7 Eq. 19), both in place in the output.
 //   real      band-limited real rows through an n/2-point complex core (fourier.ts).
+//   bluestein dims 1, complex rows of any length n <= 8192 that is not a power of two: the
+//             chirp-z transform through m-point FFTs (m >= 2n - 1) in one kernel
+//             (bluestein.cuh); chirp and filter tables in double precision on the host.
 //
 // Twiddles are computed on the host in double precision from cos/sin of 2*pi*q/M with q
 // reduced modulo M in integers, and rounded once to float (fourier.ts header comment: device
@@ -37,7 +40,7 @@ using namespace gbfft;
 
 namespace {
 
-enum Path { PATH_ONEPASS = 0, PATH_FOURSTEP = 1, PATH_2D = 2, PATH_REAL = 3 };
+enum Path { PATH_ONEPASS = 0, PATH_FOURSTEP = 1, PATH_2D = 2, PATH_REAL = 3, PATH_BLUESTEIN = 4 };
 
 struct PlanSpec {
     int64_t n = 0, batch = 0;
@@ -46,6 +49,7 @@ struct PlanSpec {
     Path path = PATH_ONEPASS;
     int log2n1 = 0, log2n2 = 0;  // four-step split
     int lowbits = 0;             // four-step two-level twiddle split
+    int log2m = 0;               // chirp-z transform length
 };
 
 int ilog2_exact(int64_t n) {
@@ -67,7 +71,10 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     if (shift != 0 && shift != 1) return FFT_ERR_INVALID_ARG;
     if (layout != FFT_LAYOUT_C2C && (dims != 1 || shift)) return FFT_ERR_INVALID_ARG;
     const int l = ilog2_exact(n);
-    if (l < 0) return FFT_ERR_UNSUPPORTED_SIZE;
+    // lengths that are not powers of two: complex rows up to kMaxBluesteinN only
+    const bool any_length = l < 0 && layout == FFT_LAYOUT_C2C && dims == 1 && n >= 3 &&
+                            n <= kMaxBluesteinN;
+    if (l < 0 && !any_length) return FFT_ERR_UNSUPPORTED_SIZE;
     if (shift && (n & 1)) return FFT_ERR_INVALID_ARG;
     PlanSpec s;
     s.n = n;
@@ -77,7 +84,10 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     s.layout = layout;
     s.shift = shift;
     s.log2n = l;
-    if (layout != FFT_LAYOUT_C2C) {
+    if (any_length) {
+        s.path = PATH_BLUESTEIN;
+        s.log2m = bluestein_log2m(n);
+    } else if (layout != FFT_LAYOUT_C2C) {
         static_assert(FFT_MAX_LOG2N_REAL == kMaxLog2RealH + 1, "header and kernels agree");
         if (l < 2 || l > FFT_MAX_LOG2N_REAL) return FFT_ERR_UNSUPPORTED_SIZE;
         s.path = PATH_REAL;
@@ -194,6 +204,17 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
                      g2.threads, g2.per_cta, g2.smem);
             break;
         }
+        case PATH_BLUESTEIN: {
+            const int w = rows_log2w(s.log2m);
+            snprintf(buf, sizeof buf,
+                     "path=bluestein n=%lld batch=%lld %s shift=%d m=%d radix=%s kernels=1 "
+                     "threads=%d rows_per_cta=%d smem=%zu",
+                     (long long)s.n, (long long)s.batch, dir, s.shift, 1 << s.log2m,
+                     radix_string(s.log2m, rows_maxrb(s.log2m)).c_str(),
+                     (1 << rows_log2t(s.log2m)) << w, 1 << w,
+                     padded_bytes(s.log2m, rows_maxrb(s.log2m), w));
+            break;
+        }
         case PATH_2D: {
             Geo g1 = rows_geo(s.log2n), g2 = cols_geo(s.log2n, s.log2n);
             snprintf(buf, sizeof buf,
@@ -241,7 +262,7 @@ struct gbfft_plan_s {
     int device = 0;
     float2* d_tw = nullptr;
     size_t tw_count = 0;
-    size_t off_a = 0, off_b = 0, off_hi = 0, off_lo = 0, off_r = 0;
+    size_t off_a = 0, off_b = 0, off_hi = 0, off_lo = 0, off_r = 0, off_chirp = 0, off_bhat = 0;
     void* d_work = nullptr;
     size_t work_bytes = 0;
     int* d_err = nullptr;
@@ -265,7 +286,7 @@ const char* fft_status_string(int status) {
         case FFT_OK: return "FFT_OK: success";
         case FFT_ERR_INVALID_ARG: return "FFT_ERR_INVALID_ARG: invalid argument";
         case FFT_ERR_UNSUPPORTED_SIZE:
-            return "FFT_ERR_UNSUPPORTED_SIZE: size is not a supported power of two";
+            return "FFT_ERR_UNSUPPORTED_SIZE: size outside the supported lengths";
         case FFT_ERR_MISALIGNED: return "FFT_ERR_MISALIGNED: data pointer not 16-byte aligned";
         case FFT_ERR_OOM: return "FFT_ERR_OOM: device allocation failed";
         case FFT_ERR_CUDA: return "FFT_ERR_CUDA: CUDA runtime or launch error";
@@ -321,6 +342,11 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
             p->work_bytes = (size_t)s.batch * (size_t)s.n * sizeof(float2);
             break;
         }
+        case PATH_BLUESTEIN:
+            p->off_a = append_pass_tables(tw, s.log2m, rows_maxrb(s.log2m));
+            p->off_chirp = host::append_chirp(tw, s.n, s.direction);
+            p->off_bhat = host::append_chirp_filter(tw, s.n, int64_t(1) << s.log2m, s.direction);
+            break;
         case PATH_REAL:
             p->off_a = append_pass_tables(tw, s.log2n - 1, real_maxrb(s.log2n - 1));
             p->off_r = append_roots(tw, s.n / 2, 1, s.n);  // w_n^k, k < n/2
@@ -388,6 +414,12 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
             const int flags = s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0;
             e = run_rows(s.log2n, s.direction, x, y, s.batch, p->d_tw + p->off_a, flags, 0,
                          p->d_err, p->wait_limit_ns, st);
+            break;
+        }
+        case PATH_BLUESTEIN: {
+            const int flags = s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0;
+            e = run_bluestein(s.log2m, x, y, s.batch, (int)s.n, p->d_tw + p->off_chirp,
+                              p->d_tw + p->off_bhat, p->d_tw + p->off_a, flags, st);
             break;
         }
         case PATH_FOURSTEP: {

@@ -1,0 +1,138 @@
+// Rows of any length n (not a power of two, n <= 8192): the chirp-z (Bluestein) transform in
+// one kernel, one pass over HBM.
+//
+// With j*k = (j^2 + k^2 - (k-j)^2)/2 the length-n DFT of sign s is a convolution,
+//   X_k = c_k * sum_j (x_j c_j) b_{k-j},   c_j = exp(s*pi*i*j^2/n),   b_d = conj(c_d),
+// which m-point FFTs (m a power of two, m >= 2n - 1) evaluate exactly on k < n.  One CTA holds
+// W rows; for each row the kernel
+//   1. loads x_j * c_j for j < n, zero up to m (in the first radix pass's register order),
+//   2. runs the forward m-point Stockham passes (the same register/shared-memory machinery as
+//      every power-of-two kernel),
+//   3. multiplies by bhat = FFT_m(b)/m (a plan table computed in double precision on the host),
+//   4. reorders through shared memory into the first pass's order when the first and last
+//      radices differ, and runs the inverse m-point passes,
+//   5. stores c_k * conv_k for k < n.
+// The chessboard shift (even n) is fused as everywhere else: (-1)^j on the forward load,
+// (-1)^k on the inverse store.  Rows start at any 8-byte boundary, so the loads and stores are
+// plain coalesced per-element accesses rather than bulk copies.
+#pragma once
+
+#include "fft_kernel.cuh"
+
+namespace gbfft {
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    k_bluestein(const float2* in, float2* out, int64_t nrows, int n,
+                const float2* __restrict__ chirp, const float2* __restrict__ bhat,
+                const float2* __restrict__ tw, int flags) {
+    static_assert(C::TFAST, "a row's threads are adjacent lanes (coalesced row accesses)");
+    extern __shared__ float2 smem[];
+    const int w = (int)threadIdx.x / C::T;
+    const int t = (int)threadIdx.x % C::T;
+    const int64_t row = (int64_t)blockIdx.x * C::W + w;
+    const bool active = row < nrows;
+    float2* sb = smem + w * C::SROW;
+
+    constexpr int R0 = C::radix(0);
+    constexpr int B0 = C::E / R0;
+    constexpr int S0 = C::N / R0;
+    constexpr int RL = C::radix(C::NPASS - 1);
+    constexpr int BL = C::E / RL;
+    constexpr int SL = C::N / RL;
+
+    float2 v[C::E];
+    const float2* src = in + (active ? row * n : 0);
+#pragma unroll
+    for (int b = 0; b < B0; ++b) {
+        const int j = t + b * C::T;
+#pragma unroll
+        for (int r = 0; r < R0; ++r) {
+            const int e = j + r * S0;
+            float2 a = make_float2(0.f, 0.f);
+            if (active && e < n) {
+                a = cmul(ldg_stream(src + e), __ldg(chirp + e));
+                if (flags & KF_CHESS_LOAD) a = neg_if(a, e & 1);
+            }
+            v[b * R0 + r] = a;
+        }
+    }
+
+    run_passes<C, -1, 0>(v, t, sb, tw);  // A = FFT_m(a); element k = j + r*SL in registers
+
+    if constexpr (R0 == RL) {
+        // the last pass leaves element j + r*N/R in v[b*R + r]: the first pass's order already
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < RL; ++r)
+                v[b * RL + r] = cmul(v[b * RL + r], __ldg(bhat + j + r * SL));
+        }
+    } else {
+        __syncthreads();  // every thread has read the last exchange
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < RL; ++r) {
+                const int k = j + r * SL;
+                sb[spad<C::LP>(k) * C::SS] = cmul(v[b * RL + r], __ldg(bhat + k));
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int b = 0; b < B0; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < R0; ++r) v[b * R0 + r] = sb[spad<C::LP>(j + r * S0) * C::SS];
+        }
+    }
+    if constexpr (C::NPASS > 1) __syncthreads();  // the buffer becomes the next exchange buffer
+
+    run_passes<C, +1, 0>(v, t, sb, tw);  // conv = IFFT_m(A * bhat)
+
+    if (active) {
+        float2* dst = out + row * n;
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < RL; ++r) {
+                const int k = j + r * SL;
+                if (k < n) {
+                    float2 y = cmul(v[b * RL + r], __ldg(chirp + k));
+                    if (flags & KF_CHESS_STORE) y = neg_if(y, k & 1);
+                    stg_stream(dst + k, y);
+                }
+            }
+        }
+    }
+}
+
+template <class C>
+cudaError_t launch_bluestein(const float2* in, float2* out, int64_t nrows, int n,
+                             const float2* chirp, const float2* bhat, const float2* tw,
+                             int flags, cudaStream_t stream) {
+    auto kern = k_bluestein<C>;
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_dev != dev) {
+        if (C::SMEM_BYTES > 48 * 1024)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    if (2 * (int64_t)n - 1 > C::N) return cudaErrorInvalidValue;
+    const int64_t grid = (nrows + C::W - 1) / C::W;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(in, out, nrows, n, chirp, bhat,
+                                                                  tw, flags);
+    return cudaGetLastError();
+}
+
+}  // namespace gbfft

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <complex>
 #include <cstdint>
 #include <cstdlib>
 #include <vector>
@@ -72,6 +73,74 @@ inline size_t append_roots(std::vector<float2>& v, int64_t count, int64_t step, 
     align_table(v);
     const size_t off = v.size();
     for (int64_t q = 0; q < count; ++q) v.push_back(root_of_unity(q * step, m));
+    return off;
+}
+
+// ---- chirp-z (Bluestein) tables for a length-n transform of sign s, n not a power of two ----
+// With j*k = (j^2 + k^2 - (k-j)^2) / 2 the DFT becomes a convolution:
+//   X_k = c_k * sum_j (x_j c_j) b_{k-j},   c_j = exp(s*pi*i*j^2/n),   b_d = conj(c_d),
+// evaluated with m-point FFTs (m a power of two, m >= 2n-1, so the circular convolution of
+// the zero-padded sequences equals the linear one on k < n).  j^2 is reduced modulo 2n in
+// integers before the angle is formed.
+
+inline std::complex<double> chirp(int64_t j, int64_t n, int sign) {
+    const double pi = 3.141592653589793238462643383279502884;
+    const int64_t q = (int64_t)(((unsigned __int128)(j < 0 ? -j : j) * (uint64_t)(j < 0 ? -j : j)) %
+                                (uint64_t)(2 * n));
+    const double th = pi * (double)q / (double)n;
+    return {std::cos(th), (double)sign * std::sin(th)};
+}
+
+// In-place iterative radix-2 FFT in double precision (sign s, unnormalised), a.size() a power
+// of two; each twiddle is evaluated directly (no recurrence).  Plan-time use only.
+inline void fft_fp64(std::vector<std::complex<double>>& a, int sign) {
+    const size_t m = a.size();
+    for (size_t i = 1, j = 0; i < m; ++i) {  // bit-reversal permutation
+        size_t bit = m >> 1;
+        for (; j & bit; bit >>= 1) j ^= bit;
+        j ^= bit;
+        if (i < j) std::swap(a[i], a[j]);
+    }
+    const double two_pi = 6.283185307179586476925286766559005768;
+    for (size_t len = 2; len <= m; len <<= 1) {
+        for (size_t k = 0; k < len / 2; ++k) {
+            const double th = two_pi * (double)k / (double)len;
+            const std::complex<double> w(std::cos(th), (double)sign * std::sin(th));
+            for (size_t i = 0; i < m; i += len) {
+                const std::complex<double> u = a[i + k], t = w * a[i + k + len / 2];
+                a[i + k] = u + t;
+                a[i + k + len / 2] = u - t;
+            }
+        }
+    }
+}
+
+// c_j for j < n; returns the offset.
+inline size_t append_chirp(std::vector<float2>& v, int64_t n, int sign) {
+    align_table(v);
+    const size_t off = v.size();
+    for (int64_t j = 0; j < n; ++j) {
+        const std::complex<double> c = chirp(j, n, sign);
+        v.push_back(make_float2((float)c.real(), (float)c.imag()));
+    }
+    return off;
+}
+
+// FFT_m^(-)(b) / m with b_d = conj(c_d) placed circularly (d and m - d for |d| < n); returns
+// the offset.
+inline size_t append_chirp_filter(std::vector<float2>& v, int64_t n, int64_t m, int sign) {
+    std::vector<std::complex<double>> b((size_t)m, std::complex<double>(0.0, 0.0));
+    for (int64_t d = 0; d < n; ++d) {
+        const std::complex<double> c = std::conj(chirp(d, n, sign));
+        b[(size_t)d] = c;
+        if (d > 0) b[(size_t)(m - d)] = c;
+    }
+    fft_fp64(b, -1);
+    align_table(v);
+    const size_t off = v.size();
+    for (int64_t q = 0; q < m; ++q)
+        v.push_back(make_float2((float)(b[(size_t)q].real() / (double)m),
+                                (float)(b[(size_t)q].imag() / (double)m)));
     return off;
 }
 

@@ -3,6 +3,7 @@
 // dispatcher (dispatch.cu) selects at run time.
 #pragma once
 
+#include "bluestein.cuh"
 #include "fft_kernel.cuh"
 #include "kernels.h"
 #include "real_kernel.cuh"
@@ -118,4 +119,12 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
                                      int mmajor, const float2* tw, const float2* twr, int* err, \
                                      uint64_t lim, cudaStream_t s) {                            \
         return launch_c2r<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, err, lim, s);        \
+    }
+
+#define GBFFT_DEF_BLUESTEIN(L)                                                                 \
+    cudaError_t gbfft::bluestein_entry_##L(const float2* in, float2* out, int64_t nrows, int n, \
+                                           const float2* chirp, const float2* bhat,             \
+                                           const float2* tw, int flags, cudaStream_t s) {       \
+        using C = FftCfg<L, rows_maxrb(L), rows_log2w(L), true>;                               \
+        return launch_bluestein<C>(in, out, nrows, n, chirp, bhat, tw, flags, s);              \
     }

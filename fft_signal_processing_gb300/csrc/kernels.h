@@ -102,6 +102,19 @@ cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_
 __host__ __device__ constexpr int rowst_log2w(int l) { return tile_log2w(l); }
 __host__ __device__ constexpr int rowst_maxrb(int l) { return l >= 9 ? 6 : 4; }
 
+// Rows of any length n that is not a power of two (chirp-z transform through m = 2^log2m
+// points, m >= 2n - 1): chirp[j] = c_j (n entries), bhat = FFT_m(conj c)/m (m entries), tw the
+// m-point pass tables.  flags: KF_CHESS_LOAD / KF_CHESS_STORE (even n).
+cudaError_t run_bluestein(int log2m, const float2* in, float2* out, int64_t nrows, int n,
+                          const float2* chirp, const float2* bhat, const float2* tw, int flags,
+                          cudaStream_t s);
+constexpr int kMaxBluesteinN = 8192;  // 2n - 1 <= 2^14: one pass, the m-point row in one CTA
+__host__ __device__ constexpr int bluestein_log2m(int64_t n) {
+    int l = 0;
+    while ((int64_t(1) << l) < 2 * n - 1) ++l;
+    return l;
+}
+
 // Real rows of 2^(log2h+1) points.
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
                     int mmajor, const float2* tw, const float2* twr, int* err, cudaStream_t s);

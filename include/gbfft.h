@@ -52,7 +52,7 @@ enum {
     FFT_OK = 0,
     FFT_ERR_INVALID_ARG = -1,      /* NULL pointer, bad enum, batch < 1, wrong exec kind,
                                       shift with a real layout, band limit out of range */
-    FFT_ERR_UNSUPPORTED_SIZE = -2, /* n not a power of two, or above the maximum */
+    FFT_ERR_UNSUPPORTED_SIZE = -2, /* n outside the supported lengths (see fft_plan_create) */
     FFT_ERR_MISALIGNED = -3,       /* a data pointer is not 16-byte aligned */
     FFT_ERR_OOM = -4,              /* device allocation of tables or workspace failed */
     FFT_ERR_CUDA = -5,             /* a CUDA runtime call or kernel launch failed */
@@ -63,12 +63,18 @@ enum {
 #define FFT_MAX_LOG2N_1D 24   /* n <= 2^24 for dims = 1, complex rows */
 #define FFT_MAX_LOG2N_REAL 15 /* n <= 2^15 for the real layouts (one-pass n/2-point core) */
 #define FFT_MAX_LOG2N_2D 12   /* n <= 2^12 per side for dims = 2 */
+#define FFT_MAX_N_ANY_LENGTH 8192 /* complex rows (dims 1) whose length is not a power of two */
 
 /*
  * fft_plan_create - plan a batched transform on the current CUDA device.
- *   n         transform length (dims 1) or image side (dims 2); power of two,
+ *   n         transform length (dims 1) or image side (dims 2): a power of two with
  *             1 <= n <= 2^24 (dims 1, complex), 4 <= n <= 2^15 (real layouts),
- *             2 <= n <= 2^12 (dims 2).
+ *             2 <= n <= 2^12 (dims 2); or, for complex rows (dims 1, FFT_LAYOUT_C2C) only,
+ *             any length 3 <= n <= FFT_MAX_N_ANY_LENGTH, computed as the chirp-z (Bluestein)
+ *             transform X_k = c_k sum_j (x_j c_j) conj(c_{k-j}), c_j = exp(s*pi*i*j^2/n),
+ *             through power-of-two FFTs of length m >= 2n - 1 in one kernel (the same
+ *             unnormalised DFT of Mota, "High Performance Fourier Transforms on GPUs with
+ *             GLSL", 2.2 Eq. 5, for lengths the radix-2^k passes cannot split).
  *   batch     number of rows (dims 1) or images (dims 2), >= 1.
  *   dims      1 or 2 (2 only with FFT_LAYOUT_C2C).
  *   direction FFT_FORWARD or FFT_INVERSE.  Real layouts: FORWARD = analysis (R2C, exec with

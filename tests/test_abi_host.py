@@ -50,9 +50,21 @@ def q(n, batch=1, dims=1, direction=-1, layout=0, shift=0):
     return fx.lib().fft_plan_query(n, batch, dims, direction, layout, shift, None, 0)
 
 
-@pytest.mark.parametrize("n", [3, 6, 1000, 0, -4])
-def test_non_power_of_two_rejected(n):
+@pytest.mark.parametrize("n", [0, -4, 8193, 10000, 3 << 20])
+def test_lengths_outside_the_supported_set_rejected(n):
     assert q(n) == fx.FFT_ERR_UNSUPPORTED_SIZE
+
+
+@pytest.mark.parametrize("n,m", [(3, 8), (5, 16), (6, 16), (100, 256), (1000, 2048),
+                                 (1025, 4096), (4096 + 1, 16384), (8191, 16384)])
+def test_any_length_rows_take_the_chirp_z_path(n, m):
+    d = fx.query(n, 5)
+    assert "path=bluestein" in d and f"m={m} " in d and "kernels=1" in d
+    assert m >= 2 * n - 1 and m // 2 < 2 * n - 1  # the smallest power of two that suffices
+    assert q(n, shift=1) == (fx.FFT_OK if n % 2 == 0 else fx.FFT_ERR_INVALID_ARG)
+    # real layouts and 2-D images stay powers of two
+    assert q(n, layout=1) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert q(n, dims=2) == fx.FFT_ERR_UNSUPPORTED_SIZE
 
 
 def test_size_limits():
@@ -85,7 +97,7 @@ def test_batch_overflow_rejected():
 
 def test_create_rejects_before_touching_the_device():
     h = ctypes.c_void_p(1)
-    rc = fx.lib().fft_plan_create(6, 1, 1, -1, 0, 0, ctypes.byref(h))
+    rc = fx.lib().fft_plan_create(8193, 1, 1, -1, 0, 0, ctypes.byref(h))
     assert rc == fx.FFT_ERR_UNSUPPORTED_SIZE and not h.value
     assert fx.lib().fft_plan_create(8, 1, 1, -1, 0, 0, None) == fx.FFT_ERR_INVALID_ARG
 

@@ -1,0 +1,104 @@
+"""GPU parity of complex rows whose length is not a power of two (the chirp-z path) against
+the fp64 oracle's direct sum (Mota, "High Performance Fourier Transforms on GPUs with GLSL",
+§2.2 Eq. 5), through the C ABI.
+
+Lengths span every chirp-z size m = 8 .. 16384 (m the power of two >= 2n - 1), including
+n just above and below powers of two, odd and even n, ragged batches, both directions, the
+chessboard shift (even n), in place, and one full benchmark-sized batch with sampled rows.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def fx():
+    import fft_signal_processing_gb300 as m
+
+    return m
+
+
+def wl():
+    from fft_signal_processing_gb300 import workloads
+
+    return workloads
+
+
+def gpu_c2c(x, n, batch, direction, shift=False, inplace=False):
+    m = fx()
+    p = m.Plan(n, batch, 1, direction, shift=shift)
+    assert "path=bluestein" in p.describe()
+    xd = torch.from_numpy(np.ascontiguousarray(x, dtype=np.complex64)).cuda()
+    if inplace:
+        p.c2c(xd, out=xd)
+        y = xd
+    else:
+        y = p.c2c(xd)
+    torch.cuda.synchronize()
+    p.check()
+    return y.cpu().numpy()
+
+
+LENGTHS = [3, 5, 6, 7, 12, 31, 33, 100, 127, 129, 255, 257, 1000, 1023, 1025, 2047, 3000,
+           4095, 4097, 6000, 8191]
+
+
+@pytest.mark.parametrize("n", LENGTHS)
+@pytest.mark.parametrize("direction", [-1, 1])
+def test_any_length_grid(n, direction):
+    batch = 37 if n <= 1100 else 3  # ragged against every rows-per-CTA count
+    x = wl().normal(7000 + n, batch, n)
+    got = gpu_c2c(x, n, batch, direction)
+    assert_parity(got, oracle.transform(x, direction), n, f"n={n} dir={direction}")
+
+
+@pytest.mark.parametrize("n", [6, 100, 1000, 4098, 8190])
+@pytest.mark.parametrize("direction", [-1, 1])
+def test_any_length_shift_in_place(n, direction):
+    batch = 5
+    x = wl().uniform(7100 + n, batch, n)
+    got = gpu_c2c(x, n, batch, direction, shift=True, inplace=True)
+    assert_parity(got, oracle.transform(x, direction, 1, True), n, f"shift n={n}")
+
+
+@pytest.mark.parametrize("n", [3, 1000, 8191])
+def test_any_length_round_trip_and_tones(n):
+    batch = 4
+    x = wl().tones(7200 + n, batch, n)
+    y = gpu_c2c(x, n, batch, -1)
+    z = gpu_c2c(y, n, batch, +1)
+    assert_parity(z, n * x.astype(np.complex128), n, f"round trip n={n}")
+    f, phi = wl().tone_params(7200 + n, batch, n)
+    for r in range(batch):  # unit tones land on their bins with magnitude ~ n
+        for k in set(f[r]):
+            amp = n * abs(np.sum(np.exp(1j * phi[r][f[r] == k])))
+            assert abs(abs(y[r, k]) - amp) < 0.05 * n + 0.6 * (2 * n) ** 0.5
+
+
+def test_any_length_full_batch_sampled():
+    """The benchmark's any-length workload at full size (n = 1000, batch = 2^26 // 1000),
+    sampled rows against the oracle's direct sum."""
+    m = fx()
+    n = 1000
+    batch = (1 << 26) // n
+    x = wl().tones(7300, batch, n)
+    p = m.Plan(n, batch, 1, m.FORWARD)
+    y = p.c2c(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    p.check()
+    rng = np.random.default_rng(7300)
+    rows = np.array(sorted({0, batch - 1, batch // 2, *rng.integers(0, batch, 29).tolist()}))
+    ys = y[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_parity(ys, oracle.transform(x[rows], -1), n, "n=1000 full batch")
