@@ -127,7 +127,7 @@ class Plan:
         self._h = h
         self.mmax = None
         if layout != LAYOUT_C2C:
-            self.mmax = self.n // 2 - 1 if mmax is None else int(mmax)
+            self.mmax = (self.n - 1) // 2 if mmax is None else int(mmax)
             _check(lib().fft_plan_set_band_limit(self._h, self.mmax), "fft_plan_set_band_limit")
 
     @property

@@ -13,9 +13,9 @@
 //   2d        n x n images: all rows, then all columns (Mota, "High Performance Fourier
 //             Transforms on GPUs with GLSL", §2.7 Eq. 19), both in place in the output.
 //   real      band-limited real rows through an n/2-point complex core (fourier.ts).
-//   bluestein dims 1, complex rows of any length n <= 8192 that is not a power of two: the
-//             chirp-z transform through m-point FFTs (m >= 2n - 1) in one kernel
-//             (bluestein.cuh); chirp and filter tables in double precision on the host.
+//   bluestein dims 1, complex or band-limited real rows of any length n <= 8192 that is not a
+//             power of two: the chirp-z transform through m-point FFTs (m >= 2n - 1) in one
+//             kernel (bluestein.cuh); chirp and filter tables in double precision on the host.
 //
 // Twiddles are computed on the host in double precision from cos/sin of 2*pi*q/M with q
 // reduced modulo M in integers, and rounded once to float (fourier.ts header comment: device
@@ -72,8 +72,7 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     if (layout != FFT_LAYOUT_C2C && (dims != 1 || shift)) return FFT_ERR_INVALID_ARG;
     const int l = ilog2_exact(n);
     // lengths that are not powers of two: complex rows up to kMaxBluesteinN only
-    const bool any_length = l < 0 && layout == FFT_LAYOUT_C2C && dims == 1 && n >= 3 &&
-                            n <= kMaxBluesteinN;
+    const bool any_length = l < 0 && dims == 1 && n >= 3 && n <= kMaxBluesteinN;
     if (l < 0 && !any_length) return FFT_ERR_UNSUPPORTED_SIZE;
     if (shift && (n & 1)) return FFT_ERR_INVALID_ARG;
     PlanSpec s;
@@ -206,10 +205,18 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
         }
         case PATH_BLUESTEIN: {
             const int w = rows_log2w(s.log2m);
+            const bool real = s.layout != FFT_LAYOUT_C2C;
+            char what[96];
+            if (real)
+                snprintf(what, sizeof what, "%s mmax=%lld layout=%s",
+                         s.direction < 0 ? "analysis(r2c)" : "synthesis(c2r)", (long long)mmax,
+                         s.layout == FFT_LAYOUT_REAL_MMAJOR ? "mmajor" : "rowmajor");
+            else
+                snprintf(what, sizeof what, "%s shift=%d", dir, s.shift);
             snprintf(buf, sizeof buf,
-                     "path=bluestein n=%lld batch=%lld %s shift=%d m=%d radix=%s kernels=1 "
+                     "path=bluestein n=%lld batch=%lld %s m=%d radix=%s kernels=1 "
                      "threads=%d rows_per_cta=%d smem=%zu",
-                     (long long)s.n, (long long)s.batch, dir, s.shift, 1 << s.log2m,
+                     (long long)s.n, (long long)s.batch, what, 1 << s.log2m,
                      radix_string(s.log2m, rows_maxrb(s.log2m)).c_str(),
                      (1 << rows_log2t(s.log2m)) << w, 1 << w,
                      padded_bytes(s.log2m, rows_maxrb(s.log2m), w));
@@ -301,7 +308,7 @@ int fft_plan_query(int64_t n, int64_t batch, int dims, int direction, int layout
     const int rc = plan_spec(n, batch, dims, direction, layout, shift, &s);
     if (rc != FFT_OK) return rc;
     if (buf && len) {
-        std::string d = describe_spec(s, s.path == PATH_REAL ? s.n / 2 - 1 : 0);
+        std::string d = describe_spec(s, s.layout != FFT_LAYOUT_C2C ? (s.n - 1) / 2 : 0);
         snprintf(buf, len, "%s", d.c_str());
     }
     return FFT_OK;
@@ -318,7 +325,7 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
     gbfft_plan_s* p = new (std::nothrow) gbfft_plan_s();
     if (!p) return FFT_ERR_OOM;
     p->s = s;
-    p->mmax = s.path == PATH_REAL ? s.n / 2 - 1 : 0;
+    p->mmax = s.layout != FFT_LAYOUT_C2C ? (s.n - 1) / 2 : 0;  // largest m with 2m < n
     if (cudaGetDevice(&p->device) != cudaSuccess) {
         delete p;
         return FFT_ERR_CUDA;
@@ -372,8 +379,8 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
 }
 
 int fft_plan_set_band_limit(fft_plan p, int64_t mmax) {
-    if (!p || p->s.path != PATH_REAL) return FFT_ERR_INVALID_ARG;
-    if (mmax < 0 || mmax >= p->s.n / 2) return FFT_ERR_INVALID_ARG;
+    if (!p || p->s.layout == FFT_LAYOUT_C2C) return FFT_ERR_INVALID_ARG;
+    if (mmax < 0 || 2 * mmax >= p->s.n) return FFT_ERR_INVALID_ARG;
     p->mmax = mmax;
     return FFT_OK;
 }
@@ -418,7 +425,7 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
         }
         case PATH_BLUESTEIN: {
             const int flags = s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0;
-            e = run_bluestein(s.log2m, x, y, s.batch, (int)s.n, p->d_tw + p->off_chirp,
+            e = run_bluestein(s.log2m, 0, x, y, s.batch, (int)s.n, 0, 0, p->d_tw + p->off_chirp,
                               p->d_tw + p->off_bhat, p->d_tw + p->off_a, flags, st);
             break;
         }
@@ -454,28 +461,39 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
 int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
     if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
     const PlanSpec& s = p->s;
-    if (s.path != PATH_REAL || s.direction != FFT_FORWARD) return FFT_ERR_INVALID_ARG;
+    if (s.layout == FFT_LAYOUT_C2C || s.direction != FFT_FORWARD) return FFT_ERR_INVALID_ARG;
     if (!aligned16(in) || !aligned16(out)) return FFT_ERR_MISALIGNED;
     const size_t in_bytes = (size_t)s.batch * (size_t)s.n * 4u;
     const size_t out_bytes = (size_t)s.batch * (size_t)(p->mmax + 1) * 8u;
     if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
-    cudaError_t e = run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax,
-                            s.layout == FFT_LAYOUT_REAL_MMAJOR, p->d_tw + p->off_a,
-                            p->d_tw + p->off_r, p->d_err, (cudaStream_t)stream);
+    const int mmajor = s.layout == FFT_LAYOUT_REAL_MMAJOR;
+    cudaError_t e =
+        s.path == PATH_BLUESTEIN
+            ? run_bluestein(s.log2m, 1, in, out, s.batch, (int)s.n, (int)p->mmax, mmajor,
+                            p->d_tw + p->off_chirp, p->d_tw + p->off_bhat, p->d_tw + p->off_a,
+                            0, (cudaStream_t)stream)
+            : run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax, mmajor,
+                      p->d_tw + p->off_a, p->d_tw + p->off_r, p->d_err, (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
 
 int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
     if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
     const PlanSpec& s = p->s;
-    if (s.path != PATH_REAL || s.direction != FFT_INVERSE) return FFT_ERR_INVALID_ARG;
+    if (s.layout == FFT_LAYOUT_C2C || s.direction != FFT_INVERSE) return FFT_ERR_INVALID_ARG;
     if (!aligned16(in) || !aligned16(out)) return FFT_ERR_MISALIGNED;
     const size_t in_bytes = (size_t)s.batch * (size_t)(p->mmax + 1) * 8u;
     const size_t out_bytes = (size_t)s.batch * (size_t)s.n * 4u;
     if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
-    cudaError_t e = run_c2r(s.log2n - 1, (const float2*)in, out, s.batch, (int)p->mmax,
-                            s.layout == FFT_LAYOUT_REAL_MMAJOR, p->d_tw + p->off_a,
-                            p->d_tw + p->off_r, p->d_err, p->wait_limit_ns, (cudaStream_t)stream);
+    const int mmajor = s.layout == FFT_LAYOUT_REAL_MMAJOR;
+    cudaError_t e =
+        s.path == PATH_BLUESTEIN
+            ? run_bluestein(s.log2m, 2, in, out, s.batch, (int)s.n, (int)p->mmax, mmajor,
+                            p->d_tw + p->off_chirp, p->d_tw + p->off_bhat, p->d_tw + p->off_a,
+                            0, (cudaStream_t)stream)
+            : run_c2r(s.log2n - 1, (const float2*)in, out, s.batch, (int)p->mmax, mmajor,
+                      p->d_tw + p->off_a, p->d_tw + p->off_r, p->d_err, p->wait_limit_ns,
+                      (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
 

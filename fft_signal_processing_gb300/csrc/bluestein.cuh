@@ -15,15 +15,24 @@
 // The chessboard shift (even n) is fused as everywhere else: (-1)^j on the forward load,
 // (-1)^k on the inverse store.  Rows start at any 8-byte boundary, so the loads and stores are
 // plain coalesced per-element accesses rather than bulk copies.
+//
+// The same kernel serves band-limited real rows of any length (the direct-sum 'dft' mode of
+// "src/sht/wgsl/fourier.ts", dftAnalysWGSL / dftSynthWGSL, for lengths the power-of-two path
+// cannot take): analysis (BLU_R2C) loads the real row as complex points with zero imaginary
+// part and stores F_m, m <= mmax, into the row-major or m-major spectrum; synthesis (BLU_C2R)
+// assembles the Hermitian spectrum on the load (X_0 = Re F_0, X_m = F_m, X_{n-m} = conj F_m
+// for 1 <= m <= mmax, other bins 0) and stores the real part of the inverse transform.
 #pragma once
 
 #include "fft_kernel.cuh"
 
 namespace gbfft {
 
-template <class C>
+enum : int { BLU_C2C = 0, BLU_R2C = 1, BLU_C2R = 2 };
+
+template <class C, int MODE>
 __global__ void __launch_bounds__(C::THREADS)
-    k_bluestein(const float2* in, float2* out, int64_t nrows, int n,
+    k_bluestein(const void* in_, void* out_, int64_t nrows, int n, int mmax, int mmajor,
                 const float2* __restrict__ chirp, const float2* __restrict__ bhat,
                 const float2* __restrict__ tw, int flags) {
     static_assert(C::TFAST, "a row's threads are adjacent lanes (coalesced row accesses)");
@@ -41,8 +50,23 @@ __global__ void __launch_bounds__(C::THREADS)
     constexpr int BL = C::E / RL;
     constexpr int SL = C::N / RL;
 
+    // element e of the length-n input: a complex row, a real row, or the Hermitian spectrum
+    auto load = [&](int e) -> float2 {
+        if constexpr (MODE == BLU_C2C) {
+            return ldg_stream(static_cast<const float2*>(in_) + row * n + e);
+        } else if constexpr (MODE == BLU_R2C) {
+            return make_float2(__ldcs(static_cast<const float*>(in_) + row * n + e), 0.f);
+        } else {
+            const float2* F = static_cast<const float2*>(in_);
+            const int m = e <= mmax ? e : n - e;  // bins above n - mmax mirror m = n - e
+            if (e > mmax && e < n - mmax) return make_float2(0.f, 0.f);
+            const float2 f = ldg_stream(F + (mmajor ? (int64_t)m * nrows + row
+                                                    : row * (mmax + 1) + m));
+            if (e == 0) return make_float2(f.x, 0.f);
+            return e <= mmax ? f : make_float2(f.x, -f.y);
+        }
+    };
     float2 v[C::E];
-    const float2* src = in + (active ? row * n : 0);
 #pragma unroll
     for (int b = 0; b < B0; ++b) {
         const int j = t + b * C::T;
@@ -51,7 +75,7 @@ __global__ void __launch_bounds__(C::THREADS)
             const int e = j + r * S0;
             float2 a = make_float2(0.f, 0.f);
             if (active && e < n) {
-                a = cmul(ldg_stream(src + e), __ldg(chirp + e));
+                a = cmul(load(e), __ldg(chirp + e));
                 if (flags & KF_CHESS_LOAD) a = neg_if(a, e & 1);
             }
             v[b * R0 + r] = a;
@@ -92,29 +116,37 @@ __global__ void __launch_bounds__(C::THREADS)
 
     run_passes<C, +1, 0>(v, t, sb, tw);  // conv = IFFT_m(A * bhat)
 
+    const int kend = MODE == BLU_R2C ? mmax + 1 : n;  // outputs kept
     if (active) {
-        float2* dst = out + row * n;
 #pragma unroll
         for (int b = 0; b < BL; ++b) {
             const int j = t + b * C::T;
 #pragma unroll
             for (int r = 0; r < RL; ++r) {
                 const int k = j + r * SL;
-                if (k < n) {
+                if (k < kend) {
                     float2 y = cmul(v[b * RL + r], __ldg(chirp + k));
-                    if (flags & KF_CHESS_STORE) y = neg_if(y, k & 1);
-                    stg_stream(dst + k, y);
+                    if constexpr (MODE == BLU_C2C) {
+                        if (flags & KF_CHESS_STORE) y = neg_if(y, k & 1);
+                        stg_stream(static_cast<float2*>(out_) + row * n + k, y);
+                    } else if constexpr (MODE == BLU_R2C) {
+                        stg_stream(static_cast<float2*>(out_) +
+                                       (mmajor ? (int64_t)k * nrows + row : row * (mmax + 1) + k),
+                                   y);
+                    } else {
+                        __stcs(static_cast<float*>(out_) + row * n + k, y.x);
+                    }
                 }
             }
         }
     }
 }
 
-template <class C>
-cudaError_t launch_bluestein(const float2* in, float2* out, int64_t nrows, int n,
-                             const float2* chirp, const float2* bhat, const float2* tw,
-                             int flags, cudaStream_t stream) {
-    auto kern = k_bluestein<C>;
+template <class C, int MODE>
+cudaError_t launch_bluestein(const void* in, void* out, int64_t nrows, int n, int mmax,
+                             int mmajor, const float2* chirp, const float2* bhat,
+                             const float2* tw, int flags, cudaStream_t stream) {
+    auto kern = k_bluestein<C, MODE>;
     static int configured_dev = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -130,8 +162,8 @@ cudaError_t launch_bluestein(const float2* in, float2* out, int64_t nrows, int n
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(in, out, nrows, n, chirp, bhat,
-                                                                  tw, flags);
+    kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(in, out, nrows, n, mmax, mmajor,
+                                                                  chirp, bhat, tw, flags);
     return cudaGetLastError();
 }
 

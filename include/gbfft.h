@@ -63,14 +63,16 @@ enum {
 #define FFT_MAX_LOG2N_1D 24   /* n <= 2^24 for dims = 1, complex rows */
 #define FFT_MAX_LOG2N_REAL 15 /* n <= 2^15 for the real layouts (one-pass n/2-point core) */
 #define FFT_MAX_LOG2N_2D 12   /* n <= 2^12 per side for dims = 2 */
-#define FFT_MAX_N_ANY_LENGTH 8192 /* complex rows (dims 1) whose length is not a power of two */
+#define FFT_MAX_N_ANY_LENGTH 8192 /* rows (dims 1, complex or real) whose length is not a power of two */
 
 /*
  * fft_plan_create - plan a batched transform on the current CUDA device.
  *   n         transform length (dims 1) or image side (dims 2): a power of two with
  *             1 <= n <= 2^24 (dims 1, complex), 4 <= n <= 2^15 (real layouts),
- *             2 <= n <= 2^12 (dims 2); or, for complex rows (dims 1, FFT_LAYOUT_C2C) only,
- *             any length 3 <= n <= FFT_MAX_N_ANY_LENGTH, computed as the chirp-z (Bluestein)
+ *             2 <= n <= 2^12 (dims 2); or, for rows (dims 1) only,
+ *             any length 3 <= n <= FFT_MAX_N_ANY_LENGTH (complex rows and band-limited real
+ *             rows, dims 1; for real rows this is the any-nphi role of the direct-sum 'dft'
+ *             mode of fourier.ts), computed as the chirp-z (Bluestein)
  *             transform X_k = c_k sum_j (x_j c_j) conj(c_{k-j}), c_j = exp(s*pi*i*j^2/n),
  *             through power-of-two FFTs of length m >= 2n - 1 in one kernel (the same
  *             unnormalised DFT of Mota, "High Performance Fourier Transforms on GPUs with
@@ -99,7 +101,7 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
  * fft_plan_set_band_limit - set mmax for a real-layout plan: the analysis keeps m = 0..mmax,
  * the synthesis reads F_0..F_mmax and assembles the Hermitian spectrum X_0 = Re F_0,
  * X_m = F_m, X_{n-m} = conj F_m (fourier.ts header comment and fftSynthWGSL).  Requires
- * 0 <= mmax < n/2 (no Nyquist bin).  The default is n/2 - 1.  Host only.
+ * 0 <= 2*mmax < n (no Nyquist bin).  The default is (n-1)/2 (n/2 - 1 for even n).  Host only.
  * Returns FFT_OK or FFT_ERR_INVALID_ARG (NULL plan, C2C plan, mmax out of range).
  */
 int fft_plan_set_band_limit(fft_plan plan, int64_t mmax);

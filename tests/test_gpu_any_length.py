@@ -1,6 +1,8 @@
-"""GPU parity of complex rows whose length is not a power of two (the chirp-z path) against
-the fp64 oracle's direct sum (Mota, "High Performance Fourier Transforms on GPUs with GLSL",
-§2.2 Eq. 5), through the C ABI.
+"""GPU parity of rows whose length is not a power of two (the chirp-z path) against the fp64
+oracle's direct sums, through the C ABI: complex rows against the DFT of Mota, "High
+Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5; band-limited real rows against
+the direct analysis/synthesis sums of fourier.ts (dftAnalysWGSL / dftSynthWGSL), both spectrum
+layouts.
 
 Lengths span every chirp-z size m = 8 .. 16384 (m the power of two >= 2n - 1), including
 n just above and below powers of two, odd and even n, ragged batches, both directions, the
@@ -102,3 +104,68 @@ def test_any_length_full_batch_sampled():
     rows = np.array(sorted({0, batch - 1, batch // 2, *rng.integers(0, batch, 29).tolist()}))
     ys = y[torch.from_numpy(rows).cuda()].cpu().numpy()
     assert_parity(ys, oracle.transform(x[rows], -1), n, "n=1000 full batch")
+
+
+# ---- band-limited real rows of any length (the any-nphi 'dft' mode) --------------------------
+LAYOUTS = {"rowmajor": 1, "mmajor": 2}
+
+
+def gpu_c2r(F_rowmajor, n, mmax, layout):
+    m = fx()
+    rows = F_rowmajor.shape[0]
+    p = m.Plan(n, rows, 1, m.INVERSE, layout=LAYOUTS[layout], mmax=mmax)
+    assert "path=bluestein" in p.describe()
+    Fin = oracle.to_mmajor(F_rowmajor) if layout == "mmajor" else F_rowmajor
+    x = p.c2r(torch.from_numpy(np.ascontiguousarray(Fin, dtype=np.complex64)).cuda())
+    torch.cuda.synchronize()
+    p.check()
+    return x.cpu().numpy()
+
+
+def gpu_r2c(x, mmax, layout):
+    m = fx()
+    rows, n = x.shape
+    p = m.Plan(n, rows, 1, m.FORWARD, layout=LAYOUTS[layout], mmax=mmax)
+    assert "path=bluestein" in p.describe()
+    F = p.r2c(torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda())
+    torch.cuda.synchronize()
+    p.check()
+    F = F.cpu().numpy()
+    return oracle.from_mmajor(F) if layout == "mmajor" else F
+
+
+REAL_LENGTHS = [3, 5, 6, 100, 999, 1000, 3000, 6000, 8191]
+
+
+@pytest.mark.parametrize("n", REAL_LENGTHS)
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+def test_any_length_real_synthesis(n, layout):
+    for mmax in sorted({0, (n - 1) // 2, max(0, n // 7)}):
+        rows = 33 if n <= 1000 else 3
+        F = wl().spectrum(7400 + n + mmax, rows, mmax)
+        got = gpu_c2r(F, n, mmax, layout)
+        assert_parity(got, oracle.c2r_direct(F, n), n, f"c2r n={n} mmax={mmax} {layout}")
+
+
+@pytest.mark.parametrize("n", REAL_LENGTHS)
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+def test_any_length_real_analysis(n, layout):
+    for mmax in sorted({0, (n - 1) // 2, max(0, n // 7)}):
+        rows = 33 if n <= 1000 else 3
+        x = wl().real_normal(7500 + n + mmax, rows, n)
+        got = gpu_r2c(x, mmax, layout)
+        ref = oracle.r2c_direct(x, mmax)
+        # per-row scale ||x_row||_2 (the RMS of the full spectrum), since few bins may be kept
+        scale = np.linalg.norm(x.astype(np.float64), axis=1)
+        assert_parity(got, ref, mmax + 1, f"r2c n={n} mmax={mmax} {layout}", scale=scale)
+
+
+@pytest.mark.parametrize("n", [1000, 6000])
+def test_any_length_real_round_trip(n):
+    mmax = (n - 1) // 2
+    F = wl().spectrum(7600 + n, 4, mmax)
+    x = gpu_c2r(F, n, mmax, "mmajor")
+    G = gpu_r2c(x, mmax, "mmajor")
+    ref = n * F.astype(np.complex128)
+    ref[:, 0] = n * F[:, 0].real
+    assert_parity(G, ref, mmax + 1, f"analysis(synthesis) n={n}")

@@ -186,6 +186,22 @@ def test_any_length_transform_and_shift(n):
     assert rel(y, n * x) < 1e-12
 
 
+@pytest.mark.parametrize("n,mmax", [(7, 3), (12, 5), (1000, 499), (999, 100)])
+def test_direct_band_limited_sums_any_length(n, mmax):
+    """Real rows of any length: the direct analysis/synthesis sums against numpy's real FFT
+    (rfft truncated to mmax; irfft of the zero-padded spectrum times n, which also ignores
+    Im F_0, as fourier.ts's synthesis does)."""
+    rng = np.random.default_rng(n)
+    x = rng.standard_normal((3, n))
+    F = oracle.r2c_direct(x, mmax)
+    assert rel(F, np.fft.rfft(x)[:, :mmax + 1]) < 1e-12
+    G = rng.standard_normal((3, mmax + 1)) + 1j * rng.standard_normal((3, mmax + 1))
+    pad = np.zeros((3, n // 2 + 1), complex)
+    pad[:, :mmax + 1] = G
+    pad[:, 0] = G[:, 0].real
+    assert rel(oracle.c2r_direct(G, n), np.fft.irfft(pad, n) * n) < 1e-12
+
+
 def test_chessboard_values():
     x = np.ones((1, 6), complex)
     np.testing.assert_array_equal(oracle.chessboard(x, 1)[0], [1, -1, 1, -1, 1, -1])
