@@ -8,7 +8,8 @@ resident in HBM.  The default workload is the batched 1-D C2C round trip: N = 40
 (-1)^j chessboard on its load, then the inverse transform (chessboard on its store) -- two
 kernel launches per step.  Other workloads (--workload): c2c_1024 (N = 1024 x 64 rows, forward),
 sweep_<log2n> (batch*N = 2^26 rows of 3 tones + noise, forward), any_<n> (the same for a
-length n <= 8192 that is not a power of two: the chirp-z path), real (2048 rows x 4096,
+length n <= 8192 that is not a power of two: the chirp-z path), realany_<n> (the real
+workload below for such a length, mmax = n/3), real (2048 rows x 4096,
 mmax = 1365, synthesis then analysis, m-major spectrum), 2d (4096 x 4096, forward with the 2-D
 chessboard then inverse).
 
@@ -79,6 +80,12 @@ class Workload:
             self.kind, self.n, self.batch, self.dims, self.shift = "c2c_fwd", n, (1 << 26) // n, 1, False
             self.desc = (f"1-D C2C fp32 forward N={n} (not a power of two: chirp-z path) x "
                          f"{(1 << 26) // n} rows (3 tones + noise)")
+        elif name.startswith("realany_"):
+            n = int(name.split("_")[1])
+            self.kind, self.n, self.batch, self.dims, self.shift = "real_rt", n, 2048, 1, False
+            self.mmax = n // 3
+            self.desc = (f"real rows 2048 x {n} (any length: chirp-z path), mmax={n // 3}: C2R "
+                         "synthesis then R2C analysis, m-major spectrum")
         elif name == "real":
             self.kind, self.n, self.batch, self.dims, self.shift = "real_rt", 4096, 2048, 1, False
             self.mmax = 1365
@@ -267,10 +274,12 @@ def oracle_step_sample(w, x, budget_s):
     if w.kind == "real_rt":
         per_row_flops = 2 * 2.5 * w.n * w.log2n
 
-        def run(rows):
+        pow2 = (w.n & (w.n - 1)) == 0
+
+        def run(rows):  # the oracle's FFT path, or its direct sums for other lengths
             F = x[:rows]
-            xr = oracle.c2r(F, w.n)
-            oracle.r2c(xr, w.mmax)
+            xr = oracle.c2r(F, w.n) if pow2 else oracle.c2r_direct(F, w.n)
+            oracle.r2c(xr, w.mmax) if pow2 else oracle.r2c_direct(xr, w.mmax)
         unit_rows = w.batch
     elif w.dims == 2:
         per_row_flops = None
