@@ -43,6 +43,7 @@ def _lib():
             "oracle_fft2d": [p, i64, i64, ci, p],
             "oracle_fftshift": [p, i64, i64, ci, p],
             "oracle_chessboard": [p, i64, i64, ci, p],
+            "oracle_roll": [p, i64, i64, i64, i64, i64, p],
             "oracle_r2c": [p, i64, i64, i64, p],
             "oracle_c2r": [p, i64, i64, i64, p],
             "oracle_r2c_direct": [p, i64, i64, i64, p],
@@ -136,6 +137,27 @@ def fftshift(x, dims=1):
     return out
 
 
+def roll(x, shift_x, shift_y=0, dims=1):
+    """Rotate every row (dims=1) or image (dims=2, last two axes ny x nx) by (shift_y, shift_x):
+    out[(y + sy) mod ny][(x + sx) mod nx] = in[y][x]; any extents, odd ones included."""
+    x = _c128(x)
+    nx = x.shape[-1]
+    ny = x.shape[-2] if dims == 2 else 1
+    out = np.empty_like(x)
+    _check(_lib().oracle_roll(_ptr(x), nx, ny, x.size // (nx * ny), int(shift_x), int(shift_y),
+                              _ptr(out)), "roll")
+    return out
+
+
+def fftshift_any(x, dims=1, inverse=False):
+    """fftshift (bin 0 to the middle: rotation by n/2 rounded down per axis) or, with
+    inverse, ifftshift (the rotation back), of every row or ny x nx image."""
+    sgn = -1 if inverse else 1
+    nx = np.shape(x)[-1]
+    ny = np.shape(x)[-2] if dims == 2 else 1
+    return roll(x, sgn * (nx // 2), sgn * (ny // 2) if dims == 2 else 0, dims)
+
+
 def chessboard(x, dims=1):
     """Multiply element-wise by (-1)^j (dims=1) or (-1)^(row+col) (dims=2)."""
     x = _c128(x)
@@ -151,17 +173,22 @@ def transform(x, direction=-1, dims=1, shift=False):
     """What one exec of a C2C plan computes, in fp64.
 
     direction -1: forward; with shift, the output is fftshift(FFT(x)).
-    direction +1: inverse; with shift, the output is (-1)^j * IFFT(x) (chessboard post-multiply).
+    direction +1: inverse; with shift, the output is IFFT(ifftshift(x)) (for even lengths the
+    chessboard (-1)^j post-multiply of IFFT(x)).
     Rows whose length is not a power of two (dims 1) take the direct sum of Mota §2.2 Eq. 5.
     """
     n = np.shape(x)[-1]
-    if dims == 1:
-        y = fft(x, direction) if (n & (n - 1)) == 0 else dft(x, direction)
-    else:
-        y = fft2d(x, direction)
-    if shift:
-        y = fftshift(y, dims) if direction == -1 else chessboard(y, dims)
-    return y
+
+    def t(v):
+        if dims == 1:
+            return fft(v, direction) if (n & (n - 1)) == 0 else dft(v, direction)
+        return fft2d(v, direction)
+
+    if not shift:
+        return t(x)
+    if direction == -1:
+        return fftshift_any(t(x), dims)
+    return t(fftshift_any(x, dims, inverse=True))
 
 
 def to_mmajor(F):

@@ -248,6 +248,28 @@ int oracle_fftshift(const double* x, int64_t n, int64_t batch, int dims, double*
     return 0;
 }
 
+/* ---------------------------------------------------------------------------------------
+ * General rotation, [Shift] "What is fftshift?" and its memory-move variants: every row
+ * (ny == 1) or ny x nx image is rotated by (sy, sx), out[(y + sy) mod ny][(x + sx) mod nx] =
+ * in[y][x], for any extents (odd ones included) and any shifts.  fftshift is the rotation by
+ * (ny/2, nx/2) rounded down, ifftshift the rotation back.
+ * ------------------------------------------------------------------------------------- */
+int oracle_roll(const double* x, int64_t nx, int64_t ny, int64_t batch, int64_t sx, int64_t sy,
+                double* out) {
+    if (!x || !out || x == out || nx < 1 || ny < 1 || batch < 1) return -1;
+    const cplx* xi = (const cplx*)x;
+    cplx* yo = (cplx*)out;
+    sx %= nx;
+    if (sx < 0) sx += nx;
+    sy %= ny;
+    if (sy < 0) sy += ny;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t y = 0; y < ny; ++y)
+            for (int64_t c = 0; c < nx; ++c)
+                yo[(b * ny + (y + sy) % ny) * nx + (c + sx) % nx] = xi[(b * ny + y) * nx + c];
+    return 0;
+}
+
 /* Multiply by the chessboard (-1)^j (dims 1) or (-1)^(row+col) (dims 2), element-wise. */
 int oracle_chessboard(const double* x, int64_t n, int64_t batch, int dims, double* out) {
     if (!x || !out || n < 1 || batch < 1 || (dims != 1 && dims != 2)) return -1;

@@ -202,6 +202,31 @@ def test_direct_band_limited_sums_any_length(n, mmax):
     assert rel(oracle.c2r_direct(G, n), np.fft.irfft(pad, n) * n) < 1e-12
 
 
+@pytest.mark.parametrize("shape", [(3, 7), (2, 8), (2, 5, 6), (1, 9, 4), (2, 8, 8)])
+def test_roll_fftshift_ifftshift_match_numpy(shape):
+    """The general rotation against numpy's fftshift / ifftshift (library routines): odd and
+    even extents, rows and rectangular images."""
+    x = crand(*shape)
+    dims = 2 if len(shape) == 3 else 1
+    axes = (-2, -1) if dims == 2 else (-1,)
+    np.testing.assert_array_equal(oracle.fftshift_any(x, dims), np.fft.fftshift(x, axes=axes))
+    np.testing.assert_array_equal(oracle.fftshift_any(x, dims, inverse=True),
+                                  np.fft.ifftshift(x, axes=axes))
+    np.testing.assert_array_equal(oracle.roll(x, 2, 1 if dims == 2 else 0, dims),
+                                  np.roll(x, (1, 2) if dims == 2 else 2, axis=axes))
+
+
+@pytest.mark.parametrize("n", [7, 9, 1001])
+def test_odd_length_shift_by_complex_exponential(n):
+    """For odd n the shifted transform is the transform of x_j * exp(+2*pi*i*j*(n//2)/n)
+    (forward), and IFFT(ifftshift(X)) is IFFT(X)_j * exp(-2*pi*i*j*(n//2)/n) (inverse)."""
+    x = crand(2, n)
+    e = np.exp(2j * np.pi * np.arange(n) * (n // 2) / n)
+    assert rel(oracle.transform(x, -1, 1, True), oracle.dft(x * e, -1)) < 1e-12
+    assert rel(oracle.transform(x, +1, 1, True), oracle.dft(x, +1) / e) < 1e-12
+    assert rel(oracle.transform(oracle.transform(x, -1, 1, True), +1, 1, True), n * x) < 1e-12
+
+
 def test_chessboard_values():
     x = np.ones((1, 6), complex)
     np.testing.assert_array_equal(oracle.chessboard(x, 1)[0], [1, -1, 1, -1, 1, -1])
