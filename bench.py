@@ -80,6 +80,11 @@ class Workload:
             self.kind, self.n, self.batch, self.dims, self.shift = "c2c_fwd", n, (1 << 26) // n, 1, False
             self.desc = (f"1-D C2C fp32 forward N={n} (not a power of two: chirp-z path) x "
                          f"{(1 << 26) // n} rows (3 tones + noise)")
+        elif name.startswith("shift_"):
+            n = int(name.split("_")[1])
+            self.kind, self.n, self.batch, self.dims, self.shift = "shift", n, (1 << 26) // n, 1, True
+            self.desc = (f"standalone fftshift by index rotation, {(1 << 26) // n} rows x {n} "
+                         "complex64, out of place")
         elif name.startswith("realany_"):
             n = int(name.split("_")[1])
             self.kind, self.n, self.batch, self.dims, self.shift = "real_rt", n, 2048, 1, False
@@ -100,7 +105,10 @@ class Workload:
         n = self.n
         self.points = self.batch * (n * n if self.dims == 2 else n)
         self.log2n = math.log2(n)  # flop count 5*N*log2(N) for any N (CS598 metric)
-        if self.kind == "real_rt":
+        if self.kind == "shift":
+            self.flops = 0.0
+            self.min_bytes = 16 * self.batch * n  # one read + one write per point
+        elif self.kind == "real_rt":
             m1 = self.mmax + 1
             self.flops = 2 * 2.5 * n * self.log2n * self.batch
             # synthesis reads the spectrum and writes reals; analysis the reverse
@@ -271,7 +279,15 @@ def oracle_step_sample(w, x, budget_s):
     import oracle
 
     cores = oracle.num_threads()
-    if w.kind == "real_rt":
+    unit = "GFLOP/s"
+    if w.kind == "shift":  # a rate in bytes moved (16 per point), like the GPU line
+        per_row_flops = 16.0 * w.n
+
+        def run(rows):
+            oracle.fftshift_any(x[:rows], 1)
+        unit_rows = w.batch
+        unit = "GB/s"
+    elif w.kind == "real_rt":
         per_row_flops = 2 * 2.5 * w.n * w.log2n
 
         pow2 = (w.n & (w.n - 1)) == 0
@@ -314,7 +330,7 @@ def oracle_step_sample(w, x, budget_s):
             break
         rows = min(unit_rows, max(rows * 2, int(rows * budget_s / max(dt, 1e-3) * 1.1)))
     gflops = per_row_flops * rows / dt / 1e9
-    return gflops, "GFLOP/s", cores, f"{rows} of {unit_rows} rows of the same workload", dt
+    return gflops, unit, cores, f"{rows} of {unit_rows} rows of the same workload", dt
 
 
 def run_reference(args, w):
@@ -329,14 +345,16 @@ def run_reference(args, w):
         if i >= args.warmup:
             times.append(v)
     value = statistics.median(times)
+    metric = ("fftshift GB/s (16 B per complex point)" if w.kind == "shift"
+              else "fp32 C2C FFT GFLOP/s (5N*log2N/t)")
     line = {
-        "impl": "reference", "metric": "fp32 C2C FFT GFLOP/s (5N*log2N/t)", "value": value,
-        "unit": "GFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "impl": "reference", "metric": metric, "value": value,
+        "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "config": {"workload": w.desc},
-        "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -366,7 +384,16 @@ def main():
     x_host = make_inputs(w, 1 + rank)
 
     with torch.cuda.stream(stream):
-        if w.kind == "real_rt":
+        if w.kind == "shift":
+            xd = torch.from_numpy(x_host).to(dev)
+            yd = torch.empty_like(xd)
+            plans = []
+
+            def launches():
+                fx.shift_ptr(xd.data_ptr(), yd.data_ptr(), w.n, 1, w.batch, 1, False,
+                             stream.cuda_stream)
+                yield
+        elif w.kind == "real_rt":
             syn = fx.Plan(w.n, w.batch, 1, fx.INVERSE, layout=fx.LAYOUT_REAL_MMAJOR, mmax=w.mmax)
             ana = fx.Plan(w.n, w.batch, 1, fx.FORWARD, layout=fx.LAYOUT_REAL_MMAJOR, mmax=w.mmax)
             F = torch.from_numpy(np.ascontiguousarray(x_host.T)).to(dev)  # m-major
@@ -401,7 +428,7 @@ def main():
         d = plan.describe()
         return int(d.split("kernels=")[1].split()[0])
 
-    kper = sum(kernels_of(p) for p in plans)
+    kper = sum(kernels_of(p) for p in plans) if plans else kernels_per_step
 
     def one_step(ev=None):
         if flush is not None:
@@ -449,7 +476,9 @@ def main():
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     dom = max(range(kernels_per_step), key=lambda i: launch_ms[i])
-    if w.kind == "real_rt":
+    if w.kind == "shift":
+        dom_bytes, dom_kernels = w.min_bytes, 1
+    elif w.kind == "real_rt":
         dom_bytes = (w.batch * (w.mmax + 1) * 8 + w.batch * w.n * 4)
         dom_kernels = 1
     else:
@@ -461,8 +490,9 @@ def main():
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peak_src,
-                "kernel": plans[min(dom, len(plans) - 1)].describe().split(" ")[0] +
-                          (f" ({dom_kernels} kernels)" if dom_kernels > 1 else ""),
+                "kernel": ("fft_shift" if not plans else
+                           plans[min(dom, len(plans) - 1)].describe().split(" ")[0] +
+                           (f" ({dom_kernels} kernels)" if dom_kernels > 1 else "")),
                 "launch_ms": round(launch_ms[dom], 4),
                 "algorithmic_bytes_per_launch": dom_bytes}
 
@@ -471,7 +501,7 @@ def main():
     # host-to-device copy, the library's transforms, one device-to-host copy, on three streams
     # with two device buffers per stage, so copies of one chunk overlap compute of another.
     e2e = None
-    if not args.no_e2e and w.kind != "real_rt" and w.dims == 1:
+    if not args.no_e2e and w.kind not in ("real_rt", "shift") and w.dims == 1:
         nchunk = 8 if w.batch % 8 == 0 else 1
         rows_c = w.batch // nchunk
         xh = torch.from_numpy(x_host).pin_memory()
@@ -536,9 +566,12 @@ def main():
                "sample": sample, "seconds": round(dt, 2)}
 
     if rank == 0:
+        metric, value, unit = "fp32 C2C FFT GFLOP/s (5N*log2N/t)", round(gflops, 1), "GFLOP/s"
+        if w.kind == "shift":  # pure data movement: the rate is bytes, not flops
+            metric, value, unit = "fftshift GB/s (16 B per complex point)", round(gbs_min, 1), "GB/s"
         line = {
-            "metric": "fp32 C2C FFT GFLOP/s (5N*log2N/t)",
-            "value": round(gflops, 1), "unit": "GFLOP/s", "n_gpus": world,
+            "metric": metric,
+            "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded numpy generators)",

@@ -33,7 +33,7 @@ ABI_SYMBOLS = (
     "fft_plan_create", "fft_plan_set_band_limit", "fft_plan_workspace_bytes",
     "fft_plan_describe", "fft_plan_query", "fft_exec_c2c", "fft_exec_r2c", "fft_exec_c2r",
     "fft_plan_check", "fft_plan_destroy", "fft_status_string", "fft_version",
-    "fft_exec_c2c_noalloc", "fft_plan_set_wait_timeout",
+    "fft_exec_c2c_noalloc", "fft_plan_set_wait_timeout", "fft_shift",
 )
 
 _LIB = None
@@ -61,6 +61,7 @@ def lib():
         L.fft_plan_describe.argtypes = [vp, ctypes.c_char_p, sz]
         L.fft_plan_query.argtypes = [i64, i64, ci, ci, ci, ci, ctypes.c_char_p, sz]
         L.fft_exec_c2c.argtypes = [vp, vp, vp, vp]
+        L.fft_shift.argtypes = [vp, vp, i64, i64, i64, ci, ci, vp]
         L.fft_exec_r2c.argtypes = [vp, vp, vp, vp]
         L.fft_exec_c2r.argtypes = [vp, vp, vp, vp]
         L.fft_plan_check.argtypes = [vp]
@@ -92,6 +93,32 @@ def query(n, batch, dims=1, direction=FORWARD, layout=LAYOUT_C2C, shift=False) -
     _check(lib().fft_plan_query(int(n), int(batch), int(dims), int(direction), int(layout),
                                 int(bool(shift)), buf, len(buf)), "fft_plan_query")
     return buf.value.decode()
+
+
+def shift_ptr(in_ptr, out_ptr, nx, ny=1, batch=1, dims=1, inverse=False, stream_ptr=0):
+    """fftshift (or ifftshift) of raw device buffers by index rotation (fft_shift)."""
+    _check(lib().fft_shift(ctypes.c_void_p(in_ptr), ctypes.c_void_p(out_ptr), int(nx), int(ny),
+                           int(batch), int(dims), int(bool(inverse)), ctypes.c_void_p(stream_ptr)),
+           "fft_shift")
+
+
+def shift(x, dims=1, inverse=False, out=None, stream=None):
+    """fftshift / ifftshift of a complex64 CUDA tensor: the last axis (dims=1) or the last two
+    axes (dims=2) of every row or image rotate by half their extent (rounded down); out=x runs
+    in place (even extents only)."""
+    import torch
+
+    if x.dtype != torch.complex64 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("shift: expected a contiguous complex64 CUDA tensor")
+    nx = x.shape[-1]
+    ny = x.shape[-2] if dims == 2 else 1
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.dtype != torch.complex64 or out.shape != x.shape or not out.is_contiguous():
+        raise TypeError("shift: out must match x")
+    shift_ptr(x.data_ptr(), out.data_ptr(), nx, ny, x.numel() // (nx * ny), dims, inverse,
+              _stream_ptr(stream).value or 0)
+    return out
 
 
 def exec_c2c_noalloc(n, batch, direction, shift, in_ptr, out_ptr, stream_ptr=0):

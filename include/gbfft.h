@@ -208,6 +208,29 @@ int fft_plan_destroy(fft_plan plan);
 int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int shift, const void* in,
                          void* out, void* stream);
 
+/*
+ * fft_shift - standalone fftshift / ifftshift by index rotation (the memory-move variants of
+ * "The 1D fftshift in CUDA by chessboard multiplication", "What is fftshift?"): moves bin 0 to
+ * the middle of every row or image, or (inverse) back.
+ *   in, out   DEVICE pointers to batch complex64 arrays, 8-byte aligned (16-byte alignment
+ *             enables 16-byte accesses); owned by the caller.  in == out (in place) is allowed
+ *             when every rotated extent is even (nx for dims 1; nx and ny for dims 2): the
+ *             rotation by half is then a swap and fftshift equals ifftshift.  Any other
+ *             overlap is an error.
+ *   nx, ny    row length; dims 1 requires ny == 1, dims 2 takes ny x nx row-major images
+ *             (rectangular allowed).  Any extents >= 1, odd ones included.
+ *   dims      1 (rows) or 2 (images: both axes rotate).
+ *   inverse   0: fftshift, out[(y + ny/2) mod ny][(x + nx/2) mod nx] = in[y][x] (halves
+ *             rounded down, numpy's convention); 1: ifftshift, the rotation back.
+ *   stream    cudaStream_t; asynchronous, no host synchronisation.
+ * The transform plans fold the same shift into their loads and stores (the chessboard for even
+ * lengths); this call is for data that are already transformed.
+ * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_UNSUPPORTED_SIZE, FFT_ERR_MISALIGNED or
+ * FFT_ERR_CUDA.
+ */
+int fft_shift(const void* in, void* out, int64_t nx, int64_t ny, int64_t batch, int dims,
+              int inverse, void* stream);
+
 /* fft_status_string - static description of a status code (never NULL). */
 const char* fft_status_string(int status);
 

@@ -134,3 +134,17 @@ def test_2d_and_real_paths():
     assert "path=2d" in fx.query(4096, 1, dims=2, shift=True)
     d = fx.query(4096, 2048, layout=2, direction=1)
     assert "path=real" in d and "core=2048" in d and "mmajor" in d
+
+
+def test_shift_argument_errors_before_touching_the_device():
+    L = fx.lib()
+    p = ctypes.c_void_p
+    assert L.fft_shift(None, p(4096), 4, 1, 1, 1, 0, None) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_shift(p(4096), p(4096), 5, 1, 1, 1, 0, None) == fx.FFT_ERR_INVALID_ARG  # odd in place
+    assert L.fft_shift(p(4096), p(4096), 4, 3, 1, 2, 0, None) == fx.FFT_ERR_INVALID_ARG  # odd ny in place
+    assert L.fft_shift(p(4096), p(1 << 20), 4, 2, 1, 1, 0, None) == fx.FFT_ERR_INVALID_ARG  # dims 1, ny != 1
+    assert L.fft_shift(p(4096), p(4104), 4, 1, 1, 1, 0, None) == fx.FFT_ERR_INVALID_ARG  # overlap
+    assert L.fft_shift(p(4096), p(1 << 20), 4, 1, 1, 3, 0, None) == fx.FFT_ERR_INVALID_ARG  # dims
+    assert L.fft_shift(p(4096), p(1 << 20), 4, 1, 1, 1, 2, None) == fx.FFT_ERR_INVALID_ARG  # inverse
+    assert L.fft_shift(p(4100), p(1 << 20), 4, 1, 1, 1, 0, None) == fx.FFT_ERR_MISALIGNED
+    assert L.fft_shift(p(4096), p(1 << 20), 1 << 40, 2, 1, 2, 0, None) == fx.FFT_ERR_UNSUPPORTED_SIZE
