@@ -17,35 +17,33 @@ namespace {
 
 constexpr int kShiftThreads = 256;
 
-// Out of place: one warp per output row, lanes along the row.  Output (b, y, x) reads input
+// Out of place, one thread per output point (or pair of points) over the whole batch, so the
+// work is spread evenly whatever the row length.  Output (b, y, x) reads input
 // (b, (y - sy) mod ny, (x - sx) mod nx); with PAIRS two neighbouring points move as one 16-byte
-// access (nx and sx even, both buffers 16-byte aligned).
-template <bool PAIRS>
+// access (nx and sx even, both buffers 16-byte aligned); with POW2 (nx a power of two) the row
+// and column come from a shift and a mask instead of a division.
+template <bool PAIRS, bool POW2>
 __global__ void __launch_bounds__(kShiftThreads)
     k_roll(const float2* __restrict__ in, float2* __restrict__ out, int64_t nx, int64_t ny,
-           int64_t rows, int64_t sx, int64_t sy) {
-    const int lane = (int)threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * kShiftThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kShiftThreads) >> 5;
-    for (int64_t r = warp; r < rows; r += nwarps) {
-        const int64_t b = r / ny, y = r - b * ny;
-        const int64_t ys = y >= sy ? y - sy : y - sy + ny;
-        const float2* src = in + (b * ny + ys) * nx;
-        float2* dst = out + r * nx;
-        if constexpr (PAIRS) {
+           int64_t units, int64_t sx, int64_t sy, int log2nx) {
+    constexpr int P = PAIRS ? 2 : 1;
+    const int64_t stride = (int64_t)gridDim.x * kShiftThreads;
 #pragma unroll 4
-            for (int64_t x = 2 * lane; x < nx; x += 64) {
-                const int64_t xs = x >= sx ? x - sx : x - sx + nx;
-                stg_stream4(reinterpret_cast<float4*>(dst + x),
-                            ldg_stream4(reinterpret_cast<const float4*>(src + xs)));
-            }
-        } else {
-#pragma unroll 4
-            for (int64_t x = lane; x < nx; x += 32) {
-                const int64_t xs = x >= sx ? x - sx : x - sx + nx;
-                stg_stream(dst + x, ldg_stream(src + xs));
-            }
+    for (int64_t u = (int64_t)blockIdx.x * kShiftThreads + threadIdx.x; u < units; u += stride) {
+        const int64_t i = u * P;
+        const int64_t row = POW2 ? i >> log2nx : i / nx;
+        const int64_t x = POW2 ? i & (nx - 1) : i - row * nx;
+        int64_t srow = row;
+        if (ny > 1) {
+            const int64_t b = row / ny, y = row - b * ny;
+            srow = b * ny + (y >= sy ? y - sy : y - sy + ny);
         }
+        const int64_t src = srow * nx + (x >= sx ? x - sx : x - sx + nx);
+        if constexpr (PAIRS)
+            stg_stream4(reinterpret_cast<float4*>(out + i),
+                        ldg_stream4(reinterpret_cast<const float4*>(in + src)));
+        else
+            stg_stream(out + i, ldg_stream(in + src));
     }
 }
 
@@ -146,15 +144,17 @@ extern "C" int fft_shift(const void* in, void* out, int64_t nx, int64_t ny, int6
             sx = (nx - sx) % nx;
             sy = (ny - sy) % ny;
         }
-        const int64_t rows = batch * ny;
         const bool pairs = (nx % 2 == 0) && (sx % 2 == 0) && aligned(in, 16) && aligned(out, 16);
-        const unsigned grid = grid_for(rows);
-        if (pairs)
-            k_roll<true><<<grid, kShiftThreads, 0, st>>>((const float2*)in, (float2*)out, nx, ny,
-                                                          rows, sx, sy);
-        else
-            k_roll<false><<<grid, kShiftThreads, 0, st>>>((const float2*)in, (float2*)out, nx,
-                                                           ny, rows, sx, sy);
+        const bool pow2 = (nx & (nx - 1)) == 0;
+        int log2nx = 0;
+        while ((INT64_C(1) << log2nx) < nx) ++log2nx;
+        const int64_t units = pairs ? points / 2 : points;
+        const unsigned grid = grid_for((units + 31) / 32);
+        const float2* x = (const float2*)in;
+        float2* y = (float2*)out;
+        auto kern = pairs ? (pow2 ? k_roll<true, true> : k_roll<true, false>)
+                          : (pow2 ? k_roll<false, true> : k_roll<false, false>);
+        kern<<<grid, kShiftThreads, 0, st>>>(x, y, nx, ny, units, sx, sy, log2nx);
         e = cudaGetLastError();
     }
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
