@@ -74,7 +74,7 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     // lengths that are not powers of two: complex rows up to kMaxBluesteinN only
     const bool any_length = l < 0 && dims == 1 && n >= 3 && n <= kMaxBluesteinN;
     if (l < 0 && !any_length) return FFT_ERR_UNSUPPORTED_SIZE;
-    if (shift && (n & 1)) return FFT_ERR_INVALID_ARG;
+    if (shift && (n & 1) && !any_length) return FFT_ERR_INVALID_ARG;
     PlanSpec s;
     s.n = n;
     s.batch = batch;
@@ -269,7 +269,8 @@ struct gbfft_plan_s {
     int device = 0;
     float2* d_tw = nullptr;
     size_t tw_count = 0;
-    size_t off_a = 0, off_b = 0, off_hi = 0, off_lo = 0, off_r = 0, off_chirp = 0, off_bhat = 0;
+    size_t off_a = 0, off_b = 0, off_hi = 0, off_lo = 0, off_r = 0;
+    size_t off_chirp = 0, off_chirp_out = 0, off_bhat = 0;  // chirp-z tables
     void* d_work = nullptr;
     size_t work_bytes = 0;
     int* d_err = nullptr;
@@ -351,7 +352,15 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
         }
         case PATH_BLUESTEIN:
             p->off_a = append_pass_tables(tw, s.log2m, rows_maxrb(s.log2m));
-            p->off_chirp = host::append_chirp(tw, s.n, s.direction);
+            {
+                // fftshift folded in: exp(+2 pi i j h/n) on the forward load, exp(-2 pi i k h/n)
+                // on the inverse store, h = n/2 rounded down
+                const int64_t h = s.n / 2;
+                const bool fwd = s.direction == FFT_FORWARD;
+                p->off_chirp = host::append_chirp(tw, s.n, s.direction, s.shift && fwd ? h : 0);
+                p->off_chirp_out = s.shift ? host::append_chirp(tw, s.n, s.direction, fwd ? 0 : -h)
+                                           : p->off_chirp;
+            }
             p->off_bhat = host::append_chirp_filter(tw, s.n, int64_t(1) << s.log2m, s.direction);
             break;
         case PATH_REAL:
@@ -423,10 +432,10 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                          p->d_err, p->wait_limit_ns, st);
             break;
         }
-        case PATH_BLUESTEIN: {
-            const int flags = s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0;
+        case PATH_BLUESTEIN: {  // the shift lives in the chirp tables
             e = run_bluestein(s.log2m, 0, x, y, s.batch, (int)s.n, 0, 0, p->d_tw + p->off_chirp,
-                              p->d_tw + p->off_bhat, p->d_tw + p->off_a, flags, st);
+                              p->d_tw + p->off_chirp_out, p->d_tw + p->off_bhat,
+                              p->d_tw + p->off_a, st);
             break;
         }
         case PATH_FOURSTEP: {
@@ -470,8 +479,8 @@ int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
     cudaError_t e =
         s.path == PATH_BLUESTEIN
             ? run_bluestein(s.log2m, 1, in, out, s.batch, (int)s.n, (int)p->mmax, mmajor,
-                            p->d_tw + p->off_chirp, p->d_tw + p->off_bhat, p->d_tw + p->off_a,
-                            0, (cudaStream_t)stream)
+                            p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
+                            p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream)
             : run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax, mmajor,
                       p->d_tw + p->off_a, p->d_tw + p->off_r, p->d_err, (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
@@ -489,8 +498,8 @@ int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
     cudaError_t e =
         s.path == PATH_BLUESTEIN
             ? run_bluestein(s.log2m, 2, in, out, s.batch, (int)s.n, (int)p->mmax, mmajor,
-                            p->d_tw + p->off_chirp, p->d_tw + p->off_bhat, p->d_tw + p->off_a,
-                            0, (cudaStream_t)stream)
+                            p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
+                            p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream)
             : run_c2r(s.log2n - 1, (const float2*)in, out, s.batch, (int)p->mmax, mmajor,
                       p->d_tw + p->off_a, p->d_tw + p->off_r, p->d_err, p->wait_limit_ns,
                       (cudaStream_t)stream);

@@ -12,9 +12,11 @@
 //   4. reorders through shared memory into the first pass's order when the first and last
 //      radices differ, and runs the inverse m-point passes,
 //   5. stores c_k * conv_k for k < n.
-// The chessboard shift (even n) is fused as everywhere else: (-1)^j on the forward load,
-// (-1)^k on the inverse store.  Rows start at any 8-byte boundary, so the loads and stores are
-// plain coalesced per-element accesses rather than bulk copies.
+// The fftshift is folded into the chirp tables, for odd n as well: the forward transform reads
+// with c_j * exp(+2*pi*i*j*h/n), the inverse stores with c_k * exp(-2*pi*i*k*h/n), h = n/2
+// rounded down (for even n these factors are the chessboard (-1)^j).  Rows start at any
+// 8-byte boundary, so the loads and stores are plain coalesced per-element accesses rather
+// than bulk copies.
 //
 // The same kernel serves band-limited real rows of any length (the direct-sum 'dft' mode of
 // "src/sht/wgsl/fourier.ts", dftAnalysWGSL / dftSynthWGSL, for lengths the power-of-two path
@@ -33,8 +35,8 @@ enum : int { BLU_C2C = 0, BLU_R2C = 1, BLU_C2R = 2 };
 template <class C, int MODE>
 __global__ void __launch_bounds__(C::THREADS)
     k_bluestein(const void* in_, void* out_, int64_t nrows, int n, int mmax, int mmajor,
-                const float2* __restrict__ chirp, const float2* __restrict__ bhat,
-                const float2* __restrict__ tw, int flags) {
+                const float2* __restrict__ chirp, const float2* __restrict__ chirp_out,
+                const float2* __restrict__ bhat, const float2* __restrict__ tw) {
     static_assert(C::TFAST, "a row's threads are adjacent lanes (coalesced row accesses)");
     extern __shared__ float2 smem[];
     const int w = (int)threadIdx.x / C::T;
@@ -74,10 +76,7 @@ __global__ void __launch_bounds__(C::THREADS)
         for (int r = 0; r < R0; ++r) {
             const int e = j + r * S0;
             float2 a = make_float2(0.f, 0.f);
-            if (active && e < n) {
-                a = cmul(load(e), __ldg(chirp + e));
-                if (flags & KF_CHESS_LOAD) a = neg_if(a, e & 1);
-            }
+            if (active && e < n) a = cmul(load(e), __ldg(chirp + e));
             v[b * R0 + r] = a;
         }
     }
@@ -125,9 +124,8 @@ __global__ void __launch_bounds__(C::THREADS)
             for (int r = 0; r < RL; ++r) {
                 const int k = j + r * SL;
                 if (k < kend) {
-                    float2 y = cmul(v[b * RL + r], __ldg(chirp + k));
+                    const float2 y = cmul(v[b * RL + r], __ldg(chirp_out + k));
                     if constexpr (MODE == BLU_C2C) {
-                        if (flags & KF_CHESS_STORE) y = neg_if(y, k & 1);
                         stg_stream(static_cast<float2*>(out_) + row * n + k, y);
                     } else if constexpr (MODE == BLU_R2C) {
                         stg_stream(static_cast<float2*>(out_) +
@@ -144,8 +142,8 @@ __global__ void __launch_bounds__(C::THREADS)
 
 template <class C, int MODE>
 cudaError_t launch_bluestein(const void* in, void* out, int64_t nrows, int n, int mmax,
-                             int mmajor, const float2* chirp, const float2* bhat,
-                             const float2* tw, int flags, cudaStream_t stream) {
+                             int mmajor, const float2* chirp, const float2* chirp_out,
+                             const float2* bhat, const float2* tw, cudaStream_t stream) {
     auto kern = k_bluestein<C, MODE>;
     static int configured_dev = -1;
     int dev = 0;
@@ -163,7 +161,7 @@ cudaError_t launch_bluestein(const void* in, void* out, int64_t nrows, int n, in
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(in, out, nrows, n, mmax, mmajor,
-                                                                  chirp, bhat, tw, flags);
+                                                                  chirp, chirp_out, bhat, tw);
     return cudaGetLastError();
 }
 

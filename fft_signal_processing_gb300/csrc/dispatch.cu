@@ -60,13 +60,13 @@ cudaError_t run_rows_t(int log2n, int dir, const float2* in, float2* out, int64_
 }
 
 cudaError_t run_bluestein(int log2m, int mode, const void* in, void* out, int64_t nrows, int n,
-                          int mmax, int mmajor, const float2* chirp, const float2* bhat,
-                          const float2* tw, int flags, cudaStream_t s) {
+                          int mmax, int mmajor, const float2* chirp, const float2* chirp_out,
+                          const float2* bhat, const float2* tw, cudaStream_t s) {
     switch (log2m) {
 #define GBFFT_C(L)                                                                          \
     case L:                                                                                 \
-        return bluestein_entry_##L(mode, in, out, nrows, n, mmax, mmajor, chirp, bhat, tw,  \
-                                   flags, s);
+        return bluestein_entry_##L(mode, in, out, nrows, n, mmax, mmajor, chirp, chirp_out, \
+                                   bhat, tw, s);
         GBFFT_BLUESTEIN_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;

@@ -115,13 +115,19 @@ inline void fft_fp64(std::vector<std::complex<double>>& a, int sign) {
     }
 }
 
-// c_j for j < n; returns the offset.
-inline size_t append_chirp(std::vector<float2>& v, int64_t n, int sign) {
+// c_j * exp(2*pi*i*j*q/n) for j < n (q = 0: the plain chirp; q = +-floor(n/2): the chirp with
+// the fftshift folded in, see append_chirp's callers); the two angles are reduced in integers
+// and added in double precision before one cos/sin.  Returns the offset.
+inline size_t append_chirp(std::vector<float2>& v, int64_t n, int sign, int64_t q = 0) {
+    const double pi = 3.141592653589793238462643383279502884;
     align_table(v);
     const size_t off = v.size();
     for (int64_t j = 0; j < n; ++j) {
-        const std::complex<double> c = chirp(j, n, sign);
-        v.push_back(make_float2((float)c.real(), (float)c.imag()));
+        const int64_t a = (int64_t)(((unsigned __int128)j * (uint64_t)j) % (uint64_t)(2 * n));
+        int64_t b = (int64_t)(((__int128)j * q) % n);
+        if (b < 0) b += n;
+        const double th = (double)sign * pi * (double)a / (double)n + 2.0 * pi * (double)b / (double)n;
+        v.push_back(make_float2((float)std::cos(th), (float)std::sin(th)));
     }
     return off;
 }

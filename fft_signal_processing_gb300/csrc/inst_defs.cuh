@@ -124,19 +124,19 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
 #define GBFFT_DEF_BLUESTEIN(L)                                                                 \
     cudaError_t gbfft::bluestein_entry_##L(int mode, const void* in, void* out, int64_t nrows,  \
                                            int n, int mmax, int mmajor, const float2* chirp,    \
-                                           const float2* bhat, const float2* tw, int flags,     \
-                                           cudaStream_t s) {                                    \
+                                           const float2* chirp_out, const float2* bhat,         \
+                                           const float2* tw, cudaStream_t s) {                  \
         using C = FftCfg<L, rows_maxrb(L), rows_log2w(L), true>;                               \
         switch (mode) {                                                                        \
             case BLU_C2C:                                                                      \
                 return launch_bluestein<C, BLU_C2C>(in, out, nrows, n, mmax, mmajor, chirp,    \
-                                                    bhat, tw, flags, s);                       \
+                                                    chirp_out, bhat, tw, s);                   \
             case BLU_R2C:                                                                      \
                 return launch_bluestein<C, BLU_R2C>(in, out, nrows, n, mmax, mmajor, chirp,    \
-                                                    bhat, tw, flags, s);                       \
+                                                    chirp_out, bhat, tw, s);                   \
             case BLU_C2R:                                                                      \
                 return launch_bluestein<C, BLU_C2R>(in, out, nrows, n, mmax, mmajor, chirp,    \
-                                                    bhat, tw, flags, s);                       \
+                                                    chirp_out, bhat, tw, s);                   \
             default: return cudaErrorInvalidValue;                                             \
         }                                                                                      \
     }

@@ -31,8 +31,8 @@ namespace gbfft {
 #define GBFFT_X_BLUESTEIN(L)                                                               \
     cudaError_t bluestein_entry_##L(int mode, const void* in, void* out, int64_t nrows,      \
                                     int n, int mmax, int mmajor, const float2* chirp,       \
-                                    const float2* bhat, const float2* tw, int flags,        \
-                                    cudaStream_t s);
+                                    const float2* chirp_out, const float2* bhat,            \
+                                    const float2* tw, cudaStream_t s);
 
 #define GBFFT_ROWS_SIZES(X) X(0) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14)
 #define GBFFT_COLS_SIZES(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12)

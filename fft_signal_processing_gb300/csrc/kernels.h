@@ -104,11 +104,12 @@ __host__ __device__ constexpr int rowst_maxrb(int l) { return l >= 9 ? 6 : 4; }
 
 // Rows of any length n that is not a power of two (chirp-z transform through m = 2^log2m
 // points, m >= 2n - 1): chirp[j] = c_j (n entries), bhat = FFT_m(conj c)/m (m entries), tw the
-// m-point pass tables.  mode 0: complex rows (flags KF_CHESS_LOAD / KF_CHESS_STORE, even n);
-// 1: real rows -> spectrum m <= mmax (row-major, or m-major if mmajor); 2: spectrum -> real rows.
+// m-point pass tables; chirp multiplies the loads and chirp_out the stores (they differ when a
+// shift is folded in).  mode 0: complex rows; 1: real rows -> spectrum m <= mmax (row-major,
+// or m-major if mmajor); 2: spectrum -> real rows.
 cudaError_t run_bluestein(int log2m, int mode, const void* in, void* out, int64_t nrows, int n,
-                          int mmax, int mmajor, const float2* chirp, const float2* bhat,
-                          const float2* tw, int flags, cudaStream_t s);
+                          int mmax, int mmajor, const float2* chirp, const float2* chirp_out,
+                          const float2* bhat, const float2* tw, cudaStream_t s);
 constexpr int kMaxBluesteinN = 8192;  // 2n - 1 <= 2^14: one pass, the m-point row in one CTA
 __host__ __device__ constexpr int bluestein_log2m(int64_t n) {
     int l = 0;

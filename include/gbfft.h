@@ -82,11 +82,15 @@ enum {
  *   direction FFT_FORWARD or FFT_INVERSE.  Real layouts: FORWARD = analysis (R2C, exec with
  *             fft_exec_r2c), INVERSE = synthesis (C2R, exec with fft_exec_c2r).
  *   layout    FFT_LAYOUT_*.
- *   shift     0 or 1; C2C only, n even.  Forward: the input is pre-multiplied by the chessboard
- *             (-1)^j (dims 1) or (-1)^(row+col) (dims 2), which for even n makes the output
- *             fftshift(X) ("The 1D fftshift in CUDA by chessboard multiplication", the
- *             chessboard section).  Inverse: the output is post-multiplied by the same
- *             chessboard, so inverse-shift(forward-shift(x)) = n*x (dims 1) or n^2*x (dims 2).
+ *   shift     0 or 1; C2C only; n even, or any length that is not a power of two.  Forward:
+ *             the input is pre-multiplied by the chessboard (-1)^j (dims 1) or (-1)^(row+col)
+ *             (dims 2), which for even n makes the output fftshift(X) ("The 1D fftshift in
+ *             CUDA by chessboard multiplication", the chessboard section).  Inverse: the output
+ *             is post-multiplied by the same chessboard, i.e. it is IFFT(ifftshift(X)), so
+ *             inverse-shift(forward-shift(x)) = n*x (dims 1) or n^2*x (dims 2).  For odd n
+ *             (chirp-z path) the factors are exp(+2*pi*i*j*h/n) on the forward load and
+ *             exp(-2*pi*i*k*h/n) on the inverse store, h = (n-1)/2, with the same meaning
+ *             (fftshift moves bin 0 to index h); they are folded into the chirp tables.
  *   out       receives the plan.
  * The plan allocates its device twiddle tables, its workspace (large 1-D sizes only) and a
  * device error word with cudaMalloc on the current device, and copies the tables (computed on

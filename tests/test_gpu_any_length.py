@@ -66,13 +66,18 @@ def test_any_length_grid(n, direction):
     assert_parity(got, oracle.transform(x, direction), n, f"n={n} dir={direction}")
 
 
-@pytest.mark.parametrize("n", [6, 100, 1000, 4098, 8190])
+@pytest.mark.parametrize("n", [3, 6, 7, 100, 1000, 1001, 4098, 4099, 8190, 8191])
 @pytest.mark.parametrize("direction", [-1, 1])
 def test_any_length_shift_in_place(n, direction):
+    """Even lengths: the chessboard; odd lengths: the complex exponentials, both folded into
+    the chirp tables; against fftshift(DFT(x)) and IFFT(ifftshift(X)) of the oracle."""
     batch = 5
     x = wl().uniform(7100 + n, batch, n)
     got = gpu_c2c(x, n, batch, direction, shift=True, inplace=True)
     assert_parity(got, oracle.transform(x, direction, 1, True), n, f"shift n={n}")
+    if direction == -1:  # bin 0 lands at index n//2
+        y = gpu_c2c(np.ones((1, n), np.complex64), n, 1, -1, shift=True)
+        assert np.argmax(np.abs(y[0])) == n // 2
 
 
 @pytest.mark.parametrize("n", [3, 1000, 8191])
