@@ -15,7 +15,8 @@ Conventions (readings of the pages):
   ("The 1D fftshift in CUDA by chessboard multiplication", "What is fftshift?");
   inverse with shift = inverse transform, then multiply by the chessboard (-1)^j.
 * ``r2c`` / ``c2r``: band-limited real analysis / synthesis of fourier.ts (header comment,
-  fftAnalysWGSL / fftSynthWGSL), 0 <= mmax < N/2, spectra row-major [rows][mmax+1] or
+  fftAnalysWGSL / fftSynthWGSL), 0 <= 2*mmax <= N (mmax = N/2 adds the real Nyquist bin,
+  counted once in the synthesis), spectra row-major [rows][mmax+1] or
   m-major [mmax+1][rows] (fourier.ts stores fm[m*NLAT + ilat]).
 """
 import ctypes

@@ -297,10 +297,13 @@ int oracle_chessboard(const double* x, int64_t n, int64_t batch, int dims, doubl
  * Synthesis (C2R): assemble the Hermitian spectrum X_0 = Re F_0, X_m = F_m,
  *   X_{N-m} = conj F_m (1 <= m <= mmax), all other bins zero; x = Re(inverse FFT of X).
  *   Im F_0 is ignored, as the page reads only the real part of F_0.
- * Both require 0 <= mmax < N/2. Spectra here are row-major [batch][mmax+1].
+ * Both take 0 <= mmax <= N/2.  The pages stop below N/2; at mmax = N/2 (even N) the Nyquist
+ * bin is its own mirror (X_{N-N/2} = X_{N/2}), so Hermitian symmetry makes it real: the
+ * synthesis uses Re F_{N/2} once (no conjugate partner) and ignores its imaginary part, as for
+ * F_0.  Spectra here are row-major [batch][mmax+1].
  * ------------------------------------------------------------------------------------- */
 int oracle_r2c(const double* xr, int64_t n, int64_t batch, int64_t mmax, double* F) {
-    if (!xr || !F || !is_pow2(n) || n < 2 || batch < 1 || mmax < 0 || mmax >= n / 2) return -1;
+    if (!xr || !F || !is_pow2(n) || n < 2 || batch < 1 || mmax < 0 || 2 * mmax > n) return -1;
     cplx* roots = make_roots(-1, n);
     if (!roots) return -1;
     int failed = 0;
@@ -330,7 +333,7 @@ int oracle_r2c(const double* xr, int64_t n, int64_t batch, int64_t mmax, double*
 }
 
 int oracle_c2r(const double* F, int64_t n, int64_t batch, int64_t mmax, double* xr) {
-    if (!F || !xr || !is_pow2(n) || n < 2 || batch < 1 || mmax < 0 || mmax >= n / 2) return -1;
+    if (!F || !xr || !is_pow2(n) || n < 2 || batch < 1 || mmax < 0 || 2 * mmax > n) return -1;
     cplx* roots = make_roots(+1, n);
     if (!roots) return -1;
     int failed = 0;
@@ -348,6 +351,11 @@ int oracle_c2r(const double* F, int64_t n, int64_t batch, int64_t mmax, double* 
                 memset(spec, 0, sizeof(cplx) * (size_t)n);
                 spec[0].re = f[0].re; /* X_0 = Re F_0 */
                 for (int64_t m = 1; m <= mmax; ++m) {
+                    if (2 * m == n) {          /* Nyquist: real, its own mirror */
+                        spec[m].re = f[m].re;
+                        spec[m].im = 0.0;
+                        continue;
+                    }
                     spec[m] = f[m];            /* X_m = F_m */
                     spec[n - m].re = f[m].re;  /* X_{N-m} = conj F_m */
                     spec[n - m].im = -f[m].im;
@@ -365,10 +373,11 @@ int oracle_c2r(const double* F, int64_t n, int64_t batch, int64_t mmax, double* 
 
 /* Direct band-limited sums, [SHT] dftAnalysWGSL / dftSynthWGSL:
  *   F_m = sum_j x_j exp(-2*pi*i*m*j/N)
- *   x_j = Re F_0 + 2 * sum_{m=1}^{mmax} Re(F_m exp(+2*pi*i*m*j/N)).
- * O(N * mmax) per row; any N >= 2 with mmax < N/2. */
+ *   x_j = Re F_0 + 2 * sum_{m=1}^{mmax} Re(F_m exp(+2*pi*i*m*j/N)),
+ * with the term of a Nyquist bin m = N/2 counted once, as Re F_{N/2} (-1)^j.
+ * O(N * mmax) per row; any N >= 2 with 0 <= 2*mmax <= N. */
 int oracle_r2c_direct(const double* xr, int64_t n, int64_t batch, int64_t mmax, double* F) {
-    if (!xr || !F || n < 2 || batch < 1 || mmax < 0 || 2 * mmax >= n) return -1;
+    if (!xr || !F || n < 2 || batch < 1 || mmax < 0 || 2 * mmax > n) return -1;
 #pragma omp parallel for schedule(dynamic)
     for (int64_t b = 0; b < batch; ++b) {
         for (int64_t m = 0; m <= mmax; ++m) {
@@ -386,13 +395,17 @@ int oracle_r2c_direct(const double* xr, int64_t n, int64_t batch, int64_t mmax, 
 }
 
 int oracle_c2r_direct(const double* F, int64_t n, int64_t batch, int64_t mmax, double* xr) {
-    if (!F || !xr || n < 2 || batch < 1 || mmax < 0 || 2 * mmax >= n) return -1;
+    if (!F || !xr || n < 2 || batch < 1 || mmax < 0 || 2 * mmax > n) return -1;
 #pragma omp parallel for schedule(dynamic)
     for (int64_t b = 0; b < batch; ++b) {
         const cplx* f = (const cplx*)F + b * (mmax + 1);
         for (int64_t j = 0; j < n; ++j) {
             double s = f[0].re;
             for (int64_t m = 1; m <= mmax; ++m) {
+                if (2 * m == n) {  /* Nyquist: Re F_{N/2} (-1)^j, once */
+                    s += (j & 1) ? -f[m].re : f[m].re;
+                    continue;
+                }
                 cplx w = unit_root(+1, (int64_t)(((__int128)m * j) % n), n);
                 s += 2.0 * (f[m].re * w.re - f[m].im * w.im);
             }

@@ -227,6 +227,27 @@ def test_odd_length_shift_by_complex_exponential(n):
     assert rel(oracle.transform(oracle.transform(x, -1, 1, True), +1, 1, True), n * x) < 1e-12
 
 
+@pytest.mark.parametrize("n", [8, 12, 1024])
+def test_nyquist_bin_full_half_spectrum(n):
+    """mmax = n/2: the full n/2 + 1 half spectrum against numpy's rfft / irfft (library
+    routines; irfft also drops the imaginary parts of bins 0 and n/2), both oracle paths."""
+    rng = np.random.default_rng(n)
+    x = rng.standard_normal((3, n))
+    h = n // 2
+    assert rel(oracle.r2c_direct(x, h), np.fft.rfft(x)) < 1e-12
+    if n & (n - 1) == 0:
+        assert rel(oracle.r2c(x, h), np.fft.rfft(x)) < 1e-12
+    G = rng.standard_normal((3, h + 1)) + 1j * rng.standard_normal((3, h + 1))
+    ref = np.fft.irfft(G, n) * n
+    assert rel(oracle.c2r_direct(G, n), ref) < 1e-12
+    if n & (n - 1) == 0:
+        assert rel(oracle.c2r(G, n), ref) < 1e-12
+    # a lone Nyquist coefficient synthesises Re F_{n/2} (-1)^j
+    N = np.zeros((1, h + 1), complex)
+    N[0, h] = 2.5 - 7j
+    np.testing.assert_allclose(oracle.c2r_direct(N, n)[0], 2.5 * (-1.0) ** np.arange(n))
+
+
 def test_chessboard_values():
     x = np.ones((1, 6), complex)
     np.testing.assert_array_equal(oracle.chessboard(x, 1)[0], [1, -1, 1, -1, 1, -1])
@@ -323,7 +344,7 @@ def test_mmajor_layout_is_fm_m_times_nlat_plus_ilat():
     np.testing.assert_array_equal(oracle.r2c(x, 5, "mmajor"), oracle.to_mmajor(oracle.r2c(x, 5)))
 
 
-@pytest.mark.parametrize("bad", [(8, 4), (8, -1), (6, 1)])
+@pytest.mark.parametrize("bad", [(8, 5), (8, -1), (6, 1)])
 def test_band_limit_rejected(bad):
     n, mmax = bad
     with pytest.raises(ValueError):
