@@ -389,7 +389,7 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
 
 int fft_plan_set_band_limit(fft_plan p, int64_t mmax) {
     if (!p || p->s.layout == FFT_LAYOUT_C2C) return FFT_ERR_INVALID_ARG;
-    if (mmax < 0 || 2 * mmax >= p->s.n) return FFT_ERR_INVALID_ARG;
+    if (mmax < 0 || 2 * mmax > p->s.n) return FFT_ERR_INVALID_ARG;  // mmax = n/2: Nyquist
     p->mmax = mmax;
     return FFT_OK;
 }

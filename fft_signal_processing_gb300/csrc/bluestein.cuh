@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(C::THREADS)
             if (e > mmax && e < n - mmax) return make_float2(0.f, 0.f);
             const float2 f = ldg_stream(F + (mmajor ? (int64_t)m * nrows + row
                                                     : row * (mmax + 1) + m));
-            if (e == 0) return make_float2(f.x, 0.f);
+            if (e == 0 || 2 * e == n) return make_float2(f.x, 0.f);  // X_0 and a Nyquist bin: real
             return e <= mmax ? f : make_float2(f.x, -f.y);
         }
     };

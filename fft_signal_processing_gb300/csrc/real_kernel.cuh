@@ -11,7 +11,8 @@
 //              X_k = (Z_k + conj Z_{H-k})/2 - i e^{-2 pi i k/N} (Z_k - conj Z_{H-k})/2;
 //   synthesis  Z_k = (X_k + conj X_{H-k}) + i e^{+2 pi i k/N} (X_k - conj X_{H-k}),
 //              z = inverse FFT_H(Z), x_{2m} = Re z_m, x_{2m+1} = Im z_m,
-// with Z_H = Z_0 and X_H = 0 (no Nyquist bin since mmax < N/2).
+// with Z_H = Z_0.  The Nyquist bin (mmax = H, even N only) is real and its own mirror:
+// analysis X_H = Re Z_0 - Im Z_0; synthesis reads Re F_H into X_H (zero when mmax < H).
 #pragma once
 
 #include <cstring>
@@ -89,9 +90,11 @@ __global__ void __launch_bounds__(C::THREADS)
     };
     if constexpr (TMA) {
         if (!tma_stage_aligned(smem, err)) return;
-        // pairs {k, H-k}: one thread reads both Z's and writes both X's in place
+        // pairs {k, H-k}: one thread reads both Z's and writes both X's in place; threads
+        // tid < W own k = 0 and keep Z_0 for the Nyquist bin
         constexpr int NB = H < 256 ? 1 : H / 256;
         constexpr int BK = H / NB;
+        const float2 z0 = (int)threadIdx.x < W ? smem[threadIdx.x] : make_float2(0.f, 0.f);
         const int npair = W * (H / 2 + 1);
         for (int i = (int)threadIdx.x; i < npair; i += C::THREADS) {
             const int wr = i % W, k = i / W;
@@ -108,6 +111,8 @@ __global__ void __launch_bounds__(C::THREADS)
             bulk_commit();
             bulk_wait_smem_read();  // shared memory stays valid until the stores have read it
         }
+        if (mmax == H && (int)threadIdx.x < W && row0 + threadIdx.x < nrows)  // X_H, real
+            stg_stream(out + (int64_t)H * nrows + row0 + threadIdx.x, make_float2(z0.x - z0.y, 0.f));
     } else {
         const int total = W * (mmax + 1);
 #pragma unroll 4
@@ -115,7 +120,13 @@ __global__ void __launch_bounds__(C::THREADS)
             const int wr = i % W, k = i / W;
             const int64_t rr = row0 + wr;
             if (rr >= nrows) continue;
-            const float2 y = recombine(smem[k * W + wr], smem[((H - k) & (H - 1)) * W + wr], k);
+            float2 y;
+            if (k == H) {  // Nyquist bin: Re Z_0 - Im Z_0
+                const float2 z0 = smem[wr];
+                y = make_float2(z0.x - z0.y, 0.f);
+            } else {
+                y = recombine(smem[k * W + wr], smem[((H - k) & (H - 1)) * W + wr], k);
+            }
             const int64_t o = mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k;
             stg_stream(out + o, y);
         }
@@ -163,8 +174,12 @@ __global__ void __launch_bounds__(C::THREADS)
             return;
         }
         if (threadIdx.x < W) {
-            smem[threadIdx.x].y = 0.f;                      // X_0 = Re F_0
-            smem[H * W + threadIdx.x] = make_float2(0.f, 0.f);  // X_H = 0
+            smem[threadIdx.x].y = 0.f;  // X_0 = Re F_0
+            // X_H = Re F_H with the Nyquist bin, else 0 (the tensor copies stop below H)
+            float2 xh = make_float2(0.f, 0.f);
+            if (mmax == H && row0 + threadIdx.x < nrows)
+                xh.x = ldg_stream(in + (int64_t)H * nrows + row0 + threadIdx.x).x;
+            smem[H * W + threadIdx.x] = xh;
         }
     } else {
         (void)err;
@@ -177,7 +192,7 @@ __global__ void __launch_bounds__(C::THREADS)
             float2 x = make_float2(0.f, 0.f);
             if (rr < nrows && k <= mmax) {
                 x = ldg_stream(in + (mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k));
-                if (k == 0) x.y = 0.f;
+                if (k == 0 || k == H) x.y = 0.f;  // X_0, X_H real
             }
             smem[k * W + wr] = x;
         }

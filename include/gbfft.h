@@ -105,7 +105,10 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
  * fft_plan_set_band_limit - set mmax for a real-layout plan: the analysis keeps m = 0..mmax,
  * the synthesis reads F_0..F_mmax and assembles the Hermitian spectrum X_0 = Re F_0,
  * X_m = F_m, X_{n-m} = conj F_m (fourier.ts header comment and fftSynthWGSL).  Requires
- * 0 <= 2*mmax < n (no Nyquist bin).  The default is (n-1)/2 (n/2 - 1 for even n).  Host only.
+ * 0 <= 2*mmax <= n.  mmax = n/2 (even n) gives the full n/2 + 1 half spectrum with the Nyquist
+ * bin, which is real and its own mirror: the analysis returns it with a zero imaginary part,
+ * the synthesis uses Re F_{n/2} once.  The default is (n-1)/2 (n/2 - 1 for even n: the pages'
+ * band limit, no Nyquist bin).  Host only.
  * Returns FFT_OK or FFT_ERR_INVALID_ARG (NULL plan, C2C plan, mmax out of range).
  */
 int fft_plan_set_band_limit(fft_plan plan, int64_t mmax);

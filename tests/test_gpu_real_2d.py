@@ -116,7 +116,7 @@ def test_real_roundtrip(layout):
 def test_real_argument_errors():
     m = fx()
     p = m.Plan(64, 4, 1, m.FORWARD, layout=1)
-    assert p.mmax == 31
+    assert L.fft_plan_set_band_limit(p.handle, 33) == m.FFT_ERR_INVALID_ARG  # above n/2
     L = m.lib()
     assert L.fft_plan_set_band_limit(p.handle, 32) == m.FFT_ERR_INVALID_ARG
     assert L.fft_plan_set_band_limit(p.handle, -1) == m.FFT_ERR_INVALID_ARG
@@ -205,3 +205,35 @@ def test_wait_timeout_real_synthesis():
     torch.cuda.synchronize()
     p.check()
     assert_parity(x.cpu().numpy(), oracle.c2r(F, n), n, "after timeout")
+
+
+# ---- the Nyquist bin: mmax = n/2, the full n/2 + 1 half spectrum -----------------------------
+@pytest.mark.parametrize("n", [4, 8, 64, 4096, 1 << 15, 1000, 6000])
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+@pytest.mark.parametrize("rows", [7, 64])  # odd: direct loads/stores; even: tensor copies
+def test_nyquist_full_half_spectrum(n, layout, rows):
+    h = n // 2
+    if n > 4096:
+        rows = 3 if rows == 7 else 4
+    x = wl().real_normal(300 + n + rows, rows, n)
+    F = gpu_r2c(x, h, layout)
+    ref = oracle.r2c_direct(x, h) if n & (n - 1) else oracle.r2c(x, h)
+    assert_parity(F, ref, h + 1, f"r2c Nyquist n={n} {layout}",
+                  scale=np.linalg.norm(x.astype(np.float64), axis=1))
+    assert np.all(F[:, h].imag == 0)  # real Nyquist bin
+    G = wl().spectrum(400 + n + rows, rows, h)
+    got = gpu_c2r(G, n, h, layout)
+    refx = oracle.c2r_direct(G, n) if n & (n - 1) else oracle.c2r(G, n)
+    assert_parity(got, refx, n, f"c2r Nyquist n={n} {layout}")
+
+
+def test_band_limit_range():
+    m = fx()
+    p = m.Plan(16, 2, 1, m.FORWARD, layout=1)
+    L = m.lib()
+    assert L.fft_plan_set_band_limit(p.handle, 8) == m.FFT_OK  # n/2: Nyquist
+    assert L.fft_plan_set_band_limit(p.handle, 9) == m.FFT_ERR_INVALID_ARG
+    assert L.fft_plan_set_band_limit(p.handle, -1) == m.FFT_ERR_INVALID_ARG
+    q = m.Plan(15, 2, 1, m.FORWARD, layout=1)  # odd length: 2*mmax <= n means mmax <= 7
+    assert L.fft_plan_set_band_limit(q.handle, 7) == m.FFT_OK
+    assert L.fft_plan_set_band_limit(q.handle, 8) == m.FFT_ERR_INVALID_ARG
