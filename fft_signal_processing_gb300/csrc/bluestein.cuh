@@ -128,9 +128,11 @@ __global__ void __launch_bounds__(C::THREADS)
                     if constexpr (MODE == BLU_C2C) {
                         stg_stream(static_cast<float2*>(out_) + row * n + k, y);
                     } else if constexpr (MODE == BLU_R2C) {
+                        // bins 0 and n/2 of a real row are real: drop the rounding residue
+                        const float2 f = (k == 0 || 2 * k == n) ? make_float2(y.x, 0.f) : y;
                         stg_stream(static_cast<float2*>(out_) +
                                        (mmajor ? (int64_t)k * nrows + row : row * (mmax + 1) + k),
-                                   y);
+                                   f);
                     } else {
                         __stcs(static_cast<float*>(out_) + row * n + k, y.x);
                     }
