@@ -33,7 +33,8 @@ ABI_SYMBOLS = (
     "fft_plan_create", "fft_plan_set_band_limit", "fft_plan_workspace_bytes",
     "fft_plan_describe", "fft_plan_query", "fft_exec_c2c", "fft_exec_r2c", "fft_exec_c2r",
     "fft_plan_check", "fft_plan_destroy", "fft_status_string", "fft_version",
-    "fft_exec_c2c_noalloc", "fft_plan_set_wait_timeout", "fft_shift",
+    "fft_exec_c2c_noalloc", "fft_plan_set_wait_timeout", "fft_shift", "fft_plan_create_2d",
+    "fft_plan_query_2d",
 )
 
 _LIB = None
@@ -60,6 +61,8 @@ def lib():
         L.fft_plan_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
         L.fft_plan_describe.argtypes = [vp, ctypes.c_char_p, sz]
         L.fft_plan_query.argtypes = [i64, i64, ci, ci, ci, ci, ctypes.c_char_p, sz]
+        L.fft_plan_create_2d.argtypes = [i64, i64, i64, ci, ci, ctypes.POINTER(vp)]
+        L.fft_plan_query_2d.argtypes = [i64, i64, i64, ci, ci, ctypes.c_char_p, sz]
         L.fft_exec_c2c.argtypes = [vp, vp, vp, vp]
         L.fft_shift.argtypes = [vp, vp, i64, i64, i64, ci, ci, vp]
         L.fft_exec_r2c.argtypes = [vp, vp, vp, vp]
@@ -87,9 +90,13 @@ def _check(rc, what):
         raise GbfftError(rc, what)
 
 
-def query(n, batch, dims=1, direction=FORWARD, layout=LAYOUT_C2C, shift=False) -> str:
+def query(n, batch, dims=1, direction=FORWARD, layout=LAYOUT_C2C, shift=False, ny=None) -> str:
     """Host-only: the execution path a plan with these parameters would use."""
     buf = ctypes.create_string_buffer(1024)
+    if dims == 2 and ny is not None and int(ny) != int(n):
+        _check(lib().fft_plan_query_2d(int(n), int(ny), int(batch), int(direction),
+                                       int(bool(shift)), buf, len(buf)), "fft_plan_query_2d")
+        return buf.value.decode()
     _check(lib().fft_plan_query(int(n), int(batch), int(dims), int(direction), int(layout),
                                 int(bool(shift)), buf, len(buf)), "fft_plan_query")
     return buf.value.decode()
@@ -138,19 +145,26 @@ def _stream_ptr(stream):
 class Plan:
     """A planned batched transform on the current CUDA device (see include/gbfft.h).
 
-    dims=1: rows of n points; dims=2: n x n images.  direction: FORWARD (-1) / INVERSE (+1),
+    dims=1: rows of n points; dims=2: ny x n images (ny = n unless given; both powers of two
+    up to 4096, rows of n points then columns of ny points).  direction: FORWARD / INVERSE,
     unnormalised.  layout: LAYOUT_C2C, or LAYOUT_REAL_ROWMAJOR / LAYOUT_REAL_MMAJOR for the
     band-limited real-row analysis (FORWARD, r2c) / synthesis (INVERSE, c2r) with mmax.
     shift: fftshift folded in as the (-1)^j chessboard (C2C only).
     """
 
     def __init__(self, n, batch=1, dims=1, direction=FORWARD, layout=LAYOUT_C2C, shift=False,
-                 mmax=None):
+                 mmax=None, ny=None):
         self.n, self.batch, self.dims = int(n), int(batch), int(dims)
         self.direction, self.layout, self.shift = int(direction), int(layout), bool(shift)
+        self.ny = (self.n if ny is None else int(ny)) if self.dims == 2 else 1
         h = ctypes.c_void_p()
-        _check(lib().fft_plan_create(self.n, self.batch, self.dims, self.direction, self.layout,
-                                     int(self.shift), ctypes.byref(h)), "fft_plan_create")
+        if self.dims == 2 and self.ny != self.n:
+            _check(lib().fft_plan_create_2d(self.n, self.ny, self.batch, self.direction,
+                                            int(self.shift), ctypes.byref(h)), "fft_plan_create_2d")
+        else:
+            _check(lib().fft_plan_create(self.n, self.batch, self.dims, self.direction,
+                                         self.layout, int(self.shift), ctypes.byref(h)),
+                   "fft_plan_create")
         self._h = h
         self.mmax = None
         if layout != LAYOUT_C2C:
@@ -191,7 +205,7 @@ class Plan:
 
     # ---- shapes ----
     def complex_shape(self):
-        return (self.batch, self.n) if self.dims == 1 else (self.batch, self.n, self.n)
+        return (self.batch, self.n) if self.dims == 1 else (self.batch, self.ny, self.n)
 
     def spectrum_shape(self):
         m1 = self.mmax + 1
@@ -230,7 +244,7 @@ class Plan:
     def c2c(self, x, out=None, stream=None):
         import torch
 
-        numel = self.batch * self.n * (self.n if self.dims == 2 else 1)
+        numel = self.batch * self.n * self.ny
         self._need(x, torch.complex64, numel, "c2c input")
         if out is None:
             out = torch.empty(self.complex_shape(), dtype=torch.complex64, device=x.device)

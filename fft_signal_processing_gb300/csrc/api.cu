@@ -50,6 +50,8 @@ struct PlanSpec {
     int log2n1 = 0, log2n2 = 0;  // four-step split
     int lowbits = 0;             // four-step two-level twiddle split
     int log2m = 0;               // chirp-z transform length
+    int64_t ny = 1;              // 2-D: rows per image (ny x n images; ny = n when square)
+    int log2ny = 0;
 };
 
 int ilog2_exact(int64_t n) {
@@ -60,8 +62,9 @@ int ilog2_exact(int64_t n) {
 }
 
 // Host validation and path choice shared by fft_plan_create and fft_plan_query.
+// ny: rows per image for dims 2 (0 means square, ny = n); ignored for dims 1.
 int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int shift,
-              PlanSpec* ps) {
+              PlanSpec* ps, int64_t ny = 0) {
     if (batch < 1) return FFT_ERR_INVALID_ARG;
     if (dims != 1 && dims != 2) return FFT_ERR_INVALID_ARG;
     if (direction != FFT_FORWARD && direction != FFT_INVERSE) return FFT_ERR_INVALID_ARG;
@@ -92,6 +95,9 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
         s.path = PATH_REAL;
     } else if (dims == 2) {
         if (l < 1 || l > FFT_MAX_LOG2N_2D) return FFT_ERR_UNSUPPORTED_SIZE;
+        s.ny = ny ? ny : n;
+        s.log2ny = ilog2_exact(s.ny);
+        if (s.log2ny < 1 || s.log2ny > FFT_MAX_LOG2N_2D) return FFT_ERR_UNSUPPORTED_SIZE;
         s.path = PATH_2D;
     } else {
         if (l > FFT_MAX_LOG2N_1D) return FFT_ERR_UNSUPPORTED_SIZE;
@@ -105,7 +111,7 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
         }
     }
     // total element count must stay addressable with 64-bit byte offsets
-    const int64_t per = dims == 2 ? n * n : n;
+    const int64_t per = dims == 2 ? n * s.ny : n;
     if (batch > (INT64_C(1) << 58) / per) return FFT_ERR_UNSUPPORTED_SIZE;
     *ps = s;
     return FFT_OK;
@@ -222,15 +228,16 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
                      padded_bytes(s.log2m, rows_maxrb(s.log2m), w));
             break;
         }
-        case PATH_2D: {
-            Geo g1 = rows_geo(s.log2n), g2 = cols_geo(s.log2n, s.log2n);
+        case PATH_2D: {  // ny x n images: n-point rows, then ny-point columns
+            Geo g1 = rows_geo(s.log2n), g2 = cols_geo(s.log2ny, s.log2n);
             snprintf(buf, sizeof buf,
                      "path=2d n=%lldx%lld batch=%lld %s shift=%d radix=%s kernels=2 "
                      "rows(threads=%d rows_per_cta=%d smem=%zu) "
-                     "columns(threads=%d cols_per_cta=%d smem=%zu)",
-                     (long long)s.n, (long long)s.n, (long long)s.batch, dir, s.shift,
+                     "columns(radix=%s threads=%d cols_per_cta=%d smem=%zu)",
+                     (long long)s.ny, (long long)s.n, (long long)s.batch, dir, s.shift,
                      radix_string(s.log2n, rows_maxrb(s.log2n)).c_str(), g1.threads, g1.per_cta,
-                     g1.smem, g2.threads, g2.per_cta, g2.smem);
+                     g1.smem, radix_string(s.log2ny, cols_pass_maxrb(s.log2ny, s.log2n)).c_str(),
+                     g2.threads, g2.per_cta, g2.smem);
             break;
         }
         default: {
@@ -315,13 +322,38 @@ int fft_plan_query(int64_t n, int64_t batch, int dims, int direction, int layout
     return FFT_OK;
 }
 
+static int create_from_spec(const PlanSpec& s, fft_plan* out);
+
 int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layout, int shift,
                     fft_plan* out) {
     if (!out) return FFT_ERR_INVALID_ARG;
     *out = nullptr;
     PlanSpec s;
-    int rc = plan_spec(n, batch, dims, direction, layout, shift, &s);
+    const int rc = plan_spec(n, batch, dims, direction, layout, shift, &s);
+    return rc != FFT_OK ? rc : create_from_spec(s, out);
+}
+
+int fft_plan_create_2d(int64_t nx, int64_t ny, int64_t batch, int direction, int shift,
+                       fft_plan* out) {
+    if (!out) return FFT_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (ny < 1) return FFT_ERR_UNSUPPORTED_SIZE;
+    PlanSpec s;
+    const int rc = plan_spec(nx, batch, 2, direction, FFT_LAYOUT_C2C, shift, &s, ny);
+    return rc != FFT_OK ? rc : create_from_spec(s, out);
+}
+
+int fft_plan_query_2d(int64_t nx, int64_t ny, int64_t batch, int direction, int shift,
+                      char* buf, size_t len) {
+    if (ny < 1) return FFT_ERR_UNSUPPORTED_SIZE;
+    PlanSpec s;
+    const int rc = plan_spec(nx, batch, 2, direction, FFT_LAYOUT_C2C, shift, &s, ny);
     if (rc != FFT_OK) return rc;
+    if (buf && len) snprintf(buf, len, "%s", describe_spec(s, 0).c_str());
+    return FFT_OK;
+}
+
+static int create_from_spec(const PlanSpec& s, fft_plan* out) {
 
     gbfft_plan_s* p = new (std::nothrow) gbfft_plan_s();
     if (!p) return FFT_ERR_OOM;
@@ -339,7 +371,7 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
             break;
         case PATH_2D:
             p->off_a = append_pass_tables(tw, s.log2n, rows_maxrb(s.log2n));  // row pass
-            p->off_b = append_pass_tables(tw, s.log2n, cols_pass_maxrb(s.log2n, s.log2n));
+            p->off_b = append_pass_tables(tw, s.log2ny, cols_pass_maxrb(s.log2ny, s.log2n));
             break;
         case PATH_FOURSTEP: {
             p->off_a = append_pass_tables(tw, s.log2n1, cols_pass_maxrb(s.log2n1, s.log2n2));
@@ -418,7 +450,7 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
     const PlanSpec& s = p->s;
     if (s.layout != FFT_LAYOUT_C2C) return FFT_ERR_INVALID_ARG;
     if (!aligned16(in) || !aligned16(out)) return FFT_ERR_MISALIGNED;
-    const size_t bytes = (size_t)s.batch * (size_t)(s.dims == 2 ? s.n * s.n : s.n) * 8u;
+    const size_t bytes = (size_t)s.batch * (size_t)(s.dims == 2 ? s.n * s.ny : s.n) * 8u;
     if (in != out && ranges_overlap(in, bytes, out, bytes)) return FFT_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     const float2* x = (const float2*)in;
@@ -451,12 +483,11 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                                p->d_err, p->wait_limit_ns, st);
             break;
         }
-        case PATH_2D: {
-            const int64_t n = s.n;
-            e = run_rows(s.log2n, s.direction, x, y, s.batch * n, p->d_tw + p->off_a,
+        case PATH_2D: {  // batch*ny rows of n points, then batch*n columns of ny points
+            e = run_rows(s.log2n, s.direction, x, y, s.batch * s.ny, p->d_tw + p->off_a,
                          (s.shift && fwd) ? KF_CHESS_LOAD : 0, 1, p->d_err, p->wait_limit_ns, st);
             if (e == cudaSuccess)
-                e = run_cols(s.log2n, s.direction, y, y, s.batch * n, s.log2n,
+                e = run_cols(s.log2ny, s.direction, y, y, s.batch * s.n, s.log2n,
                              p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0, 1,
                              nullptr, nullptr, 0, p->d_err, p->wait_limit_ns, st);
             break;

@@ -41,24 +41,26 @@ cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, c
                       int flags, int ep, const float2* hi, const float2* lo, int lowbits,
                       int* err, uint64_t lim, cudaStream_t s) {
     if constexpr (L >= kColsTmaMinLog2 && L <= kColsTmaMaxLog2) {
-        // the planners only ask for matrices at least one tile wide at these sizes
-        if (!cols_use_tma(L, log2s)) return cudaErrorInvalidValue;
-        if constexpr (L >= kBigTileMinLog2) {
-            using RC = ColsBigCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
-            return launch_cols_big<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags, ep,
-                                                ColsTwiddle{hi, lo, lowbits}, err, lim, s);
-        } else {
-            using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
-            return launch_cols_tma<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags, ep,
-                                                ColsTwiddle{hi, lo, lowbits}, err, lim, s);
+        if (cols_use_tma(L, log2s)) {  // matrices at least one column tile wide
+            if constexpr (L >= kBigTileMinLog2) {
+                using RC = ColsBigCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
+                return launch_cols_big<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags,
+                                                    ep, ColsTwiddle{hi, lo, lowbits}, err, lim,
+                                                    s);
+            } else {
+                using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
+                return launch_cols_tma<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags,
+                                                    ep, ColsTwiddle{hi, lo, lowbits}, err, lim,
+                                                    s);
+            }
         }
-    } else {
-        (void)err;
-        (void)lim;
-        using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 0), false>;
-        MapCols<TW> m{count, log2s, L, ep, hi, lo, lowbits};
-        return launch_fft<C, DIR, MapCols<TW>>(in, out, m, tw, flags, s);
     }
+    // short columns, and images narrower than a tile: the generic strided kernel
+    (void)err;
+    (void)lim;
+    using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 0), false>;
+    MapCols<TW> m{count, log2s, L, ep, hi, lo, lowbits};
+    return launch_fft<C, DIR, MapCols<TW>>(in, out, m, tw, flags, s);
 }
 
 template <int L, int DIR>

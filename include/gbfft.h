@@ -102,6 +102,23 @@ int fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int layou
                     fft_plan* out);
 
 /*
+ * fft_plan_create_2d - plan a batched 2-D C2C transform of rectangular images: batch images of
+ * ny rows x nx columns, row-major, complex64 (Mota, "High Performance Fourier Transforms on
+ * GPUs with GLSL", 2.7 Eq. 19: the nx-point transform of every row, then the ny-point
+ * transform of every column).  nx and ny are powers of two with 2 <= nx, ny <= 2^12; shift
+ * folds the 2-D fftshift in as the chessboard (-1)^(x+y) (forward load, inverse store).
+ * Everything else (ownership, execution with fft_exec_c2c, errors) is as for fft_plan_create
+ * with dims = 2, which is the square case ny = nx.
+ */
+int fft_plan_create_2d(int64_t nx, int64_t ny, int64_t batch, int direction, int shift,
+                       fft_plan* out);
+
+/* fft_plan_query_2d - host-only description of the plan fft_plan_create_2d would make (as
+ * fft_plan_query); allocates nothing and touches no device. */
+int fft_plan_query_2d(int64_t nx, int64_t ny, int64_t batch, int direction, int shift, char* buf,
+                      size_t len);
+
+/*
  * fft_plan_set_band_limit - set mmax for a real-layout plan: the analysis keeps m = 0..mmax,
  * the synthesis reads F_0..F_mmax and assembles the Hermitian spectrum X_0 = Re F_0,
  * X_m = F_m, X_{n-m} = conj F_m (fourier.ts header comment and fftSynthWGSL).  Requires

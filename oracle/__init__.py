@@ -127,6 +127,15 @@ def fft2d(x, sign=-1):
     return out
 
 
+def fft2d_rect(x, sign=-1):
+    """Row-column 2-D FFT of every ny x nx image (last two axes, powers of two, rectangular
+    allowed): the 1-D FFT of every row, then of every column (Mota §2.7 Eq. 19)."""
+    x = _c128(x)
+    rows = fft(x, sign)
+    cols = fft(np.ascontiguousarray(np.swapaxes(rows, -1, -2)), sign)
+    return np.ascontiguousarray(np.swapaxes(cols, -1, -2))
+
+
 def fftshift(x, dims=1):
     """Rotate every row (dims=1) or image (dims=2) by n/2 (numpy-style fftshift, even n)."""
     x = _c128(x)
@@ -183,7 +192,7 @@ def transform(x, direction=-1, dims=1, shift=False):
     def t(v):
         if dims == 1:
             return fft(v, direction) if (n & (n - 1)) == 0 else dft(v, direction)
-        return fft2d(v, direction)
+        return fft2d(v, direction) if np.shape(v)[-2] == n else fft2d_rect(v, direction)
 
     if not shift:
         return t(x)

@@ -148,3 +148,14 @@ def test_shift_argument_errors_before_touching_the_device():
     assert L.fft_shift(p(4096), p(1 << 20), 4, 1, 1, 1, 2, None) == fx.FFT_ERR_INVALID_ARG  # inverse
     assert L.fft_shift(p(4100), p(1 << 20), 4, 1, 1, 1, 0, None) == fx.FFT_ERR_MISALIGNED
     assert L.fft_shift(p(4096), p(1 << 20), 1 << 40, 2, 1, 2, 0, None) == fx.FFT_ERR_UNSUPPORTED_SIZE
+
+
+@pytest.mark.parametrize("ny,nx", [(4096, 2), (2, 4096), (64, 128), (4096, 8), (8, 4096)])
+def test_rectangular_2d_plans(ny, nx):
+    d = fx.query(nx, 3, dims=2, ny=ny)
+    assert f"path=2d n={ny}x{nx} " in d and "kernels=2" in d
+    L = fx.lib()
+    assert L.fft_plan_query_2d(nx, 3 * ny, 1, -1, 0, None, 0) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert L.fft_plan_query_2d(nx, 0, 1, -1, 0, None, 0) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert L.fft_plan_query_2d(nx, 8192, 1, -1, 0, None, 0) == fx.FFT_ERR_UNSUPPORTED_SIZE
+    assert L.fft_plan_create_2d(nx, ny, 1, -1, 0, None) == fx.FFT_ERR_INVALID_ARG

@@ -237,3 +237,24 @@ def test_band_limit_range():
     q = m.Plan(15, 2, 1, m.FORWARD, layout=1)  # odd length: 2*mmax <= n means mmax <= 7
     assert L.fft_plan_set_band_limit(q.handle, 7) == m.FFT_OK
     assert L.fft_plan_set_band_limit(q.handle, 8) == m.FFT_ERR_INVALID_ARG
+
+
+# ---- rectangular 2-D images (fft_plan_create_2d) ----------------------------------------------
+@pytest.mark.parametrize("ny,nx", [(4096, 2), (2, 4096), (64, 128), (128, 64), (1024, 256),
+                                   (4096, 8), (8, 4096), (4096, 16), (512, 4096), (32, 2)])
+@pytest.mark.parametrize("direction", [-1, 1])
+@pytest.mark.parametrize("shift", [False, True])
+def test_2d_rectangular(ny, nx, direction, shift):
+    m = fx()
+    batch = 2 if ny * nx <= (1 << 20) else 1
+    rng = np.random.default_rng(ny * 7 + nx)
+    img = (rng.standard_normal((batch, ny, nx)) +
+           1j * rng.standard_normal((batch, ny, nx))).astype(np.complex64)
+    p = m.Plan(nx, batch, 2, direction, shift=shift, ny=ny)
+    assert f"n={ny}x{nx}" in p.describe()
+    xd = torch.from_numpy(img).cuda()
+    y = p.c2c(xd, out=xd) if (ny + nx) % 3 == 0 else p.c2c(xd)  # some in place
+    torch.cuda.synchronize()
+    p.check()
+    assert_parity(y.cpu().numpy(), oracle.transform(img, direction, 2, shift), nx * ny,
+                  f"2d {ny}x{nx} dir={direction} shift={shift}")

@@ -248,6 +248,20 @@ def test_nyquist_bin_full_half_spectrum(n):
     np.testing.assert_allclose(oracle.c2r_direct(N, n)[0], 2.5 * (-1.0) ** np.arange(n))
 
 
+@pytest.mark.parametrize("ny,nx", [(2, 8), (16, 4), (64, 32)])
+def test_rectangular_2d_matches_numpy_and_separability(ny, nx):
+    x = crand(2, ny, nx)
+    assert rel(oracle.fft2d_rect(x, -1), np.fft.fft2(x)) < 1e-13
+    assert rel(oracle.fft2d_rect(x, +1), np.fft.ifft2(x) * nx * ny) < 1e-13
+    u, v = crand(1, ny)[0], crand(1, nx)[0]
+    sep = oracle.fft2d_rect(np.outer(u, v)[None], -1)[0]
+    assert rel(sep, np.outer(oracle.fft(u[None])[0], oracle.fft(v[None])[0])) < 1e-13
+    # the shifted transform: 2-D fftshift of the transform; the inverse undoes it up to nx*ny
+    y = oracle.transform(x, -1, 2, True)
+    assert rel(y, np.fft.fftshift(np.fft.fft2(x), axes=(-2, -1))) < 1e-13
+    assert rel(oracle.transform(y, +1, 2, True), nx * ny * x) < 1e-13
+
+
 def test_chessboard_values():
     x = np.ones((1, 6), complex)
     np.testing.assert_array_equal(oracle.chessboard(x, 1)[0], [1, -1, 1, -1, 1, -1])
