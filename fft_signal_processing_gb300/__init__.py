@@ -34,7 +34,7 @@ ABI_SYMBOLS = (
     "fft_plan_describe", "fft_plan_query", "fft_exec_c2c", "fft_exec_r2c", "fft_exec_c2r",
     "fft_plan_check", "fft_plan_destroy", "fft_status_string", "fft_version",
     "fft_exec_c2c_noalloc", "fft_plan_set_wait_timeout", "fft_shift", "fft_plan_create_2d",
-    "fft_plan_query_2d",
+    "fft_plan_query_2d", "fft_plan_set_normalization",
 )
 
 _LIB = None
@@ -58,6 +58,7 @@ def lib():
         i64, ci, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
         L.fft_plan_create.argtypes = [i64, i64, ci, ci, ci, ci, ctypes.POINTER(vp)]
         L.fft_plan_set_band_limit.argtypes = [vp, i64]
+        L.fft_plan_set_normalization.argtypes = [vp, ci]
         L.fft_plan_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
         L.fft_plan_describe.argtypes = [vp, ctypes.c_char_p, sz]
         L.fft_plan_query.argtypes = [i64, i64, ci, ci, ci, ci, ctypes.c_char_p, sz]
@@ -153,7 +154,7 @@ class Plan:
     """
 
     def __init__(self, n, batch=1, dims=1, direction=FORWARD, layout=LAYOUT_C2C, shift=False,
-                 mmax=None, ny=None):
+                 mmax=None, ny=None, normalize=False):
         self.n, self.batch, self.dims = int(n), int(batch), int(dims)
         self.direction, self.layout, self.shift = int(direction), int(layout), bool(shift)
         self.ny = (self.n if ny is None else int(ny)) if self.dims == 2 else 1
@@ -167,6 +168,8 @@ class Plan:
                    "fft_plan_create")
         self._h = h
         self.mmax = None
+        if normalize:
+            self.set_normalization(True)
         if layout != LAYOUT_C2C:
             self.mmax = (self.n - 1) // 2 if mmax is None else int(mmax)
             _check(lib().fft_plan_set_band_limit(self._h, self.mmax), "fft_plan_set_band_limit")
@@ -187,6 +190,11 @@ class Plan:
 
     def check(self):
         _check(lib().fft_plan_check(self._h), "fft_plan_check")
+
+    def set_normalization(self, on: bool = True):
+        """Scale the output by 1/n (1/(nx*ny) for 2-D), or not (the default)."""
+        _check(lib().fft_plan_set_normalization(self._h, int(bool(on))),
+               "fft_plan_set_normalization")
 
     def set_wait_timeout(self, ns: int):
         """Limit of every device-side wait of this plan's kernels (0: give up at once)."""

@@ -282,6 +282,7 @@ struct gbfft_plan_s {
     size_t work_bytes = 0;
     int* d_err = nullptr;
     uint64_t wait_limit_ns = 2000000000ull;  // bounded device waits: 2 s
+    int normalize = 0;                       // 1: output scaled by 1/n (1/(nx*ny) for 2-D)
 };
 
 static void free_plan(gbfft_plan_s* p) {
@@ -390,8 +391,8 @@ static int create_from_spec(const PlanSpec& s, fft_plan* out) {
                 const int64_t h = s.n / 2;
                 const bool fwd = s.direction == FFT_FORWARD;
                 p->off_chirp = host::append_chirp(tw, s.n, s.direction, s.shift && fwd ? h : 0);
-                p->off_chirp_out = s.shift ? host::append_chirp(tw, s.n, s.direction, fwd ? 0 : -h)
-                                           : p->off_chirp;
+                // a table of its own, so that fft_plan_set_normalization can rescale it
+                p->off_chirp_out = host::append_chirp(tw, s.n, s.direction, s.shift && !fwd ? -h : 0);
             }
             p->off_bhat = host::append_chirp_filter(tw, s.n, int64_t(1) << s.log2m, s.direction);
             break;
@@ -416,6 +417,25 @@ static int create_from_spec(const PlanSpec& s, fft_plan* out) {
         return map_cuda(e);
     }
     *out = p;
+    return FFT_OK;
+}
+
+int fft_plan_set_normalization(fft_plan p, int normalize) {
+    if (!p || p->s.layout != FFT_LAYOUT_C2C || (normalize != 0 && normalize != 1))
+        return FFT_ERR_INVALID_ARG;
+    const PlanSpec& s = p->s;
+    if (s.path == PATH_BLUESTEIN && normalize != p->normalize) {
+        // the chirp of the store, times 1/n when normalising (rewritten in place)
+        std::vector<float2> t;
+        const bool fwd = s.direction == FFT_FORWARD;
+        const size_t off = host::append_chirp(t, s.n, s.direction, s.shift && !fwd ? -(s.n / 2) : 0);
+        const float f = normalize ? (float)(1.0 / (double)s.n) : 1.f;
+        for (size_t i = off; i < t.size(); ++i) t[i] = make_float2(t[i].x * f, t[i].y * f);
+        if (cudaMemcpy(p->d_tw + p->off_chirp_out, t.data() + off,
+                       (t.size() - off) * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FFT_ERR_CUDA;
+    }
+    p->normalize = normalize;
     return FFT_OK;
 }
 
@@ -459,7 +479,8 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
     cudaError_t e = cudaSuccess;
     switch (s.path) {
         case PATH_ONEPASS: {
-            const int flags = s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0;
+            const int flags = (s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0) |
+                              (p->normalize ? kf_scale(s.log2n) : 0);
             e = run_rows(s.log2n, s.direction, x, y, s.batch, p->d_tw + p->off_a, flags, 0,
                          p->d_err, p->wait_limit_ns, st);
             break;
@@ -479,7 +500,9 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                          p->wait_limit_ns, st);
             if (e == cudaSuccess)
                 e = run_rows_t(s.log2n2, s.direction, wk, y, s.batch * n1, s.log2n1,
-                               p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0,
+                               p->d_tw + p->off_b,
+                               ((s.shift && !fwd) ? KF_CHESS_STORE : 0) |
+                                   (p->normalize ? kf_scale(s.log2n) : 0),
                                p->d_err, p->wait_limit_ns, st);
             break;
         }
@@ -488,8 +511,10 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                          (s.shift && fwd) ? KF_CHESS_LOAD : 0, 1, p->d_err, p->wait_limit_ns, st);
             if (e == cudaSuccess)
                 e = run_cols(s.log2ny, s.direction, y, y, s.batch * s.n, s.log2n,
-                             p->d_tw + p->off_b, (s.shift && !fwd) ? KF_CHESS_STORE : 0, 1,
-                             nullptr, nullptr, 0, p->d_err, p->wait_limit_ns, st);
+                             p->d_tw + p->off_b,
+                             ((s.shift && !fwd) ? KF_CHESS_STORE : 0) |
+                                 (p->normalize ? kf_scale(s.log2n + s.log2ny) : 0),
+                             1, nullptr, nullptr, 0, p->d_err, p->wait_limit_ns, st);
             break;
         }
         default:

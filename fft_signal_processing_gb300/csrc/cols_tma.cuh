@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
                 const int k = j + r * SL;
                 float2 y = v[b * RL + r];
                 if (flags & KF_CHESS_STORE) y = neg_if(y, (k * elem_parity + cp) & 1);
+                y = scale_pow2(y, flags);
                 smem[k * W + w] = y;  // dense [row][W] tile for the copy engine
             }
         }

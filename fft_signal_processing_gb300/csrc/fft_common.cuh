@@ -199,8 +199,20 @@ enum : int {
     KF_CHESS_LOAD = 1,   // multiply input element (row, j) by (-1)^j before the transform
     KF_CHESS_STORE = 2,  // multiply output element (row, k) by (-1)^k after the transform
     KF_CHESS_ROW = 4,    // 2-D chessboard: also multiply by (-1)^row
+    KF_SCALE_SHIFT = 8,  // bits 8..15 hold k: the stored output is multiplied by 2^-k (k = 0: not)
 };
 
+// Flag bits asking the final store of a transform of 2^k points to scale by 1/2^k.
+__host__ __device__ constexpr int kf_scale(int k) { return k << KF_SCALE_SHIFT; }
+
 __device__ __forceinline__ float2 neg_if(float2 v, int odd) { return odd ? cneg(v) : v; }
+
+// v * 2^-k for the k held in flags: an exact power-of-two scaling (k < 127 keeps 2^-k normal).
+__device__ __forceinline__ float2 scale_pow2(float2 v, int flags) {
+    const int k = (flags >> KF_SCALE_SHIFT) & 0xff;
+    if (k == 0) return v;
+    const float s = __int_as_float((127 - k) << 23);
+    return make_float2(v.x * s, v.y * s);
+}
 
 }  // namespace gbfft

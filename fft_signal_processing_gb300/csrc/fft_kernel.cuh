@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(C::THREADS)
                 float2 y = v[b * RL + r];
                 if constexpr (M::TWIDDLE) y = ctw<DIR>(y, map.twiddle(tr, k));
                 if (flags & KF_CHESS_STORE) y = neg_if(y, (k * M::SE * ep + sp) & 1);
+                y = scale_pow2(y, flags);
                 stg_stream(dst + k * os, y);
             }
         }

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
                     const int k = j + r * SL;
                     float2 y = v[b * RL + r];
                     if (flags & KF_CHESS_STORE) y = neg_if(y, (k + rp) & 1);
+                    y = scale_pow2(y, flags);
                     stg_stream(dst + k, y);
                 }
             }

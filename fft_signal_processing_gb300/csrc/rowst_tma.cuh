@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
                 const int k = j + r * SL;
                 float2 y = v[b * RL + r];
                 if (flags & KF_CHESS_STORE) y = neg_if(y, rp);
+                y = scale_pow2(y, flags);
                 smem[k * W + w] = y;  // dense [k2][W] tile for the copy engine
             }
         }

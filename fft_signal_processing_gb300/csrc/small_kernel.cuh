@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(256)
         for (int k = 0; k < N; ++k) {
             float2 y = v[k];
             if (flags & KF_CHESS_STORE) y = neg_if(y, (k + rp) & 1);
+            y = scale_pow2(y, flags);
             sm[tid * RS + k] = y;  // only this thread touches its row
         }
     }

@@ -119,6 +119,20 @@ int fft_plan_query_2d(int64_t nx, int64_t ny, int64_t batch, int direction, int 
                       size_t len);
 
 /*
+ * fft_plan_set_normalization - normalize = 1 scales the plan's output by 1/n (dims 1) or
+ * 1/(nx*ny) (dims 2), the factor Mota, "High Performance Fourier Transforms on GPUs with
+ * GLSL", puts on the inverse transform (2.2 Eq. 5; 2.7 for images), so that a normalised
+ * inverse undoes the forward transform exactly; 0 (the default) leaves both directions
+ * unnormalised.  The factor is applied in the last kernel's store (an exact power of two for
+ * power-of-two sizes; folded into the store chirp for other lengths), at no extra pass.
+ * C2C plans only.  Host call; for lengths that are not powers of two it rewrites a small plan
+ * table with a synchronous copy, so call it before enqueueing work that uses the plan.
+ * Returns FFT_OK, FFT_ERR_INVALID_ARG (NULL or real-layout plan, normalize not 0/1) or
+ * FFT_ERR_CUDA.
+ */
+int fft_plan_set_normalization(fft_plan plan, int normalize);
+
+/*
  * fft_plan_set_band_limit - set mmax for a real-layout plan: the analysis keeps m = 0..mmax,
  * the synthesis reads F_0..F_mmax and assembles the Hermitian spectrum X_0 = Re F_0,
  * X_m = F_m, X_{n-m} = conj F_m (fourier.ts header comment and fftSynthWGSL).  Requires
