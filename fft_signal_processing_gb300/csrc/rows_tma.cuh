@@ -39,7 +39,9 @@ struct RowsTmaCfg {
     static_assert((STAGE * sizeof(float2)) % 128 == 0, "stages stay 128-byte aligned");
 };
 
-template <class RC, int DIR>
+// SCALE: the output scaling of normalised plans (flags' scale bits) is a separate
+// instantiation, so that the unscaled kernel carries none of its code.
+template <class RC, int DIR, bool SCALE>
 __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     k_rows_tma(const float2* in, float2* out, int64_t nrows, const float2* __restrict__ tw,
                int flags, int row_parity, int* err, uint64_t limit_ns) {
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
                     const int k = j + r * SL;
                     float2 y = v[b * RL + r];
                     if (flags & KF_CHESS_STORE) y = neg_if(y, (k + rp) & 1);
-                    y = scale_pow2(y, flags);
+                    if constexpr (SCALE) y = scale_pow2(y, flags);
                     stg_stream(dst + k, y);
                 }
             }
@@ -156,19 +158,24 @@ template <class RC, int DIR>
 cudaError_t launch_rows_tma(const float2* in, float2* out, int64_t nrows, const float2* tw,
                             int flags, int row_parity, int* err, uint64_t limit_ns,
                             cudaStream_t stream) {
-    auto kern = k_rows_tma<RC, DIR>;
+    auto plain = k_rows_tma<RC, DIR, false>;
+    auto scaled = k_rows_tma<RC, DIR, true>;
+    auto kern = (flags >> KF_SCALE_SHIFT) ? scaled : plain;
     static int configured_dev = -1;  // attributes and occupancy are per device
     static int grid_per_sm = 0, num_sms = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)RC::SMEM_BYTES);
+        for (auto k : {plain, scaled}) {
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)RC::SMEM_BYTES);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        }
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&grid_per_sm, kern, RC::C::THREADS,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&grid_per_sm, plain, RC::C::THREADS,
                                                               RC::SMEM_BYTES);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
