@@ -13,7 +13,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 pytestmark = pytest.mark.skipif(torch.cuda.is_available(),
-                                reason="CPU test of the gloo path (a GPU box would pick NCCL)")
+                                reason="CPU test of the gloo path (with CUDA present the bench picks NCCL)")
 
 
 def _free_port():
