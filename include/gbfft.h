@@ -1,12 +1,13 @@
 /*
  * gbfft.h - C ABI of the batched fp32 FFT library for one NVIDIA GB300 GPU (sm_103a).
  *
- * The library computes, for power-of-two n,
+ * The library computes
  *
  *     X_k = sum_{j<n} x_j * exp(s * 2*pi*i * j*k / n),   s = -1 forward, s = +1 inverse,
  *
- * on batches of contiguous rows (dims = 1) or n x n images (dims = 2, row-column: all rows,
- * then all columns), with no 1/n scaling in either direction.  This is the discrete Fourier
+ * on batches of contiguous rows (dims = 1: power-of-two n, or any n up to 8192) or images
+ * (dims = 2, power-of-two sides, row-column: all rows, then all columns), unnormalised in both
+ * directions unless a plan asks for 1/n (fft_plan_set_normalization).  This is the discrete Fourier
  * transform of Mota, "High Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5, with
  * the sign convention of its Eq. 5 / Algorithm 2 and the unnormalised inverse of the WGSL
  * Stockham kernels in "src/sht/wgsl/fourier.ts"; the 2-D form is Mota §2.7 Eq. 19.
