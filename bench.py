@@ -11,7 +11,8 @@ sweep_<log2n> (batch*N = 2^26 rows of 3 tones + noise, forward), any_<n> (the sa
 length n <= 8192 that is not a power of two: the chirp-z path), realany_<n> (the real
 workload below for such a length, mmax = n/3), real (2048 rows x 4096,
 mmax = 1365, synthesis then analysis, m-major spectrum), 2d (4096 x 4096, forward with the 2-D
-chessboard then inverse).
+chessboard then inverse), shift_<n> (standalone fftshift of 2^26 points in rows of n; this one
+reports GB/s, as it moves data and computes nothing).
 
 Metric: effective GFLOP/s = 5*N*log2(N) per complex transform (2.5*N*log2(N) per real row,
 2 * 5*n^2*log2(n) per 2-D image) / time, whole job over all ranks.  The JSON line also carries
