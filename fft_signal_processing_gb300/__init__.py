@@ -8,6 +8,10 @@ calls raise instead of computing anything another way.
     from fft_signal_processing_gb300 import Plan, FORWARD, INVERSE
     p = Plan(4096, batch=16384, direction=FORWARD, shift=True)
     y = p.c2c(x)                # x: complex64 CUDA tensor [16384, 4096]
+    Plan(1000, 64).c2c(z)                                   # any length up to 8192
+    Plan(4096, 2048, layout=LAYOUT_REAL_MMAJOR, mmax=1365).r2c(rows)   # band-limited real rows
+    Plan(1024, 1, dims=2, ny=512, direction=INVERSE, normalize=True).c2c(img)  # 512 x 1024
+    shift(y)                                                # standalone fftshift
 """
 import ctypes
 import os
