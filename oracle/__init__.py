@@ -42,6 +42,7 @@ def _lib():
             "oracle_dft_bins": [p, i64, ci, p, i64, p],
             "oracle_fft": [p, i64, i64, ci, p],
             "oracle_fft2d": [p, i64, i64, ci, p],
+            "oracle_fft_any": [p, i64, i64, ci, p],
             "oracle_fftshift": [p, i64, i64, ci, p],
             "oracle_chessboard": [p, i64, i64, ci, p],
             "oracle_roll": [p, i64, i64, i64, i64, i64, p],
@@ -113,6 +114,16 @@ def fft(x, sign=-1):
     n = x.shape[-1]
     out = np.empty_like(x)
     _check(_lib().oracle_fft(_ptr(x), n, x.size // n, int(sign), _ptr(out)), "fft")
+    return out
+
+
+def fft_any(x, sign=-1):
+    """Mixed-radix recursive FFT of every row (last axis), any length N >= 1: radix = the
+    smallest prime factor of N at each level, the direct sum for prime lengths."""
+    x = _c128(x)
+    n = x.shape[-1]
+    out = np.empty_like(x)
+    _check(_lib().oracle_fft_any(_ptr(x), n, x.size // n, int(sign), _ptr(out)), "fft_any")
     return out
 
 

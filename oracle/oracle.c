@@ -225,6 +225,69 @@ int oracle_fft2d(const double* x, int64_t n, int64_t batch, int sign, double* ou
 }
 
 /* ---------------------------------------------------------------------------------------
+ * Mixed-radix recursive decimation in time for any N >= 1: [Mota] §2.3.1 Eq. 9-10 with the
+ * radix p the smallest prime factor of N instead of 2,
+ *   X_k = sum_{r<p} w_N^{r*k} Y_r[k mod N/p],   Y_r = the N/p-point DFT of x_r, x_{r+p}, ...,
+ * and the direct sum of Eq. 5 when N itself is prime.  O(N * sum of the prime factors).
+ * ------------------------------------------------------------------------------------- */
+static int64_t smallest_prime_factor(int64_t n) {
+    if (n % 2 == 0) return 2;
+    for (int64_t p = 3; p * p <= n; p += 2)
+        if (n % p == 0) return p;
+    return n;
+}
+
+static int fft_any_rec(const cplx* x, int64_t stride, int64_t n, int sign, cplx* out) {
+    if (n == 1) {
+        out[0] = x[0];
+        return 0;
+    }
+    const int64_t p = smallest_prime_factor(n), m = n / p;
+    cplx* w = (cplx*)malloc(sizeof(cplx) * (size_t)n);  /* w_n^q, q < n */
+    cplx* sub = (cplx*)malloc(sizeof(cplx) * (size_t)n); /* p transforms of m points */
+    if (!w || !sub) {
+        free(w);
+        free(sub);
+        return -1;
+    }
+    for (int64_t q = 0; q < n; ++q) w[q] = unit_root(sign, q, n);
+    int rc = 0;
+    if (p == n) { /* prime: the direct sum */
+        for (int64_t j = 0; j < n; ++j) sub[j] = x[j * stride];
+    } else {
+        for (int64_t r = 0; r < p && rc == 0; ++r)
+            rc = fft_any_rec(x + r * stride, stride * p, m, sign, sub + r * m);
+    }
+    for (int64_t k = 0; k < n && rc == 0; ++k) {
+        double sre = 0.0, sim = 0.0;
+        for (int64_t r = 0; r < p; ++r) {
+            const cplx y = p == n ? sub[r] : sub[r * m + k % m];
+            const cplx t = cmul(y, w[(int64_t)(((__int128)r * k) % n)]);
+            sre += t.re;
+            sim += t.im;
+        }
+        out[k].re = sre;
+        out[k].im = sim;
+    }
+    free(w);
+    free(sub);
+    return rc;
+}
+
+int oracle_fft_any(const double* x, int64_t n, int64_t batch, int sign, double* out) {
+    if (!x || !out || n < 1 || batch < 1 || (sign != 1 && sign != -1)) return -1;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t b = 0; b < batch; ++b) {
+        if (fft_any_rec((const cplx*)x + b * n, 1, n, sign, (cplx*)out + b * n) != 0) {
+#pragma omp atomic write
+            failed = 1;
+        }
+    }
+    return failed ? -1 : 0;
+}
+
+/* ---------------------------------------------------------------------------------------
  * fftshift by index rotation, [Shift] "What is fftshift?": bin 0 moves to index N/2.
  * For even N the rotation by N/2 is its own inverse, so this is also ifftshift.
  *   dims == 1: every row of length n is rotated by n/2.

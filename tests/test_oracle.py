@@ -262,6 +262,23 @@ def test_rectangular_2d_matches_numpy_and_separability(ny, nx):
     assert rel(oracle.transform(y, +1, 2, True), nx * ny * x) < 1e-13
 
 
+@pytest.mark.parametrize("n", [1, 2, 3, 6, 7, 12, 30, 97, 100, 210, 1000, 1024, 3 * 5 * 7 * 11,
+                               2 * 8191, 60000])
+@pytest.mark.parametrize("sign", [-1, 1])
+def test_mixed_radix_fft_any_length(n, sign):
+    """The mixed-radix FFT against numpy's FFT (a library routine) at composite, prime and
+    power-of-two lengths, against the direct sum at small lengths and against the radix-2
+    recursion at powers of two."""
+    x = crand(2, n)
+    ref = np.fft.fft(x) if sign < 0 else np.fft.ifft(x) * n
+    got = oracle.fft_any(x, sign)
+    assert rel(got, ref) < 1e-12
+    if n <= 210:
+        assert rel(got, oracle.dft(x, sign)) < 1e-12
+    if n & (n - 1) == 0:
+        assert rel(got, oracle.fft(x, sign)) < 1e-13
+
+
 def test_chessboard_values():
     x = np.ones((1, 6), complex)
     np.testing.assert_array_equal(oracle.chessboard(x, 1)[0], [1, -1, 1, -1, 1, -1])
