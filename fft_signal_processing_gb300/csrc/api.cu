@@ -74,7 +74,7 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     if (shift != 0 && shift != 1) return FFT_ERR_INVALID_ARG;
     if (layout != FFT_LAYOUT_C2C && (dims != 1 || shift)) return FFT_ERR_INVALID_ARG;
     const int l = ilog2_exact(n);
-    // lengths that are not powers of two: complex rows up to kMaxBluesteinN only
+    // lengths that are not powers of two: rows (complex or real) up to kMaxBluesteinN only
     const bool any_length = l < 0 && dims == 1 && n >= 3 && n <= kMaxBluesteinN;
     if (l < 0 && !any_length) return FFT_ERR_UNSUPPORTED_SIZE;
     if (shift && (n & 1) && !any_length) return FFT_ERR_INVALID_ARG;
