@@ -8,6 +8,10 @@
 // transforms times w_n^{n2*k1} into the scratch array, pass 2 reads it and writes the N2-point
 // row transforms transposed into the output.  Pass 1 overwrites every scratch element that pass
 // 2 reads, so the scratch never needs clearing between calls.
+//
+// Both kernels bound every device-side wait; a wait that gives up records KERR_WAIT_TIMEOUT in
+// a file-scope error word (sticky until read), which the status form of the call (n == 0)
+// reads and clears after synchronising the caller's stream.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -17,6 +21,7 @@
 #include "fft_kernel.cuh"
 #include "host_tables.h"
 #include "kernels.h"
+#include "tma.cuh"
 
 using namespace gbfft;
 
@@ -28,6 +33,7 @@ static constexpr int kTableFloat2 = 1 << 16;                 // 512 KiB of twidd
 // Every GPU that loads this module holds these until the process exits.
 static __device__ __align__(256) float2 g_scratch[kScratchPoints];
 static __device__ __align__(256) float2 g_tables[kTableFloat2];
+static __device__ int g_err;  // KERR_* of a kernel that gave up, 0 otherwise
 
 namespace {
 
@@ -36,6 +42,7 @@ struct DeviceState {
     bool ready = false;
     float2* scratch = nullptr;  // device address of g_scratch on this device
     float2* tables = nullptr;   // device address of g_tables on this device
+    int* err = nullptr;         // device address of g_err on this device
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -78,6 +85,9 @@ int setup_device(int dev, DeviceState** out) {
         st.scratch = (float2*)p;
         if (cudaGetSymbolAddress(&p, g_tables) != cudaSuccess) return FFT_ERR_CUDA;
         st.tables = (float2*)p;
+        if (cudaGetSymbolAddress(&p, g_err) != cudaSuccess) return FFT_ERR_CUDA;
+        st.err = (int*)p;
+        if (cudaMemset(st.err, 0, sizeof(int)) != cudaSuccess) return FFT_ERR_CUDA;
         if (cudaMemcpy(st.tables, t.data(), t.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
             cudaSuccess)
             return FFT_ERR_CUDA;
@@ -87,10 +97,30 @@ int setup_device(int dev, DeviceState** out) {
     return FFT_OK;
 }
 
+// Status form: wait for the stream, then read and clear this device's error word.
+int query_status(cudaStream_t s) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FFT_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FFT_ERR_CUDA;
+    int* err = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_dev[dev].ready) return FFT_OK;  // nothing ran on this device
+        err = g_dev[dev].err;
+    }
+    int h = 0;
+    if (cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FFT_ERR_CUDA;
+    if (h == 0) return FFT_OK;
+    if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return FFT_ERR_CUDA;
+    return h == KERR_WAIT_TIMEOUT ? FFT_ERR_TIMEOUT : FFT_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int shift,
                                     const void* in, void* out, void* stream) {
+    if (n == 0) return query_status((cudaStream_t)stream);
     if (!in || !out || batch < 1) return FFT_ERR_INVALID_ARG;
     if (direction != FFT_FORWARD && direction != FFT_INVERSE) return FFT_ERR_INVALID_ARG;
     if (shift != 0 && shift != 1) return FFT_ERR_INVALID_ARG;
@@ -116,11 +146,11 @@ extern "C" int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = run_cols(l1, direction, (const float2*)in, st->scratch, batch << l2, l2,
                              st->tables + o.col, (shift && fwd) ? KF_CHESS_LOAD : 0, 0,
-                             st->tables + o.hi, st->tables + o.lo, lowbits, nullptr,
+                             st->tables + o.hi, st->tables + o.lo, lowbits, st->err,
                              2000000000ull, s);
     if (e == cudaSuccess)
         e = run_rows_t(l2, direction, st->scratch, (float2*)out, batch << l1, l1,
-                       st->tables + o.row, (shift && !fwd) ? KF_CHESS_STORE : 0, nullptr,
+                       st->tables + o.row, (shift && !fwd) ? KF_CHESS_STORE : 0, st->err,
                        2000000000ull, s);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }

@@ -241,8 +241,14 @@ int fft_plan_destroy(fft_plan plan);
  * or threads) race and corrupt each other's results; serialise them.  The scratch keeps the
  * last call's contents, and nothing in it needs clearing (every element read is first
  * written by the same call).
+ * Device-side waits are bounded (2 s).  A wait that gives up makes its kernel stop early (the
+ * output is then undefined) and sets a static error word of the library on that device; the
+ * word stays set until read.  The call itself returns before the kernels run, so it cannot
+ * report this: call fft_exec_c2c_noalloc with n == 0 (every other argument but `stream` is
+ * ignored) to synchronise `stream`, read and clear the word, and get FFT_ERR_TIMEOUT if any
+ * earlier call on the current device timed out (FFT_OK otherwise).
  * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_UNSUPPORTED_SIZE, FFT_ERR_MISALIGNED or
- * FFT_ERR_CUDA.
+ * FFT_ERR_CUDA; the status form (n == 0) returns FFT_OK, FFT_ERR_TIMEOUT or FFT_ERR_CUDA.
  */
 int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int shift, const void* in,
                          void* out, void* stream);
