@@ -27,6 +27,7 @@
 #pragma once
 
 #include "fft_kernel.cuh"
+#include "launch_cache.cuh"
 
 namespace gbfft {
 
@@ -147,17 +148,17 @@ cudaError_t launch_bluestein(const void* in, void* out, int64_t nrows, int n, in
                              int mmajor, const float2* chirp, const float2* chirp_out,
                              const float2* bhat, const float2* tw, cudaStream_t stream) {
     auto kern = k_bluestein<C, MODE>;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int, LaunchGeom*) {
+            return C::SMEM_BYTES > 48 * 1024
+                       ? cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)C::SMEM_BYTES)
+                       : cudaSuccess;
+        },
+        &geo);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        if (C::SMEM_BYTES > 48 * 1024)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-    }
     if (2 * (int64_t)n - 1 > C::N) return cudaErrorInvalidValue;
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid <= 0) return cudaSuccess;

@@ -258,25 +258,14 @@ cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log
                             const float2* tw, int flags, int elem_parity, ColsTwiddle twd,
                             int* err, uint64_t limit_ns, cudaStream_t stream) {
     auto kern = k_cols_tma<RC, DIR, TW>;
-    static int configured_dev = -1;
-    static int per_sm = 0, num_sms = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int dev, LaunchGeom* g) {
+            return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
+        },
+        &geo);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RC::C::THREADS,
-                                                              RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        configured_dev = dev;
-    }
     EncodeTiledFn encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const int64_t S = int64_t(1) << log2s;
@@ -295,7 +284,7 @@ cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log
             return cudaErrorInvalidValue;
     }
     const int64_t ntiles = nmat * (S / RC::W);
-    const int64_t resident = (int64_t)per_sm * num_sms;
+    const int64_t resident = (int64_t)geo.per_sm * geo.num_sms;
     const int64_t grid = ntiles < resident ? ntiles : resident;
     if (grid <= 0) return cudaSuccess;
     kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(

@@ -240,15 +240,17 @@ __global__ void __launch_bounds__(C::THREADS)
 // device and instantiation: Tag (the launch configuration) keeps one record per kernel.
 template <class Tag, class K>
 cudaError_t configure_once(K kern, size_t smem) {
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || configured_dev == dev) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e == cudaSuccess) configured_dev = dev;
-    return e;
+    static LaunchCache cache;
+    LaunchGeom geo;
+    return cache.get(
+        [&](int, LaunchGeom*) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            return e == cudaSuccess
+                       ? cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100)
+                       : e;
+        },
+        &geo);
 }
 
 // 2-D tensor map over an m-major spectrum [mmax+1][nrows]: (row, coefficient), box W x BK.

@@ -180,26 +180,15 @@ cudaError_t launch_rows_big(const float2* in, float2* out, int64_t nrows, const 
                             int flags, int row_parity, int* err, uint64_t limit_ns,
                             cudaStream_t stream) {
     auto kern = k_rows_big<RC, DIR>;
-    static int configured_dev = -1;
-    static int per_sm = 0, num_sms = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int dev, LaunchGeom* g) {
+            return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
+        },
+        &geo);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RC::C::THREADS,
-                                                              RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        configured_dev = dev;
-    }
-    const int64_t resident = (int64_t)per_sm * num_sms;
+    const int64_t resident = (int64_t)geo.per_sm * geo.num_sms;
     const int64_t grid = nrows < resident ? nrows : resident;
     if (grid <= 0) return cudaSuccess;
     kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(in, out, nrows, tw, flags,

@@ -161,29 +161,18 @@ cudaError_t launch_rows_tma(const float2* in, float2* out, int64_t nrows, const 
     auto plain = k_rows_tma<RC, DIR, false>;
     auto scaled = k_rows_tma<RC, DIR, true>;
     auto kern = (flags >> KF_SCALE_SHIFT) ? scaled : plain;
-    static int configured_dev = -1;  // attributes and occupancy are per device
-    static int grid_per_sm = 0, num_sms = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;  // attributes and occupancy are per device
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int dev, LaunchGeom* g) {
+            cudaError_t r = setup_persistent(scaled, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
+            return r == cudaSuccess ? setup_persistent(plain, RC::C::THREADS, RC::SMEM_BYTES, dev, g)
+                                    : r;
+        },
+        &geo);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        for (auto k : {plain, scaled}) {
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)RC::SMEM_BYTES);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        }
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&grid_per_sm, plain, RC::C::THREADS,
-                                                              RC::SMEM_BYTES);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (grid_per_sm < 1) return cudaErrorInvalidConfiguration;
-        configured_dev = dev;
-    }
     const int64_t nblocks = (nrows + RC::W - 1) / RC::W;
-    const int64_t resident = (int64_t)grid_per_sm * num_sms;
+    const int64_t resident = (int64_t)geo.per_sm * geo.num_sms;
     const int64_t grid = nblocks < resident ? nblocks : resident;
     if (grid <= 0) return cudaSuccess;
     kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(in, out, nrows, tw, flags, row_parity,

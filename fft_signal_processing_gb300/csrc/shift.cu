@@ -11,6 +11,7 @@
 
 #include "../../include/gbfft.h"
 #include "fft_common.cuh"
+#include "launch_cache.cuh"
 
 namespace gbfft {
 namespace {
@@ -94,13 +95,14 @@ __global__ void __launch_bounds__(kShiftThreads)
 }
 
 unsigned grid_for(int64_t warps_needed) {
-    static int num_sms = 0;
-    if (num_sms == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            num_sms = 1;
-    }
+    static LaunchCache cache;  // the SM count of each device
+    LaunchGeom geo;
+    if (cache.get([](int dev, LaunchGeom* g) {
+            return cudaDeviceGetAttribute(&g->num_sms, cudaDevAttrMultiProcessorCount, dev);
+        },
+                  &geo) != cudaSuccess)
+        geo.num_sms = 1;
+    const int num_sms = geo.num_sms;
     const int64_t blocks = (warps_needed * 32 + kShiftThreads - 1) / kShiftThreads;
     const int64_t cap = (int64_t)num_sms * 8;  // eight CTAs of 256 threads per SM
     return (unsigned)(blocks < cap ? (blocks < 1 ? 1 : blocks) : cap);

@@ -188,25 +188,14 @@ cudaError_t launch_cols_big(const float2* in, float2* out, int64_t nmat, int log
                             const float2* tw, int flags, int elem_parity, ColsTwiddle twd,
                             int* err, uint64_t limit_ns, cudaStream_t stream) {
     auto kern = k_cols_big<RC, DIR, TW>;
-    static int configured_dev = -1;
-    static int per_sm = 0, num_sms = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int dev, LaunchGeom* g) {
+            return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
+        },
+        &geo);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RC::C::THREADS,
-                                                              RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        configured_dev = dev;
-    }
     EncodeTiledFn encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     const int64_t S = int64_t(1) << log2s;
@@ -222,7 +211,7 @@ cudaError_t launch_cols_big(const float2* in, float2* out, int64_t nmat, int log
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int64_t ntiles = nmat * (S / RC::W);
-    const int64_t resident = (int64_t)per_sm * num_sms;
+    const int64_t resident = (int64_t)geo.per_sm * geo.num_sms;
     const int64_t grid = ntiles < resident ? ntiles : resident;
     if (grid <= 0) return cudaSuccess;
     kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(
@@ -348,29 +337,18 @@ cudaError_t launch_rowst_big(const float2* in, float2* out, int64_t nrows, int l
                              const float2* tw, int flags, int* err, uint64_t limit_ns,
                              cudaStream_t stream) {
     auto kern = k_rowst_big<RC, DIR>;
-    static int configured_dev = -1;
-    static int per_sm = 0, num_sms = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static LaunchCache cache;
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int dev, LaunchGeom* g) {
+            return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
+        },
+        &geo);
     if (e != cudaSuccess) return e;
-    if (configured_dev != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RC::C::THREADS,
-                                                              RC::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        configured_dev = dev;
-    }
     const int64_t n1 = int64_t(1) << log2n1;
     if (n1 < RC::W || nrows % n1) return cudaErrorInvalidValue;
     const int64_t nblocks = nrows / RC::W;
-    const int64_t resident = (int64_t)per_sm * num_sms;
+    const int64_t resident = (int64_t)geo.per_sm * geo.num_sms;
     const int64_t grid = nblocks < resident ? nblocks : resident;
     if (grid <= 0) return cudaSuccess;
     kern<<<(unsigned)grid, RC::C::THREADS, RC::SMEM_BYTES, stream>>>(in, out, nrows, log2n1, tw,

@@ -5,6 +5,8 @@
 
 #include <stdint.h>
 
+#include "launch_cache.cuh"
+
 namespace gbfft {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
