@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--impl", default="gbfft", choices=["gbfft", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the K-step timed window until about this long has passed")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the batch per GPU (small profiling captures only)")
     return ap.parse_args()
@@ -118,7 +120,7 @@ class Workload:
             per = 5.0 * n * self.log2n * (2 if self.dims == 2 else 1) * (n if self.dims == 2 else 1)
             ntr = 2 if self.kind == "c2c_rt" else 1
             self.flops = ntr * per * self.batch
-            passes = 1 if (self.dims == 1 and n <= (1 << 14)) else (3 if n >= (1 << 23) else 2)
+            passes = 1 if (self.dims == 1 and n <= (1 << 14)) else 2  # one-pass, or two
             self.min_bytes = ntr * 16 * self.points  # one-pass minimum per transform
             self.pass_bytes = ntr * 16 * self.points * passes
         self.large = self.points * 8 > 2 * L2_BYTES
@@ -137,6 +139,13 @@ class Workload:
         w.large = w.points * 8 > 2 * L2_BYTES
         w.desc += f" (rows overridden to {rows})"
         return w
+
+
+def config_of(w, world):
+    """The workload's `config` object (both arms print the same one)."""
+    return {"workload": w.desc, "n": w.n, "batch_per_gpu": w.batch, "dims": w.dims,
+            "l2": "inputs larger than L2" if w.large else "L2 flushed between steps",
+            "parallelism": f"replicas x{world} (batch sharded, no collective)"}
 
 
 def make_inputs(w, seed):
@@ -170,7 +179,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -352,13 +361,61 @@ def run_reference(args, w):
         "impl": "reference", "metric": metric, "value": value,
         "unit": unit, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": w.desc},
+        "data": "synthetic (seeded)", "config": config_of(w, world),
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def host_link_ceiling(dev, nbytes=512 * 1024 * 1024, reps=3):
+    """Plain pinned-memory copy rates on this machine (GB/s): host->device, device->host, and both
+    at once on two streams (the ceiling of an end-to-end step that streams its input in and its
+    result out).  Best of `reps`, CUDA events."""
+    import torch
+
+    hs = [torch.empty(nbytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ds = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s1)
+            s2.wait_event(e0)
+            fn()
+            e2 = torch.cuda.Event()
+            e2.record(s2)
+            s1.wait_event(e2)
+            e1.record(s1)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            ds[0].copy_(hs[0], non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s1):
+            hs[1].copy_(ds[1], non_blocking=True)
+
+    def both():
+        with torch.cuda.stream(s1):
+            ds[0].copy_(hs[0], non_blocking=True)
+        with torch.cuda.stream(s2):
+            hs[1].copy_(ds[1], non_blocking=True)
+
+    t_h2d, t_d2h, t_both = timed(h2d), timed(d2h), timed(both)
+    del hs, ds
+    return {"h2d_gbs": round(nbytes / (t_h2d * 1e-3) / 1e9, 1),
+            "d2h_gbs": round(nbytes / (t_d2h * 1e-3) / 1e9, 1),
+            "both_directions_gbs": round(2 * nbytes / (t_both * 1e-3) / 1e9, 1),
+            "bytes_each_way": nbytes, "how": "pinned torch copy_, best of 3, CUDA events"}
 
 
 # ---- the library arm --------------------------------------------------------------------------------
@@ -445,25 +502,41 @@ def main():
             one_step()
     torch.cuda.synchronize()
 
-    # timed region: per-step events around every launch (on the launching stream)
+    # Timed region: windows of exactly K steps, each bracketed by a barrier and a device
+    # synchronisation, with events around every launch on the launching stream.  The window is
+    # repeated (the same count on every rank) until about --min-seconds have passed, so that the
+    # clock sampler sees the kernels running; the step time is the median over windows.
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(kernels_per_step + 1)]
            for _ in range(args.steps)]
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     clocks.start()
     time.sleep(0.3)
-    barrier(pg)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for s in range(args.steps):
-            one_step(evs[s])
-    torch.cuda.synchronize()
-    barrier(pg)
+
+    def timed_window():
+        barrier(pg)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for s in range(args.steps):
+                one_step(evs[s])
+        torch.cuda.synchronize()
+        barrier(pg)
+        wall = time.perf_counter() - t0
+        return [[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(kernels_per_step)]
+                for s in range(args.steps)], wall
+
+    windows = [timed_window()]
+    n_windows = int(min(200, max(3, math.ceil(args.min_seconds / max(windows[0][1], 1e-4)))))
+    n_windows = int(max_over_ranks(pg, float(n_windows)))
+    while len(windows) < n_windows:
+        windows.append(timed_window())
     clk = clocks.stop()
-    per_launch = [[evs[s][i].elapsed_time(evs[s][i + 1]) for i in range(kernels_per_step)]
-                  for s in range(args.steps)]
-    step_ms_local = statistics.mean(sum(pl) for pl in per_launch)
+    step_ms_windows = [statistics.mean(sum(pl) for pl in win) for win, _ in windows]
+    step_ms_local = statistics.median(step_ms_windows)
     step_ms = max_over_ranks(pg, step_ms_local)
-    launch_ms = [statistics.mean(pl[i] for pl in per_launch) for i in range(kernels_per_step)]
+    launch_ms = [statistics.median(statistics.mean(pl[i] for pl in win) for win, _ in windows)
+                 for i in range(kernels_per_step)]
+    timed_seconds = sum(wall for _, wall in windows)
 
     gflops, gbs_min = job_rates(w, world, step_ms)
 
@@ -551,11 +624,14 @@ def main():
         ev1.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(pg, ev0.elapsed_time(ev1) / args.steps)
+        link_gbs = round(2 * xh.numel() * xh.element_size() / (e2e_ms * 1e-3) / 1e9, 1)
+        link = host_link_ceiling(dev)
         e2e = {"value": round(w.flops * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
                "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                "d2h_bytes_per_step": int(outh.numel() * outh.element_size()),
                "ms_per_step": round(e2e_ms, 4), "chunks_per_step": nchunk,
-               "h2d_d2h_gbs": round(2 * xh.numel() * xh.element_size() / (e2e_ms * 1e-3) / 1e9, 1)}
+               "h2d_d2h_gbs": link_gbs, "host_link": link,
+               "host_link_frac": round(link_gbs / link["both_directions_gbs"], 3)}
         fwd_c.close()
         if inv_c is not None:
             inv_c.close()
@@ -576,15 +652,17 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded numpy generators)",
-            "config": {"workload": w.desc, "n": w.n, "batch_per_gpu": w.batch, "dims": w.dims,
-                       "l2": "inputs larger than L2" if w.large else "L2 flushed between steps",
-                       "parallelism": f"replicas x{world} (batch sharded, no collective)"},
+            "config": config_of(w, world),
             "hbm_gbs_min_traffic": round(gbs_min, 1),
             "hbm_frac_min_traffic": round(gbs_min / world / peak, 4),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": kper * args.steps,
+            "gpu_launches": kper * args.steps * len(windows),
+            "timed_windows": {"count": len(windows), "steps_each": args.steps,
+                              "seconds": round(timed_seconds, 3),
+                              "ms_per_step_min": round(min(step_ms_windows), 4),
+                              "ms_per_step_max": round(max(step_ms_windows), 4)},
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
