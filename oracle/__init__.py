@@ -258,3 +258,74 @@ def c2r_direct(F, n):
     x = np.empty((rows, n), dtype=np.float64)
     _check(_lib().oracle_c2r_direct(_ptr(F), n, rows, m1 - 1, _ptr(x)), "c2r_direct")
     return x
+
+
+# ---- index maps (what the load and store epilogues do when no arithmetic intervenes) --------
+def fourstep_order(x, n1):
+    """The output order of the four-step decomposition n = n1*N2 + n2, k = k1 + N1*k2 (the
+    CS598 page "Fast Fourier Transform on CPU and GPU", four-step remark): entry (k1, k2) of
+    the [N1][N2] intermediate, held at k1*N2 + k2, is output bin k1 + N1*k2.  For every row."""
+    x = np.asarray(x)
+    n = x.shape[-1]
+    n2 = n // n1
+    return np.ascontiguousarray(
+        np.swapaxes(x.reshape(x.shape[:-1] + (n1, n2)), -1, -2)).reshape(x.shape)
+
+
+def hermitian_half(F, n):
+    """The first n/2 bins X_0..X_{n/2-1} of the Hermitian spectrum a band-limited synthesis
+    builds from F_0..F_mmax (fourier.ts header comment, fftSynthWGSL): X_0 = Re F_0, X_m = F_m
+    for 1 <= m <= mmax, zero above (row-major F)."""
+    F = _c128(F)
+    rows, m1 = F.shape
+    X = np.zeros((rows, n // 2), dtype=np.complex128)
+    k = min(m1, n // 2)
+    X[:, :k] = F[:, :k]
+    X[:, 0] = X[:, 0].real
+    return X
+
+
+def pair_pack(x):
+    """Two real rows per complex row (Mota, "High Performance Fourier Transforms on GPUs with
+    GLSL", §2.6 Eq. 17): y = x_{2p} + i x_{2p+1}; an odd row count pairs the last row with
+    zeros."""
+    x = _f64(x)
+    if x.shape[0] % 2:
+        x = np.concatenate([x, np.zeros((1, x.shape[1]))])
+    return x[0::2] + 1j * x[1::2]
+
+
+def pair_unpack(Y, mmax, rows):
+    """The two real rows' spectra from the transform of their packed row (the unpacking of
+    Mota §2.6 Eq. 18, whose printed form is garbled; this is the form Hermitian symmetry
+    gives): X1_k = (Y_k + conj Y_{n-k})/2, X2_k = (Y_k - conj Y_{n-k})/(2i), k = 0..mmax,
+    as a row-major spectrum of `rows` rows."""
+    Y = _c128(Y)
+    n = Y.shape[-1]
+    k = np.arange(mmax + 1)
+    Yk, Yn = Y[:, k], np.conj(Y[:, (n - k) % n])
+    F = np.empty((2 * Y.shape[0], mmax + 1), dtype=np.complex128)
+    F[0::2] = (Yk + Yn) / 2
+    F[1::2] = (Yk - Yn) / 2j
+    return F[:rows]
+
+
+def pair_assemble(F, n):
+    """The packed spectrum Y_k = X1_k + i X2_k of two real rows, k = 0..n-1, each X the
+    Hermitian extension of a band-limited F (X_0 = Re F_0, X_m = F_m and X_{n-m} = conj F_m
+    for 1 <= m <= mmax, a Nyquist bin m = n/2 real, other bins zero; fourier.ts header
+    comment).  The inverse transform of Y is x1 + i x2 (row-major F; odd row counts pair the
+    last row with zeros)."""
+    F = _c128(F)
+    rows, m1 = F.shape
+    if rows % 2:
+        F = np.concatenate([F, np.zeros((1, m1), dtype=np.complex128)])
+    X = np.zeros((F.shape[0], n), dtype=np.complex128)
+    for m in range(m1):
+        f = F[:, m].copy()
+        if m == 0 or 2 * m == n:
+            f = f.real.astype(np.complex128)
+        X[:, m] = f
+        if m != 0 and 2 * m != n:
+            X[:, n - m] = np.conj(f)
+    return X[0::2] + 1j * X[1::2]

@@ -380,3 +380,48 @@ def test_band_limit_rejected(bad):
     n, mmax = bad
     with pytest.raises(ValueError):
         oracle.r2c(np.zeros((1, n)), mmax)
+
+
+# ---- index maps used by the bit-exact epilogue tests ------------------------------------------
+def test_fourstep_order_is_the_four_step_output_map():
+    """The four-step FFT written out with numpy's FFT (columns, twiddle w_n^{n2*k1}, rows) gives
+    the DFT only when its [N1][N2] result is read through fourstep_order."""
+    rng = np.random.default_rng(40)
+    n1, n2 = 8, 16
+    n = n1 * n2
+    x = rng.standard_normal((3, n)) + 1j * rng.standard_normal((3, n))
+    a = x.reshape(3, n1, n2)
+    y = np.fft.fft(a, axis=1)                                  # over n1, for each n2
+    y *= np.exp(-2j * np.pi * np.outer(np.arange(n1), np.arange(n2)) / n)  # w_n^{k1*n2}
+    z = np.fft.fft(y, axis=2).reshape(3, n)                    # over n2: [k1][k2]
+    np.testing.assert_allclose(oracle.fourstep_order(z, n1), oracle.fft(x), atol=1e-9)
+    assert oracle.fourstep_order(np.arange(8.0)[None], 2).tolist() == [[0, 4, 1, 5, 2, 6, 3, 7]]
+
+
+def test_pair_pack_unpack_gives_both_rows_spectra():
+    rng = np.random.default_rng(41)
+    for rows, n, mmax in ((5, 64, 32), (4, 60, 20), (1, 16, 3)):
+        x = rng.standard_normal((rows, n))
+        Y = oracle.fft_any(oracle.pair_pack(x), -1)
+        np.testing.assert_allclose(oracle.pair_unpack(Y, mmax, rows),
+                                   np.fft.fft(x)[:, :mmax + 1], atol=1e-9)
+
+
+def test_pair_assemble_synthesises_both_rows():
+    rng = np.random.default_rng(42)
+    for rows, n, mmax in ((5, 64, 32), (4, 60, 30), (3, 64, 10)):
+        F = rng.standard_normal((rows, mmax + 1)) + 1j * rng.standard_normal((rows, mmax + 1))
+        y = oracle.fft_any(oracle.pair_assemble(F, n), +1)
+        x = np.empty((2 * y.shape[0], n))
+        x[0::2], x[1::2] = y.real, y.imag
+        np.testing.assert_allclose(x[:rows], oracle.c2r_direct(F, n), atol=1e-9)
+
+
+def test_hermitian_half_is_the_lower_half_of_the_synthesis_spectrum():
+    rng = np.random.default_rng(43)
+    n, mmax = 32, 12
+    F = rng.standard_normal((3, mmax + 1)) + 1j * rng.standard_normal((3, mmax + 1))
+    Y = oracle.pair_assemble(F[:1], n)  # a row paired with zeros: Y = X of that row
+    np.testing.assert_array_equal(oracle.hermitian_half(F, n)[:1], Y[:, :n // 2])
+    assert oracle.hermitian_half(F, n)[0, 0].imag == 0
+    assert np.all(oracle.hermitian_half(F[:, :3], n)[:, 3:] == 0)
