@@ -8,7 +8,7 @@ calls raise instead of computing anything another way.
     from fft_signal_processing_gb300 import Plan, FORWARD, INVERSE
     p = Plan(4096, batch=16384, direction=FORWARD, shift=True)
     y = p.c2c(x)                # x: complex64 CUDA tensor [16384, 4096]
-    Plan(1000, 64).c2c(z)                                   # any length up to 8192
+    Plan(1000, 64).c2c(z)                                   # any length up to 2^20
     Plan(4096, 2048, layout=LAYOUT_REAL_MMAJOR, mmax=1365).r2c(rows)   # band-limited real rows
     Plan(1024, 1, dims=2, ny=512, direction=INVERSE, normalize=True).c2c(img)  # 512 x 1024
     shift(y)                                                # standalone fftshift
@@ -38,7 +38,8 @@ ABI_SYMBOLS = (
     "fft_plan_describe", "fft_plan_query", "fft_exec_c2c", "fft_exec_r2c", "fft_exec_c2r",
     "fft_plan_check", "fft_plan_destroy", "fft_status_string", "fft_version",
     "fft_exec_c2c_noalloc", "fft_plan_set_wait_timeout", "fft_shift", "fft_plan_create_2d",
-    "fft_plan_query_2d", "fft_plan_set_normalization",
+    "fft_plan_query_2d", "fft_plan_set_normalization", "fft_plan_set_real_pairing",
+    "fft_plan_set_diagnostic",
 )
 
 _LIB = None
@@ -63,6 +64,8 @@ def lib():
         L.fft_plan_create.argtypes = [i64, i64, ci, ci, ci, ci, ctypes.POINTER(vp)]
         L.fft_plan_set_band_limit.argtypes = [vp, i64]
         L.fft_plan_set_normalization.argtypes = [vp, ci]
+        L.fft_plan_set_real_pairing.argtypes = [vp, ci]
+        L.fft_plan_set_diagnostic.argtypes = [vp, ci]
         L.fft_plan_workspace_bytes.argtypes = [vp, ctypes.POINTER(sz)]
         L.fft_plan_describe.argtypes = [vp, ctypes.c_char_p, sz]
         L.fft_plan_query.argtypes = [i64, i64, ci, ci, ci, ci, ctypes.c_char_p, sz]
@@ -154,11 +157,12 @@ class Plan:
     up to 4096, rows of n points then columns of ny points).  direction: FORWARD / INVERSE,
     unnormalised.  layout: LAYOUT_C2C, or LAYOUT_REAL_ROWMAJOR / LAYOUT_REAL_MMAJOR for the
     band-limited real-row analysis (FORWARD, r2c) / synthesis (INVERSE, c2r) with mmax.
-    shift: fftshift folded in as the (-1)^j chessboard (C2C only).
+    shift: fftshift folded in as the (-1)^j chessboard (C2C only).  pairing: real layouts only,
+    two real rows per complex transform (fft_plan_set_real_pairing).
     """
 
     def __init__(self, n, batch=1, dims=1, direction=FORWARD, layout=LAYOUT_C2C, shift=False,
-                 mmax=None, ny=None, normalize=False):
+                 mmax=None, ny=None, normalize=False, pairing=False):
         self.n, self.batch, self.dims = int(n), int(batch), int(dims)
         self.direction, self.layout, self.shift = int(direction), int(layout), bool(shift)
         self.ny = (self.n if ny is None else int(ny)) if self.dims == 2 else 1
@@ -177,6 +181,8 @@ class Plan:
         if layout != LAYOUT_C2C:
             self.mmax = (self.n - 1) // 2 if mmax is None else int(mmax)
             _check(lib().fft_plan_set_band_limit(self._h, self.mmax), "fft_plan_set_band_limit")
+        if pairing:
+            _check(lib().fft_plan_set_real_pairing(self._h, 1), "fft_plan_set_real_pairing")
 
     @property
     def handle(self):
@@ -199,6 +205,11 @@ class Plan:
         """Scale the output by 1/n (1/(nx*ny) for 2-D), or not (the default)."""
         _check(lib().fft_plan_set_normalization(self._h, int(bool(on))),
                "fft_plan_set_normalization")
+
+    def set_index_only(self, on: bool = True):
+        """Test hook: the kernels move values through their load/store epilogues only
+        (fft_plan_set_diagnostic with FFT_DIAG_INDEX_ONLY)."""
+        _check(lib().fft_plan_set_diagnostic(self._h, 1 if on else 0), "fft_plan_set_diagnostic")
 
     def set_wait_timeout(self, ns: int):
         """Limit of every device-side wait of this plan's kernels (0: give up at once)."""

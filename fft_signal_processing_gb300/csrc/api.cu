@@ -40,7 +40,14 @@ using namespace gbfft;
 
 namespace {
 
-enum Path { PATH_ONEPASS = 0, PATH_FOURSTEP = 1, PATH_2D = 2, PATH_REAL = 3, PATH_BLUESTEIN = 4 };
+enum Path {
+    PATH_ONEPASS = 0,
+    PATH_FOURSTEP = 1,
+    PATH_2D = 2,
+    PATH_REAL = 3,
+    PATH_BLUESTEIN = 4,
+    PATH_BLUESTEIN_MP = 5,  // any length above kMaxBluesteinN: chirp-z over four-step passes
+};
 
 struct PlanSpec {
     int64_t n = 0, batch = 0;
@@ -74,8 +81,8 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     if (shift != 0 && shift != 1) return FFT_ERR_INVALID_ARG;
     if (layout != FFT_LAYOUT_C2C && (dims != 1 || shift)) return FFT_ERR_INVALID_ARG;
     const int l = ilog2_exact(n);
-    // lengths that are not powers of two: rows (complex or real) up to kMaxBluesteinN only
-    const bool any_length = l < 0 && dims == 1 && n >= 3 && n <= kMaxBluesteinN;
+    // lengths that are not powers of two: rows (complex or real) up to kMaxBluesteinMpN
+    const bool any_length = l < 0 && dims == 1 && n >= 3 && n <= kMaxBluesteinMpN;
     if (l < 0 && !any_length) return FFT_ERR_UNSUPPORTED_SIZE;
     if (shift && (n & 1) && !any_length) return FFT_ERR_INVALID_ARG;
     PlanSpec s;
@@ -87,8 +94,11 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     s.shift = shift;
     s.log2n = l;
     if (any_length) {
-        s.path = PATH_BLUESTEIN;
+        s.path = n <= kMaxBluesteinN ? PATH_BLUESTEIN : PATH_BLUESTEIN_MP;
         s.log2m = bluestein_log2m(n);
+        s.log2n1 = s.log2m / 2;  // four-step split of the m-point transforms (multi-pass)
+        s.log2n2 = s.log2m - s.log2m / 2;
+        s.lowbits = (s.log2m + 1) / 2;
     } else if (layout != FFT_LAYOUT_C2C) {
         static_assert(FFT_MAX_LOG2N_REAL == kMaxLog2RealH + 1, "header and kernels agree");
         if (l < 2 || l > FFT_MAX_LOG2N_REAL) return FFT_ERR_UNSUPPORTED_SIZE;
@@ -184,7 +194,7 @@ Geo real_geo(int lh) {
     return {(1 << real_log2t(lh)) << w, 1 << w, (size_t)slots * (1u << w) * 8u};
 }
 
-std::string describe_spec(const PlanSpec& s, int64_t mmax) {
+std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
     char buf[512];
     const char* dir = s.direction < 0 ? "forward" : "inverse";
     switch (s.path) {
@@ -220,12 +230,29 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
             else
                 snprintf(what, sizeof what, "%s shift=%d", dir, s.shift);
             snprintf(buf, sizeof buf,
-                     "path=bluestein n=%lld batch=%lld %s m=%d radix=%s kernels=1 "
+                     "path=bluestein n=%lld batch=%lld %s%s m=%d radix=%s kernels=1 "
                      "threads=%d rows_per_cta=%d smem=%zu",
-                     (long long)s.n, (long long)s.batch, what, 1 << s.log2m,
+                     (long long)s.n, (long long)s.batch, what,
+                     real && real_pair ? " rows_per_transform=2" : "", 1 << s.log2m,
                      radix_string(s.log2m, rows_maxrb(s.log2m)).c_str(),
                      (1 << rows_log2t(s.log2m)) << w, 1 << w,
                      padded_bytes(s.log2m, rows_maxrb(s.log2m), w));
+            break;
+        }
+        case PATH_BLUESTEIN_MP: {
+            const bool real = s.layout != FFT_LAYOUT_C2C;
+            char what[128];
+            if (real)
+                snprintf(what, sizeof what, "%s mmax=%lld layout=%s rows_per_transform=2",
+                         s.direction < 0 ? "analysis(r2c)" : "synthesis(c2r)", (long long)mmax,
+                         s.layout == FFT_LAYOUT_REAL_MMAJOR ? "mmajor" : "rowmajor");
+            else
+                snprintf(what, sizeof what, "%s shift=%d", dir, s.shift);
+            snprintf(buf, sizeof buf,
+                     "path=bluestein_multipass n=%lld batch=%lld %s m=%d n1=%d n2=%d kernels=7 "
+                     "(chirp, fourstep fwd x2, filter, fourstep inv x2, chirp)",
+                     (long long)s.n, (long long)s.batch, what, 1 << s.log2m, 1 << s.log2n1,
+                     1 << s.log2n2);
             break;
         }
         case PATH_2D: {  // ny x n images: n-point rows, then ny-point columns
@@ -241,6 +268,22 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax) {
             break;
         }
         default: {
+            if (real_pair) {  // two rows per n-point complex transform
+                const int l = s.log2n, w = rows_log2w(l), lp = sched_rbits(l, rows_maxrb(l), 0);
+                const size_t slots = std::max(
+                    (size_t)(sched_npass(l, rows_maxrb(l)) > 1 ? spad_size(1 << l, lp) : 0),
+                    (size_t)1 << l);
+                snprintf(buf, sizeof buf,
+                         "path=real n=%lld batch=%lld %s mmax=%lld layout=%s core=%lld "
+                         "rows_per_transform=2 radix=%s kernels=1 threads=%d pairs_per_cta=%d "
+                         "smem=%zu",
+                         (long long)s.n, (long long)s.batch,
+                         s.direction < 0 ? "analysis(r2c)" : "synthesis(c2r)", (long long)mmax,
+                         s.layout == FFT_LAYOUT_REAL_MMAJOR ? "mmajor" : "rowmajor",
+                         (long long)s.n, radix_string(l, rows_maxrb(l)).c_str(),
+                         (1 << rows_log2t(l)) << w, 1 << w, (slots << w) * 8u);
+                break;
+            }
             Geo g = real_geo(s.log2n - 1);
             snprintf(buf, sizeof buf,
                      "path=real n=%lld batch=%lld %s mmax=%lld layout=%s core=%lld radix=%s "
@@ -277,12 +320,15 @@ struct gbfft_plan_s {
     float2* d_tw = nullptr;
     size_t tw_count = 0;
     size_t off_a = 0, off_b = 0, off_hi = 0, off_lo = 0, off_r = 0;
+    size_t off_pair = 0;  // real plans: pass tables of the n-point complex core (pairing)
     size_t off_chirp = 0, off_chirp_out = 0, off_bhat = 0;  // chirp-z tables
     void* d_work = nullptr;
     size_t work_bytes = 0;
     int* d_err = nullptr;
     uint64_t wait_limit_ns = 2000000000ull;  // bounded device waits: 2 s
     int normalize = 0;                       // 1: output scaled by 1/n (1/(nx*ny) for 2-D)
+    int real_pair = 0;                       // 1: two real rows per complex transform
+    int index_only = 0;                      // diagnostic: epilogues only (fft_plan_set_diagnostic)
 };
 
 static void free_plan(gbfft_plan_s* p) {
@@ -396,9 +442,29 @@ static int create_from_spec(const PlanSpec& s, fft_plan* out) {
             }
             p->off_bhat = host::append_chirp_filter(tw, s.n, int64_t(1) << s.log2m, s.direction);
             break;
+        case PATH_BLUESTEIN_MP: {
+            p->off_a = append_pass_tables(tw, s.log2n1, cols_pass_maxrb(s.log2n1, s.log2n2));
+            p->off_b = append_pass_tables(tw, s.log2n2, rowst_maxrb(s.log2n2));
+            const int64_t m = int64_t(1) << s.log2m;
+            const int64_t nlo = int64_t(1) << s.lowbits, nhi = int64_t(1) << (s.log2m - s.lowbits);
+            p->off_hi = append_roots(tw, nhi, nlo, m);  // w_m^{qh * 2^lowbits}
+            p->off_lo = append_roots(tw, nlo, 1, m);    // w_m^{ql}
+            const int64_t h = s.n / 2;
+            const bool fwd = s.direction == FFT_FORWARD;
+            const bool c2c = s.layout == FFT_LAYOUT_C2C;
+            p->off_chirp = host::append_chirp(tw, s.n, s.direction, c2c && s.shift && fwd ? h : 0);
+            p->off_chirp_out =
+                host::append_chirp(tw, s.n, s.direction, c2c && s.shift && !fwd ? -h : 0);
+            p->off_bhat = host::append_chirp_filter(tw, s.n, m, s.direction);
+            const int64_t ntr = c2c ? s.batch : (s.batch + 1) / 2;
+            p->work_bytes = 2 * (size_t)ntr * (size_t)m * sizeof(float2);  // A and B
+            break;
+        }
         case PATH_REAL:
             p->off_a = append_pass_tables(tw, s.log2n - 1, real_maxrb(s.log2n - 1));
             p->off_r = append_roots(tw, s.n / 2, 1, s.n);  // w_n^k, k < n/2
+            if (s.log2n <= kMaxLog2RealPair)  // n-point core of the two-rows-per-transform option
+                p->off_pair = append_pass_tables(tw, s.log2n, rows_maxrb(s.log2n));
             break;
     }
     align_table(tw);
@@ -424,7 +490,7 @@ int fft_plan_set_normalization(fft_plan p, int normalize) {
     if (!p || p->s.layout != FFT_LAYOUT_C2C || (normalize != 0 && normalize != 1))
         return FFT_ERR_INVALID_ARG;
     const PlanSpec& s = p->s;
-    if (s.path == PATH_BLUESTEIN && normalize != p->normalize) {
+    if ((s.path == PATH_BLUESTEIN || s.path == PATH_BLUESTEIN_MP) && normalize != p->normalize) {
         // the chirp of the store, times 1/n when normalising (rewritten in place)
         std::vector<float2> t;
         const bool fwd = s.direction == FFT_FORWARD;
@@ -446,6 +512,36 @@ int fft_plan_set_band_limit(fft_plan p, int64_t mmax) {
     return FFT_OK;
 }
 
+int fft_plan_set_real_pairing(fft_plan p, int pairing) {
+    if (!p || p->s.layout == FFT_LAYOUT_C2C || (pairing != 0 && pairing != 1))
+        return FFT_ERR_INVALID_ARG;
+    if (pairing && p->s.path == PATH_REAL && p->s.log2n > kMaxLog2RealPair)
+        return FFT_ERR_UNSUPPORTED_SIZE;
+    p->real_pair = pairing;
+    return FFT_OK;
+}
+
+// The (path, size) combinations whose kernels carry the index-only diagnostic.
+static bool index_only_supported(const gbfft_plan_s* p) {
+    const PlanSpec& s = p->s;
+    switch (s.path) {
+        case PATH_ONEPASS: return s.log2n == 12;
+        case PATH_FOURSTEP: return s.log2n == 15;
+        case PATH_REAL: return p->real_pair ? s.log2n == 12 : (s.log2n == 12 || s.log2n == 15);
+        default: return false;
+    }
+}
+
+int fft_plan_set_diagnostic(fft_plan p, int mode) {
+    if (!p || (mode != 0 && mode != FFT_DIAG_INDEX_ONLY)) return FFT_ERR_INVALID_ARG;
+    p->index_only = mode == FFT_DIAG_INDEX_ONLY;
+    if (p->index_only && !index_only_supported(p)) {
+        p->index_only = 0;
+        return FFT_ERR_UNSUPPORTED_SIZE;
+    }
+    return FFT_OK;
+}
+
 int fft_plan_set_wait_timeout(fft_plan p, uint64_t ns) {
     if (!p) return FFT_ERR_INVALID_ARG;
     p->wait_limit_ns = ns;
@@ -460,9 +556,28 @@ int fft_plan_workspace_bytes(fft_plan p, size_t* bytes) {
 
 int fft_plan_describe(fft_plan p, char* buf, size_t len) {
     if (!p || !buf || !len) return FFT_ERR_INVALID_ARG;
-    std::string d = describe_spec(p->s, p->mmax);
+    std::string d = describe_spec(p->s, p->mmax, p->real_pair);
     snprintf(buf, len, "%s", d.c_str());
     return FFT_OK;
+}
+
+static cudaError_t exec_chirp_mp(fft_plan p, int mode, const void* in, void* out,
+                                 cudaStream_t st) {
+    const PlanSpec& s = p->s;
+    ChirpMpTables t;
+    t.chirp = p->d_tw + p->off_chirp;
+    t.chirp_out = p->d_tw + p->off_chirp_out;
+    t.bhat = p->d_tw + p->off_bhat;
+    t.tw_cols = p->d_tw + p->off_a;
+    t.tw_rows = p->d_tw + p->off_b;
+    t.hi = p->d_tw + p->off_hi;
+    t.lo = p->d_tw + p->off_lo;
+    t.lowbits = s.lowbits;
+    float2* A = (float2*)p->d_work;
+    float2* B = A + p->work_bytes / (2 * sizeof(float2));
+    return run_bluestein_mp(mode, in, out, s.batch, (int)s.n, s.log2m, (int)p->mmax,
+                            s.layout == FFT_LAYOUT_REAL_MMAJOR, t, A, B, p->d_err,
+                            p->wait_limit_ns, st);
 }
 
 int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
@@ -476,11 +591,13 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
     const float2* x = (const float2*)in;
     float2* y = (float2*)out;
     const bool fwd = s.direction == FFT_FORWARD;
+    if (p->index_only && !index_only_supported(p)) return FFT_ERR_UNSUPPORTED_SIZE;
+    const int diag = p->index_only ? KF_INDEX_ONLY : 0;
     cudaError_t e = cudaSuccess;
     switch (s.path) {
         case PATH_ONEPASS: {
             const int flags = (s.shift ? (fwd ? KF_CHESS_LOAD : KF_CHESS_STORE) : 0) |
-                              (p->normalize ? kf_scale(s.log2n) : 0);
+                              (p->normalize ? kf_scale(s.log2n) : 0) | diag;
             e = run_rows(s.log2n, s.direction, x, y, s.batch, p->d_tw + p->off_a, flags, 0,
                          p->d_err, p->wait_limit_ns, st);
             break;
@@ -491,18 +608,21 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                               p->d_tw + p->off_a, st);
             break;
         }
+        case PATH_BLUESTEIN_MP:  // in == out is fine: the input is read into the workspace first
+            e = exec_chirp_mp(p, 0, x, y, st);
+            break;
         case PATH_FOURSTEP: {
             float2* wk = (float2*)p->d_work;
             const int64_t n1 = int64_t(1) << s.log2n1, n2 = int64_t(1) << s.log2n2;
             e = run_cols(s.log2n1, s.direction, x, wk, s.batch * n2, s.log2n2,
-                         p->d_tw + p->off_a, (s.shift && fwd) ? KF_CHESS_LOAD : 0, 0,
+                         p->d_tw + p->off_a, ((s.shift && fwd) ? KF_CHESS_LOAD : 0) | diag, 0,
                          p->d_tw + p->off_hi, p->d_tw + p->off_lo, s.lowbits, p->d_err,
                          p->wait_limit_ns, st);
             if (e == cudaSuccess)
                 e = run_rows_t(s.log2n2, s.direction, wk, y, s.batch * n1, s.log2n1,
                                p->d_tw + p->off_b,
                                ((s.shift && !fwd) ? KF_CHESS_STORE : 0) |
-                                   (p->normalize ? kf_scale(s.log2n) : 0),
+                                   (p->normalize ? kf_scale(s.log2n) : 0) | diag,
                                p->d_err, p->wait_limit_ns, st);
             break;
         }
@@ -532,13 +652,22 @@ int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
     const size_t out_bytes = (size_t)s.batch * (size_t)(p->mmax + 1) * 8u;
     if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
     const int mmajor = s.layout == FFT_LAYOUT_REAL_MMAJOR;
-    cudaError_t e =
-        s.path == PATH_BLUESTEIN
-            ? run_bluestein(s.log2m, 1, in, out, s.batch, (int)s.n, (int)p->mmax, mmajor,
-                            p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
-                            p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream)
-            : run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax, mmajor,
-                      p->d_tw + p->off_a, p->d_tw + p->off_r, p->d_err, (cudaStream_t)stream);
+    if (p->index_only && !index_only_supported(p)) return FFT_ERR_UNSUPPORTED_SIZE;
+    const int diag = p->index_only ? KF_INDEX_ONLY : 0;
+    cudaError_t e;
+    if (s.path == PATH_BLUESTEIN_MP)
+        e = exec_chirp_mp(p, 3, in, out, (cudaStream_t)stream);
+    else if (s.path == PATH_BLUESTEIN)
+        e = run_bluestein(s.log2m, p->real_pair ? 3 : 1, in, out, s.batch, (int)s.n,
+                          (int)p->mmax, mmajor, p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
+                          p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream);
+    else if (p->real_pair)
+        e = run_real_pair(s.log2n, true, in, out, s.batch, (int)p->mmax, mmajor,
+                          p->d_tw + p->off_pair, diag, (cudaStream_t)stream);
+    else
+        e = run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax, mmajor,
+                    p->d_tw + p->off_a, p->d_tw + p->off_r, diag, p->d_err,
+                    (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
 
@@ -551,14 +680,22 @@ int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
     const size_t out_bytes = (size_t)s.batch * (size_t)s.n * 4u;
     if (ranges_overlap(in, in_bytes, out, out_bytes)) return FFT_ERR_INVALID_ARG;
     const int mmajor = s.layout == FFT_LAYOUT_REAL_MMAJOR;
-    cudaError_t e =
-        s.path == PATH_BLUESTEIN
-            ? run_bluestein(s.log2m, 2, in, out, s.batch, (int)s.n, (int)p->mmax, mmajor,
-                            p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
-                            p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream)
-            : run_c2r(s.log2n - 1, (const float2*)in, out, s.batch, (int)p->mmax, mmajor,
-                      p->d_tw + p->off_a, p->d_tw + p->off_r, p->d_err, p->wait_limit_ns,
-                      (cudaStream_t)stream);
+    if (p->index_only && !index_only_supported(p)) return FFT_ERR_UNSUPPORTED_SIZE;
+    const int diag = p->index_only ? KF_INDEX_ONLY : 0;
+    cudaError_t e;
+    if (s.path == PATH_BLUESTEIN_MP)
+        e = exec_chirp_mp(p, 4, in, out, (cudaStream_t)stream);
+    else if (s.path == PATH_BLUESTEIN)
+        e = run_bluestein(s.log2m, p->real_pair ? 4 : 2, in, out, s.batch, (int)s.n,
+                          (int)p->mmax, mmajor, p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
+                          p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream);
+    else if (p->real_pair)
+        e = run_real_pair(s.log2n, false, in, out, s.batch, (int)p->mmax, mmajor,
+                          p->d_tw + p->off_pair, diag, (cudaStream_t)stream);
+    else
+        e = run_c2r(s.log2n - 1, (const float2*)in, out, s.batch, (int)p->mmax, mmajor,
+                    p->d_tw + p->off_a, p->d_tw + p->off_r, diag, p->d_err, p->wait_limit_ns,
+                    (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
 

@@ -24,6 +24,11 @@
 // part and stores F_m, m <= mmax, into the row-major or m-major spectrum; synthesis (BLU_C2R)
 // assembles the Hermitian spectrum on the load (X_0 = Re F_0, X_m = F_m, X_{n-m} = conj F_m
 // for 1 <= m <= mmax, other bins 0) and stores the real part of the inverse transform.
+// BLU_R2C2 / BLU_C2R2 take two real rows per transform instead (Mota, "High Performance Fourier
+// Transforms on GPUs with GLSL", §2.6 Eq. 17-18): analysis transforms y = x1 + i x2 and unpacks
+// X1_k = (Y_k + conj Y_{n-k})/2, X2_k = (Y_k - conj Y_{n-k})/(2i) through shared memory;
+// synthesis assembles Y_k = X1_k + i X2_k from both Hermitian spectra and stores Re y and Im y.
+// Half the transforms of the one-row modes, for the same outputs.
 #pragma once
 
 #include "fft_kernel.cuh"
@@ -31,7 +36,14 @@
 
 namespace gbfft {
 
-enum : int { BLU_C2C = 0, BLU_R2C = 1, BLU_C2R = 2 };
+enum : int { BLU_C2C = 0, BLU_R2C = 1, BLU_C2R = 2, BLU_R2C2 = 3, BLU_C2R2 = 4 };
+
+// Shared-memory slots per transform: the padded exchange, and for the two-row analysis the
+// n outputs that the unpack reads.
+template <class C, int MODE>
+__host__ __device__ constexpr int blu_slots() {
+    return MODE == BLU_R2C2 ? (C::SROW > C::N ? C::SROW : C::N) : C::SROW;
+}
 
 template <class C, int MODE>
 __global__ void __launch_bounds__(C::THREADS)
@@ -39,12 +51,18 @@ __global__ void __launch_bounds__(C::THREADS)
                 const float2* __restrict__ chirp, const float2* __restrict__ chirp_out,
                 const float2* __restrict__ bhat, const float2* __restrict__ tw) {
     static_assert(C::TFAST, "a row's threads are adjacent lanes (coalesced row accesses)");
+    constexpr bool PAIR = MODE == BLU_R2C2 || MODE == BLU_C2R2;
+    constexpr int SLOTS = blu_slots<C, MODE>();
     extern __shared__ float2 smem[];
     const int w = (int)threadIdx.x / C::T;
     const int t = (int)threadIdx.x % C::T;
+    // one-row modes: transform `row` is row `row`; two-row modes: rows 2*row and 2*row + 1 of
+    // the nrows real rows (the second absent when nrows is odd)
     const int64_t row = (int64_t)blockIdx.x * C::W + w;
-    const bool active = row < nrows;
-    float2* sb = smem + w * C::SROW;
+    const int64_t ntr = PAIR ? (nrows + 1) / 2 : nrows;
+    const bool active = row < ntr;
+    const bool has2 = PAIR && 2 * row + 1 < nrows;
+    float2* sb = smem + w * SLOTS;
 
     constexpr int R0 = C::radix(0);
     constexpr int B0 = C::E / R0;
@@ -59,6 +77,27 @@ __global__ void __launch_bounds__(C::THREADS)
             return ldg_stream(static_cast<const float2*>(in_) + row * n + e);
         } else if constexpr (MODE == BLU_R2C) {
             return make_float2(__ldcs(static_cast<const float*>(in_) + row * n + e), 0.f);
+        } else if constexpr (MODE == BLU_R2C2) {  // y = x1 + i x2
+            const float* x = static_cast<const float*>(in_) + 2 * row * n + e;
+            return make_float2(__ldcs(x), has2 ? __ldcs(x + n) : 0.f);
+        } else if constexpr (MODE == BLU_C2R2) {  // Y_e = X1_e + i X2_e
+            const float2* F = static_cast<const float2*>(in_);
+            if (e > mmax && e < n - mmax) return make_float2(0.f, 0.f);
+            const int m = e <= mmax ? e : n - e;
+            const int64_t r1 = 2 * row;
+            float2 f1 = ldg_stream(F + (mmajor ? (int64_t)m * nrows + r1 : r1 * (mmax + 1) + m));
+            float2 f2 = make_float2(0.f, 0.f);
+            if (has2)
+                f2 = ldg_stream(F + (mmajor ? (int64_t)m * nrows + r1 + 1
+                                            : (r1 + 1) * (mmax + 1) + m));
+            if (e == 0 || 2 * e == n) {  // X_0 and a Nyquist bin: real
+                f1.y = 0.f;
+                f2.y = 0.f;
+            } else if (e > mmax) {  // mirrored bin: conj
+                f1.y = -f1.y;
+                f2.y = -f2.y;
+            }
+            return make_float2(f1.x - f2.y, f1.y + f2.x);
         } else {
             const float2* F = static_cast<const float2*>(in_);
             const int m = e <= mmax ? e : n - e;  // bins above n - mmax mirror m = n - e
@@ -116,6 +155,39 @@ __global__ void __launch_bounds__(C::THREADS)
 
     run_passes<C, +1, 0>(v, t, sb, tw);  // conv = IFFT_m(A * bhat)
 
+    if constexpr (MODE == BLU_R2C2) {
+        // Y_k = c_k conv_k for k < n into shared memory, then the unpack of both rows
+        if constexpr (C::NPASS > 1) __syncthreads();  // the last exchange has been read
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < RL; ++r) {
+                const int k = j + r * SL;
+                if (k < n) sb[k] = cmul(v[b * RL + r], __ldg(chirp_out + k));
+            }
+        }
+        __syncthreads();
+        if (active) {
+            float2* F = static_cast<float2*>(out_);
+            const int64_t r1 = 2 * row;
+            for (int m = t; m <= mmax; m += C::T) {
+                const float2 ym = sb[m], yn = sb[m == 0 ? 0 : n - m];
+                float2 f1 = make_float2(0.5f * (ym.x + yn.x), 0.5f * (ym.y - yn.y));
+                float2 f2 = make_float2(0.5f * (ym.y + yn.y), 0.5f * (yn.x - ym.x));
+                if (m == 0 || 2 * m == n) {  // real bins: drop the rounding residue
+                    f1.y = 0.f;
+                    f2.y = 0.f;
+                }
+                stg_stream(F + (mmajor ? (int64_t)m * nrows + r1 : r1 * (mmax + 1) + m), f1);
+                if (has2)
+                    stg_stream(F + (mmajor ? (int64_t)m * nrows + r1 + 1
+                                           : (r1 + 1) * (mmax + 1) + m),
+                               f2);
+            }
+        }
+        return;
+    }
     const int kend = MODE == BLU_R2C ? mmax + 1 : n;  // outputs kept
     if (active) {
 #pragma unroll
@@ -134,6 +206,10 @@ __global__ void __launch_bounds__(C::THREADS)
                         stg_stream(static_cast<float2*>(out_) +
                                        (mmajor ? (int64_t)k * nrows + row : row * (mmax + 1) + k),
                                    f);
+                    } else if constexpr (MODE == BLU_C2R2) {
+                        float* x = static_cast<float*>(out_) + 2 * row * n + k;
+                        __stcs(x, y.x);
+                        if (has2) __stcs(x + n, y.y);
                     } else {
                         __stcs(static_cast<float*>(out_) + row * n + k, y.x);
                     }
@@ -148,23 +224,26 @@ cudaError_t launch_bluestein(const void* in, void* out, int64_t nrows, int n, in
                              int mmajor, const float2* chirp, const float2* chirp_out,
                              const float2* bhat, const float2* tw, cudaStream_t stream) {
     auto kern = k_bluestein<C, MODE>;
+    constexpr size_t smem = (size_t)blu_slots<C, MODE>() * C::W * sizeof(float2);
     static LaunchCache cache;
     LaunchGeom geo;
     cudaError_t e = cache.get(
         [&](int, LaunchGeom*) {
-            return C::SMEM_BYTES > 48 * 1024
+            return smem > 48 * 1024
                        ? cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)C::SMEM_BYTES)
+                                              (int)smem)
                        : cudaSuccess;
         },
         &geo);
     if (e != cudaSuccess) return e;
     if (2 * (int64_t)n - 1 > C::N) return cudaErrorInvalidValue;
-    const int64_t grid = (nrows + C::W - 1) / C::W;
+    const bool pair = MODE == BLU_R2C2 || MODE == BLU_C2R2;
+    const int64_t ntr = pair ? (nrows + 1) / 2 : nrows;  // transforms
+    const int64_t grid = (ntr + C::W - 1) / C::W;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, stream>>>(in, out, nrows, n, mmax, mmajor,
-                                                                  chirp, chirp_out, bhat, tw);
+    kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, n, mmax, mmajor, chirp,
+                                                       chirp_out, bhat, tw);
     return cudaGetLastError();
 }
 

@@ -101,7 +101,9 @@ __device__ __forceinline__ float2 root2(const ColsTwiddle& t, uint32_t q, uint32
     return cmul(__ldg(t.hi + (q >> t.lowbits)), __ldg(t.lo + (q & ((1u << t.lowbits) - 1u))));
 }
 
-template <class RC, int DIR, bool TW>
+// IDX: the index-only diagnostic (identity_passes in place of the radix passes, no four-step
+// twiddle).
+template <class RC, int DIR, bool TW, bool IDX = false>
 __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     k_cols_tma(const __grid_constant__ CUtensorMap imap, const __grid_constant__ CUtensorMap omap,
                int64_t nmat, int log2s, const float2* __restrict__ tw, int flags, int elem_parity,
@@ -192,12 +194,15 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         }
         __syncthreads();  // the stage becomes the exchange buffer
 
-        run_passes<C, DIR, 0>(v, t, smem + w, tw);
+        if constexpr (IDX)
+            identity_passes<C>(v, t, smem + w);
+        else
+            run_passes<C, DIR, 0>(v, t, smem + w, tw);
 
         // Output k = j + r*SL of column c.  Four-step: times w_M^{c*k} (M = L*S), formed as
         // w^{c*j} * w^{c*SL*a} * w^{c*SL*TA*b} for r = a + TA*b: one table lookup per butterfly,
         // the per-column factors from shared memory.
-        if constexpr (TW) {
+        if constexpr (TW && !IDX) {
             const float2* fw = fac + w;
 #pragma unroll
             for (int b = 0; b < BL; ++b) {
@@ -257,12 +262,28 @@ template <class RC, int DIR, bool TW>
 cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log2s,
                             const float2* tw, int flags, int elem_parity, ColsTwiddle twd,
                             int* err, uint64_t limit_ns, cudaStream_t stream) {
-    auto kern = k_cols_tma<RC, DIR, TW>;
+    const auto plain = k_cols_tma<RC, DIR, TW>;
+    auto kern = plain;
+    if (flags & KF_INDEX_ONLY) {  // instantiated for the 128-point pass of 2^15 only
+        if constexpr (RC::L == 128) {
+            kern = k_cols_tma<RC, DIR, TW, true>;
+            static LaunchCache icache;
+            LaunchGeom g;
+            cudaError_t e = icache.get(
+                [&](int dev, LaunchGeom* gg) {
+                    return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, gg);
+                },
+                &g);
+            if (e != cudaSuccess) return e;
+        } else {
+            return cudaErrorNotSupported;
+        }
+    }
     static LaunchCache cache;
     LaunchGeom geo;
     cudaError_t e = cache.get(
         [&](int dev, LaunchGeom* g) {
-            return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
+            return setup_persistent(plain, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
         },
         &geo);
     if (e != cudaSuccess) return e;

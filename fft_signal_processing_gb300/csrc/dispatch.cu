@@ -73,11 +73,23 @@ cudaError_t run_bluestein(int log2m, int mode, const void* in, void* out, int64_
     }
 }
 
+cudaError_t run_real_pair(int log2n, bool analysis, const void* in, void* out, int64_t nrows,
+                          int mmax, int mmajor, const float2* tw, int flags, cudaStream_t s) {
+    switch (log2n) {
+#define GBFFT_C(L) \
+    case L: return rpair_entry_##L(analysis, in, out, nrows, mmax, mmajor, tw, flags, s);
+        GBFFT_RPAIR_SIZES(GBFFT_C)
+#undef GBFFT_C
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, int* err, cudaStream_t s) {
+                    int mmajor, const float2* tw, const float2* twr, int flags, int* err,
+                    cudaStream_t s) {
     switch (log2h) {
 #define GBFFT_C(L) \
-    case L: return r2c_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, err, s);
+    case L: return r2c_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, flags, err, s);
         GBFFT_REAL_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;
@@ -85,11 +97,11 @@ cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int 
 }
 
 cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, int* err, uint64_t lim,
-                    cudaStream_t s) {
+                    int mmajor, const float2* tw, const float2* twr, int flags, int* err,
+                    uint64_t lim, cudaStream_t s) {
     switch (log2h) {
 #define GBFFT_C(L) \
-    case L: return c2r_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, err, lim, s);
+    case L: return c2r_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, flags, err, lim, s);
         GBFFT_REAL_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;

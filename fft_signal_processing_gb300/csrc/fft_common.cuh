@@ -200,6 +200,7 @@ enum : int {
     KF_CHESS_STORE = 2,  // multiply output element (row, k) by (-1)^k after the transform
     KF_CHESS_ROW = 4,    // 2-D chessboard: also multiply by (-1)^row
     KF_SCALE_SHIFT = 8,  // bits 8..15 hold k: the stored output is multiplied by 2^-k (k = 0: not)
+    KF_INDEX_ONLY = 16,  // diagnostic: no butterflies, twiddles or recombination (identity_passes)
 };
 
 // Flag bits asking the final store of a transform of 2^k points to scale by 1/2^k.

@@ -133,6 +133,34 @@ __device__ __forceinline__ void run_passes(float2 (&v)[C::E], int t, float2* sb,
     }
 }
 
+// Index-only diagnostic (the bit-exact test of the load and store epilogues): in place of the
+// radix passes, the values held in the first pass's register order (element j + r*N/R0 in
+// v[b*R0 + r]) move unchanged into the last pass's order (element j + r*N/RL in v[b*RL + r])
+// through the exchange buffer (sb: this transform's first slot, slots C::SS apart, room for the
+// padded full length), so that the store epilogue writes element k where the load read it.
+template <class C>
+__device__ __forceinline__ void identity_passes(float2 (&v)[C::E], int t, float2* sb) {
+    constexpr int R0 = C::radix(0);
+    constexpr int RL = C::radix(C::NPASS - 1);
+    if constexpr (R0 != RL) {
+        constexpr int B0 = C::E / R0, S0 = C::N / R0;
+        constexpr int BL = C::E / RL, SL = C::N / RL;
+#pragma unroll
+        for (int b = 0; b < B0; ++b) {
+#pragma unroll
+            for (int r = 0; r < R0; ++r)
+                sb[spad<C::LP>(t + b * C::T + r * S0) * C::SS] = v[b * R0 + r];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+#pragma unroll
+            for (int r = 0; r < RL; ++r)
+                v[b * RL + r] = sb[spad<C::LP>(t + b * C::T + r * SL) * C::SS];
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------------------------
 // Maps: where transform `tr` (0 <= tr < count) keeps its points.  Element e of the input is at
 // in_base(tr) + e*in_stride(), element k of the output at out_base(tr) + k*out_stride().

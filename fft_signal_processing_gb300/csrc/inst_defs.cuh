@@ -7,6 +7,7 @@
 #include "fft_kernel.cuh"
 #include "kernels.h"
 #include "real_kernel.cuh"
+#include "real_pair.cuh"
 #include "cols_tma.cuh"
 #include "rows_big.cuh"
 #include "rows_tma.cuh"
@@ -113,14 +114,24 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
 
 #define GBFFT_DEF_REAL(L)                                                                      \
     cudaError_t gbfft::r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,     \
-                                     int mmajor, const float2* tw, const float2* twr, int* err, \
-                                     cudaStream_t s) {                                          \
-        return launch_r2c<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, err, s);             \
+                                     int mmajor, const float2* tw, const float2* twr,           \
+                                     int flags, int* err, cudaStream_t s) {                     \
+        return launch_r2c<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, flags, err, s);      \
     }                                                                                           \
     cudaError_t gbfft::c2r_entry_##L(const float2* in, float* out, int64_t nrows, int mmax,     \
-                                     int mmajor, const float2* tw, const float2* twr, int* err, \
-                                     uint64_t lim, cudaStream_t s) {                            \
-        return launch_c2r<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, err, lim, s);        \
+                                     int mmajor, const float2* tw, const float2* twr,           \
+                                     int flags, int* err, uint64_t lim, cudaStream_t s) {       \
+        return launch_c2r<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, flags, err, lim,     \
+                                    s);                                                         \
+    }
+
+// Real rows two per complex transform: the one-pass kernel's geometry for n-point rows.
+#define GBFFT_DEF_RPAIR(L)                                                                     \
+    cudaError_t gbfft::rpair_entry_##L(bool analysis, const void* in, void* out,                \
+                                       int64_t nrows, int mmax, int mmajor, const float2* tw,   \
+                                       int flags, cudaStream_t s) {                             \
+        using C = FftCfg<L, rows_maxrb(L), rows_log2w(L), true>;                               \
+        return launch_real_pair<C>(analysis, in, out, nrows, mmax, mmajor, tw, flags, s);      \
     }
 
 #define GBFFT_DEF_BLUESTEIN(L)                                                                 \
@@ -139,6 +150,12 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
             case BLU_C2R:                                                                      \
                 return launch_bluestein<C, BLU_C2R>(in, out, nrows, n, mmax, mmajor, chirp,    \
                                                     chirp_out, bhat, tw, s);                   \
+            case BLU_R2C2:                                                                     \
+                return launch_bluestein<C, BLU_R2C2>(in, out, nrows, n, mmax, mmajor, chirp,   \
+                                                     chirp_out, bhat, tw, s);                  \
+            case BLU_C2R2:                                                                     \
+                return launch_bluestein<C, BLU_C2R2>(in, out, nrows, n, mmax, mmajor, chirp,   \
+                                                     chirp_out, bhat, tw, s);                  \
             default: return cudaErrorInvalidValue;                                             \
         }                                                                                      \
     }

@@ -22,11 +22,16 @@ namespace gbfft {
                                  uint64_t lim, cudaStream_t s);
 #define GBFFT_X_REAL(L)                                                                    \
     cudaError_t r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,        \
-                              int mmajor, const float2* tw, const float2* twr, int* err,    \
-                              cudaStream_t s);                                              \
+                              int mmajor, const float2* tw, const float2* twr, int flags,   \
+                              int* err, cudaStream_t s);                                    \
     cudaError_t c2r_entry_##L(const float2* in, float* out, int64_t nrows, int mmax,        \
-                              int mmajor, const float2* tw, const float2* twr, int* err,    \
-                              uint64_t lim, cudaStream_t s);
+                              int mmajor, const float2* tw, const float2* twr, int flags,   \
+                              int* err, uint64_t lim, cudaStream_t s);
+
+#define GBFFT_X_RPAIR(L)                                                                   \
+    cudaError_t rpair_entry_##L(bool analysis, const void* in, void* out, int64_t nrows,    \
+                                int mmax, int mmajor, const float2* tw, int flags,          \
+                                cudaStream_t s);
 
 #define GBFFT_X_BLUESTEIN(L)                                                               \
     cudaError_t bluestein_entry_##L(int mode, const void* in, void* out, int64_t nrows,      \
@@ -38,6 +43,7 @@ namespace gbfft {
 #define GBFFT_COLS_SIZES(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12)
 #define GBFFT_ROWS_T_SIZES(X) X(8) X(9) X(10) X(11) X(12)
 #define GBFFT_REAL_SIZES(X) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14)
+#define GBFFT_RPAIR_SIZES(X) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14)
 
 #define GBFFT_BLUESTEIN_SIZES(X) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14)
 
@@ -46,5 +52,6 @@ GBFFT_BLUESTEIN_SIZES(GBFFT_X_BLUESTEIN)
 GBFFT_COLS_SIZES(GBFFT_X_COLS)
 GBFFT_ROWS_T_SIZES(GBFFT_X_ROWS_T)
 GBFFT_REAL_SIZES(GBFFT_X_REAL)
+GBFFT_RPAIR_SIZES(GBFFT_X_RPAIR)
 
 }  // namespace gbfft

@@ -117,11 +117,37 @@ __host__ __device__ constexpr int bluestein_log2m(int64_t n) {
     return l;
 }
 
+// Rows of any length kMaxBluesteinN < n <= kMaxBluesteinMpN (not a power of two): the chirp-z
+// transform with four-step m-point FFTs over the workspaces A and B (each ntr * m complex64,
+// ntr = nrows for complex rows, (nrows + 1) / 2 for real rows, taken two per transform).
+// mode: 0 complex rows; 3 real rows -> spectrum; 4 spectrum -> real rows.
+struct ChirpMpTables {
+    const float2* chirp;      // c_j (with any fftshift folded in), j < n
+    const float2* chirp_out;  // c_k for the store (shift and normalisation folded in), k < n
+    const float2* bhat;       // FFT_m(conj c)/m, m entries
+    const float2* tw_cols;    // pass tables of the m-point four-step column pass
+    const float2* tw_rows;    // pass tables of its row pass
+    const float2* hi;         // two-level w_m^q table of the inter-pass twiddle
+    const float2* lo;
+    int lowbits;
+};
+cudaError_t run_bluestein_mp(int mode, const void* in, void* out, int64_t nrows, int n,
+                             int log2m, int mmax, int mmajor, const ChirpMpTables& t, float2* A,
+                             float2* B, int* err, uint64_t lim, cudaStream_t s);
+constexpr int64_t kMaxBluesteinMpN = int64_t(1) << 20;  // m = 2^21 at most
+
+// Real rows of 2^log2n points, two per n-point complex transform (rows 2p, 2p+1).
+cudaError_t run_real_pair(int log2n, bool analysis, const void* in, void* out, int64_t nrows,
+                          int mmax, int mmajor, const float2* tw, int flags, cudaStream_t s);
+constexpr int kMaxLog2RealPair = 14;
+
 // Real rows of 2^(log2h+1) points.
+// flags: KF_INDEX_ONLY (the diagnostic, real rows of 4096 and 2^15 points) or 0.
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, int* err, cudaStream_t s);
-cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
-                    int mmajor, const float2* tw, const float2* twr, int* err, uint64_t limit_ns,
+                    int mmajor, const float2* tw, const float2* twr, int flags, int* err,
                     cudaStream_t s);
+cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
+                    int mmajor, const float2* tw, const float2* twr, int flags, int* err,
+                    uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace gbfft

@@ -39,7 +39,9 @@ struct RealCfg {
 // TMA = true (m-major spectrum, even row count): the spectrum tile [k][W] leaves through
 // tensor stores of a 2-D map over (row, coefficient); coefficients above mmax are clipped by
 // the map's extent.
-template <class C, bool TMA>
+// IDX: the index-only diagnostic: no core transform (identity_passes) and no recombination, so
+// X_k = z_k (k < H) and X_H = z_0 land where the store epilogue puts them.
+template <class C, bool TMA, bool IDX = false>
 __global__ void __launch_bounds__(C::THREADS)
     k_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
           const float2* __restrict__ tw, const float2* __restrict__ twr,
@@ -66,7 +68,10 @@ __global__ void __launch_bounds__(C::THREADS)
         for (int r = 0; r < R0; ++r)
             v[b * R0 + r] = active ? ldg_stream(src + j + r * S0) : make_float2(0.f, 0.f);
     }
-    run_passes<C, -1, 0>(v, t, smem + w, tw);
+    if constexpr (IDX)
+        identity_passes<C>(v, t, smem + w);
+    else
+        run_passes<C, -1, 0>(v, t, smem + w, tw);
 
     constexpr int RL = C::radix(C::NPASS - 1);
     constexpr int BL = C::E / RL;
@@ -95,7 +100,7 @@ __global__ void __launch_bounds__(C::THREADS)
         constexpr int NB = H < 256 ? 1 : H / 256;
         constexpr int BK = H / NB;
         const float2 z0 = (int)threadIdx.x < W ? smem[threadIdx.x] : make_float2(0.f, 0.f);
-        const int npair = W * (H / 2 + 1);
+        const int npair = IDX ? 0 : W * (H / 2 + 1);
         for (int i = (int)threadIdx.x; i < npair; i += C::THREADS) {
             const int wr = i % W, k = i / W;
             const int km = (H - k) & (H - 1);
@@ -112,7 +117,8 @@ __global__ void __launch_bounds__(C::THREADS)
             bulk_wait_smem_read();  // shared memory stays valid until the stores have read it
         }
         if (mmax == H && (int)threadIdx.x < W && row0 + threadIdx.x < nrows)  // X_H, real
-            stg_stream(out + (int64_t)H * nrows + row0 + threadIdx.x, make_float2(z0.x - z0.y, 0.f));
+            stg_stream(out + (int64_t)H * nrows + row0 + threadIdx.x,
+                       IDX ? z0 : make_float2(z0.x - z0.y, 0.f));
     } else {
         const int total = W * (mmax + 1);
 #pragma unroll 4
@@ -121,7 +127,9 @@ __global__ void __launch_bounds__(C::THREADS)
             const int64_t rr = row0 + wr;
             if (rr >= nrows) continue;
             float2 y;
-            if (k == H) {  // Nyquist bin: Re Z_0 - Im Z_0
+            if (IDX) {
+                y = smem[(k & (H - 1)) * W + wr];
+            } else if (k == H) {  // Nyquist bin: Re Z_0 - Im Z_0
                 const float2 z0 = smem[wr];
                 y = make_float2(z0.x - z0.y, 0.f);
             } else {
@@ -137,7 +145,9 @@ __global__ void __launch_bounds__(C::THREADS)
 // TMA = true (m-major spectrum, even row count): the spectrum tile [k][W] (k < H) arrives by
 // tensor loads of a 2-D map over (row, coefficient); coefficients above mmax are filled with
 // zeros by the copy engine.  The wait is bounded (limit_ns), reporting into *err.
-template <class C, bool TMA>
+// IDX: the index-only diagnostic: no recombination and no core transform, so
+// x_{2k} = Re X_k, x_{2k+1} = Im X_k for the gathered X_k, k < H.
+template <class C, bool TMA, bool IDX = false>
 __global__ void __launch_bounds__(C::THREADS)
     k_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
           const float2* __restrict__ tw, const float2* __restrict__ twr,
@@ -211,6 +221,10 @@ __global__ void __launch_bounds__(C::THREADS)
         for (int r = 0; r < R0; ++r) {
             const int k = j + r * S0;
             const float2 xk = smem[k * W + w];
+            if (IDX) {
+                v[b * R0 + r] = xk;
+                continue;
+            }
             const float2 xm = smem[(H - k) * W + w];
             const float2 xc = make_float2(xm.x, -xm.y);             // conj X_{H-k}
             const float2 sum = cadd(xk, xc);
@@ -220,7 +234,10 @@ __global__ void __launch_bounds__(C::THREADS)
     }
     __syncthreads();  // the exchange buffer aliases the gathered spectrum
 
-    run_passes<C, +1, 0>(v, t, smem + w, tw);
+    if constexpr (IDX)
+        identity_passes<C>(v, t, smem + w);
+    else
+        run_passes<C, +1, 0>(v, t, smem + w, tw);
 
     constexpr int RL = C::radix(C::NPASS - 1);
     constexpr int BL = C::E / RL;
@@ -278,16 +295,16 @@ bool real_use_tma(int64_t nrows, int mmajor) {
     return mmajor && C::W >= 2 && (nrows % 2) == 0 && nrows >= C::W;
 }
 
-template <class C>
-cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
-                       const float2* tw, const float2* twr, int* err, cudaStream_t stream) {
+template <class C, bool IDX>
+cudaError_t launch_r2c_impl(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
+                            const float2* tw, const float2* twr, int* err, cudaStream_t stream) {
     constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CUtensorMap map;
     std::memset(&map, 0, sizeof map);
     if (real_use_tma<C>(nrows, mmajor)) {
-        auto kern = k_r2c<C, true>;
+        auto kern = k_r2c<C, true, IDX>;
         struct Tag {};
         cudaError_t e = configure_once<Tag>(kern, smem);
         if (e == cudaSuccess) e = encode_spectrum_map<C>(&map, out, nrows, mmax);
@@ -295,7 +312,7 @@ cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, in
         kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr,
                                                             map, err);
     } else {
-        auto kern = k_r2c<C, false>;
+        auto kern = k_r2c<C, false, IDX>;
         struct Tag {};
         cudaError_t e = configure_once<Tag>(kern, smem);
         if (e != cudaSuccess) return e;
@@ -305,17 +322,17 @@ cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, in
     return cudaGetLastError();
 }
 
-template <class C>
-cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
-                       const float2* tw, const float2* twr, int* err, uint64_t limit_ns,
-                       cudaStream_t stream) {
+template <class C, bool IDX>
+cudaError_t launch_c2r_impl(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
+                            const float2* tw, const float2* twr, int* err, uint64_t limit_ns,
+                            cudaStream_t stream) {
     constexpr size_t smem = RealCfg<C>::SMEM_BYTES;
     const int64_t grid = (nrows + C::W - 1) / C::W;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     CUtensorMap map;
     std::memset(&map, 0, sizeof map);
     if (real_use_tma<C>(nrows, mmajor)) {
-        auto kern = k_c2r<C, true>;
+        auto kern = k_c2r<C, true, IDX>;
         struct Tag {};
         cudaError_t e = configure_once<Tag>(kern, smem);
         if (e == cudaSuccess) e = encode_spectrum_map<C>(&map, in, nrows, mmax);
@@ -323,7 +340,7 @@ cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, in
         kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(in, out, nrows, mmax, mmajor, tw, twr,
                                                             map, err, limit_ns);
     } else {
-        auto kern = k_c2r<C, false>;
+        auto kern = k_c2r<C, false, IDX>;
         struct Tag {};
         cudaError_t e = configure_once<Tag>(kern, smem);
         if (e != cudaSuccess) return e;
@@ -331,6 +348,36 @@ cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, in
                                                             map, err, limit_ns);
     }
     return cudaGetLastError();
+}
+
+// The index-only diagnostic (KF_INDEX_ONLY in flags) is instantiated for real rows of 4096 and
+// 2^15 points only.
+template <class C>
+cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
+                       const float2* tw, const float2* twr, int flags, int* err,
+                       cudaStream_t stream) {
+    if (flags & KF_INDEX_ONLY) {
+        if constexpr (C::LOG2N == 11 || C::LOG2N == 14)
+            return launch_r2c_impl<C, true>(in, out, nrows, mmax, mmajor, tw, twr, err, stream);
+        else
+            return cudaErrorNotSupported;
+    }
+    return launch_r2c_impl<C, false>(in, out, nrows, mmax, mmajor, tw, twr, err, stream);
+}
+
+template <class C>
+cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, int mmajor,
+                       const float2* tw, const float2* twr, int flags, int* err,
+                       uint64_t limit_ns, cudaStream_t stream) {
+    if (flags & KF_INDEX_ONLY) {
+        if constexpr (C::LOG2N == 11 || C::LOG2N == 14)
+            return launch_c2r_impl<C, true>(in, out, nrows, mmax, mmajor, tw, twr, err,
+                                            limit_ns, stream);
+        else
+            return cudaErrorNotSupported;
+    }
+    return launch_c2r_impl<C, false>(in, out, nrows, mmax, mmajor, tw, twr, err, limit_ns,
+                                     stream);
 }
 
 }  // namespace gbfft

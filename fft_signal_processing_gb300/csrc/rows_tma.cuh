@@ -40,8 +40,9 @@ struct RowsTmaCfg {
 };
 
 // SCALE: the output scaling of normalised plans (flags' scale bits) is a separate
-// instantiation, so that the unscaled kernel carries none of its code.
-template <class RC, int DIR, bool SCALE>
+// instantiation, so that the unscaled kernel carries none of its code.  IDX: the index-only
+// diagnostic (identity_passes in place of the radix passes), instantiated for 4096 points only.
+template <class RC, int DIR, bool SCALE, bool IDX = false>
 __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     k_rows_tma(const float2* in, float2* out, int64_t nrows, const float2* __restrict__ tw,
                int flags, int row_parity, int* err, uint64_t limit_ns) {
@@ -132,7 +133,10 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
                 }
             }
         };
-        run_passes<C, DIR, 0>(v, t, sbuf + w * RC::SROW, tw);
+        if constexpr (IDX)
+            identity_passes<C>(v, t, sbuf + w * RC::SROW);
+        else
+            run_passes<C, DIR, 0>(v, t, sbuf + w * RC::SROW, tw);
 
         if (active) {
             float2* dst = out + row * N;
@@ -161,6 +165,22 @@ cudaError_t launch_rows_tma(const float2* in, float2* out, int64_t nrows, const 
     auto plain = k_rows_tma<RC, DIR, false>;
     auto scaled = k_rows_tma<RC, DIR, true>;
     auto kern = (flags >> KF_SCALE_SHIFT) ? scaled : plain;
+    if (flags & KF_INDEX_ONLY) {
+        if constexpr (RC::LOG2N == 12) {
+            auto idx = k_rows_tma<RC, DIR, false, true>;
+            static LaunchCache icache;
+            LaunchGeom g;
+            cudaError_t e = icache.get(
+                [&](int dev, LaunchGeom* gg) {
+                    return setup_persistent(idx, RC::C::THREADS, RC::SMEM_BYTES, dev, gg);
+                },
+                &g);
+            if (e != cudaSuccess) return e;
+            kern = idx;
+        } else {
+            return cudaErrorNotSupported;
+        }
+    }
     static LaunchCache cache;  // attributes and occupancy are per device
     LaunchGeom geo;
     cudaError_t e = cache.get(

@@ -38,7 +38,8 @@ struct RowsTTmaCfg {
     static_assert(W >= 2, "tensor boxes are at least 16 bytes wide");
 };
 
-template <class RC, int DIR>
+// IDX: the index-only diagnostic (identity_passes in place of the radix passes).
+template <class RC, int DIR, bool IDX = false>
 __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     k_rowst_tma(const float2* in, const __grid_constant__ CUtensorMap omap, int64_t nrows,
                 int log2n1, const float2* __restrict__ tw, int flags, int* err,
@@ -106,7 +107,10 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         }
         __syncthreads();  // the stage becomes the exchange buffer
 
-        run_passes<C, DIR, 0>(v, t, smem + w, tw);
+        if constexpr (IDX)
+            identity_passes<C>(v, t, smem + w);
+        else
+            run_passes<C, DIR, 0>(v, t, smem + w, tw);
 
         __syncthreads();  // every thread has read the last exchange
 #pragma unroll
@@ -139,12 +143,28 @@ template <class RC, int DIR>
 cudaError_t launch_rowst_tma(const float2* in, float2* out, int64_t nrows, int log2n1,
                              const float2* tw, int flags, int* err, uint64_t limit_ns,
                              cudaStream_t stream) {
-    auto kern = k_rowst_tma<RC, DIR>;
+    const auto plain = k_rowst_tma<RC, DIR>;
+    auto kern = plain;
+    if (flags & KF_INDEX_ONLY) {  // instantiated for the 256-point pass of 2^15 only
+        if constexpr (RC::N == 256) {
+            kern = k_rowst_tma<RC, DIR, true>;
+            static LaunchCache icache;
+            LaunchGeom g;
+            cudaError_t e = icache.get(
+                [&](int dev, LaunchGeom* gg) {
+                    return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, gg);
+                },
+                &g);
+            if (e != cudaSuccess) return e;
+        } else {
+            return cudaErrorNotSupported;
+        }
+    }
     static LaunchCache cache;
     LaunchGeom geo;
     cudaError_t e = cache.get(
         [&](int dev, LaunchGeom* g) {
-            return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
+            return setup_persistent(plain, RC::C::THREADS, RC::SMEM_BYTES, dev, g);
         },
         &geo);
     if (e != cudaSuccess) return e;

@@ -5,7 +5,7 @@
  *
  *     X_k = sum_{j<n} x_j * exp(s * 2*pi*i * j*k / n),   s = -1 forward, s = +1 inverse,
  *
- * on batches of contiguous rows (dims = 1: power-of-two n, or any n up to 8192) or images
+ * on batches of contiguous rows (dims = 1: power-of-two n, or any n up to 2^20) or images
  * (dims = 2, power-of-two sides, row-column: all rows, then all columns), unnormalised in both
  * directions unless a plan asks for 1/n (fft_plan_set_normalization).  This is the discrete Fourier
  * transform of Mota, "High Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5, with
@@ -64,7 +64,7 @@ enum {
 #define FFT_MAX_LOG2N_1D 24   /* n <= 2^24 for dims = 1, complex rows */
 #define FFT_MAX_LOG2N_REAL 15 /* n <= 2^15 for the real layouts (one-pass n/2-point core) */
 #define FFT_MAX_LOG2N_2D 12   /* n <= 2^12 per side for dims = 2 */
-#define FFT_MAX_N_ANY_LENGTH 8192 /* rows (dims 1, complex or real) whose length is not a power of two */
+#define FFT_MAX_N_ANY_LENGTH 1048576 /* rows (dims 1, complex or real) whose length is not a power of two */
 
 /*
  * fft_plan_create - plan a batched transform on the current CUDA device.
@@ -75,9 +75,12 @@ enum {
  *             rows, dims 1; for real rows this is the any-nphi role of the direct-sum 'dft'
  *             mode of fourier.ts), computed as the chirp-z (Bluestein)
  *             transform X_k = c_k sum_j (x_j c_j) conj(c_{k-j}), c_j = exp(s*pi*i*j^2/n),
- *             through power-of-two FFTs of length m >= 2n - 1 in one kernel (the same
- *             unnormalised DFT of Mota, "High Performance Fourier Transforms on GPUs with
- *             GLSL", 2.2 Eq. 5, for lengths the radix-2^k passes cannot split).
+ *             through power-of-two FFTs of length m >= 2n - 1 (the same unnormalised DFT of
+ *             Mota, "High Performance Fourier Transforms on GPUs with GLSL", 2.2 Eq. 5, for
+ *             lengths the radix-2^k passes cannot split): in one kernel for n <= 8192, as
+ *             seven passes over a plan workspace of 2 * rows * m complex64 above that (chirp,
+ *             four-step forward FFT, filter, four-step inverse FFT, chirp).  Real rows above
+ *             8192 points always take two rows per transform (fft_plan_set_real_pairing).
  *   batch     number of rows (dims 1) or images (dims 2), >= 1.
  *   dims      1 or 2 (2 only with FFT_LAYOUT_C2C).
  *   direction FFT_FORWARD or FFT_INVERSE.  Real layouts: FORWARD = analysis (R2C, exec with
@@ -146,6 +149,22 @@ int fft_plan_set_normalization(fft_plan plan, int normalize);
 int fft_plan_set_band_limit(fft_plan plan, int64_t mmax);
 
 /*
+ * fft_plan_set_real_pairing - for a real-layout plan, pairing = 1 transforms two real rows per
+ * complex transform: rows 2p and 2p+1 are packed as y = x1 + i x2 and one n-point complex FFT
+ * serves both (Mota, "High Performance Fourier Transforms on GPUs with GLSL", §2.6 Eq. 17-18:
+ * X1_k = (Y_k + conj Y_{n-k})/2, X2_k = (Y_k - conj Y_{n-k})/(2i), and for the synthesis
+ * Y_k = X1_k + i X2_k, x1 = Re y, x2 = Im y).  pairing = 0 (the default) takes one row per
+ * n/2-point complex transform with the two-for-one recombination of "src/sht/wgsl/fourier.ts".
+ * Both give the same spectra and rows (within fp32 rounding); the layouts, band limit and
+ * argument rules of fft_exec_r2c / fft_exec_c2r are unchanged, and an odd batch pairs its last
+ * row with a zero row that is never written.  Power-of-two plans take it for n <= 2^14 (one
+ * CTA holds the n-point complex row); plans of other lengths (the chirp-z path) for every n.
+ * Host only.  Returns FFT_OK, FFT_ERR_INVALID_ARG (NULL plan, C2C plan, pairing not 0/1) or
+ * FFT_ERR_UNSUPPORTED_SIZE (power-of-two n > 2^14).
+ */
+int fft_plan_set_real_pairing(fft_plan plan, int pairing);
+
+/*
  * fft_plan_set_wait_timeout - time limit, in nanoseconds, of every device-side wait of the
  * plan's kernels (waits for asynchronous bulk copies into shared memory).  A wait that runs out
  * makes its CTA record the failure in the plan's device error word, wait (for at most 1 s) for
@@ -155,6 +174,23 @@ int fft_plan_set_band_limit(fft_plan plan, int64_t mmax);
  * without a real stall.  Host only.  Returns FFT_OK or FFT_ERR_INVALID_ARG (NULL plan).
  */
 int fft_plan_set_wait_timeout(fft_plan plan, uint64_t ns);
+
+/*
+ * fft_plan_set_diagnostic - test hook.  mode = FFT_DIAG_INDEX_ONLY makes the plan's kernels
+ * skip every butterfly, twiddle multiplication and real-row recombination, so that an execution
+ * moves each input value, unchanged, through the load and store epilogues alone: the
+ * chessboard sign flips, the four-step transposed store X[k1 + N1*k2], the Hermitian gather of
+ * a synthesis, the pack and unpack of two real rows per transform, and the row-major or
+ * m-major spectrum layouts.  A test compares those outputs bit for bit with the index maps of
+ * an independent implementation; the results are not Fourier transforms.  Built in for the
+ * one-pass 4096-point and four-step 2^15-point C2C plans, real plans of 4096 and 2^15 points,
+ * and 4096-point real plans with two rows per transform.  mode = 0 restores normal
+ * execution.  Host only.  Returns FFT_OK, FFT_ERR_INVALID_ARG (NULL plan, unknown mode) or
+ * FFT_ERR_UNSUPPORTED_SIZE (another plan; its exec calls then also return that status while
+ * the mode is set).
+ */
+#define FFT_DIAG_INDEX_ONLY 1
+int fft_plan_set_diagnostic(fft_plan plan, int mode);
 
 /* fft_plan_workspace_bytes - device bytes the plan holds besides its twiddle tables
  * (informational).  Returns FFT_OK or FFT_ERR_INVALID_ARG. */

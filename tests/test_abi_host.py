@@ -50,7 +50,7 @@ def q(n, batch=1, dims=1, direction=-1, layout=0, shift=0):
     return fx.lib().fft_plan_query(n, batch, dims, direction, layout, shift, None, 0)
 
 
-@pytest.mark.parametrize("n", [0, -4, 8193, 10000, 3 << 20])
+@pytest.mark.parametrize("n", [0, -4, (1 << 20) + 1, 3 << 20, 1000003 * 3])
 def test_lengths_outside_the_supported_set_rejected(n):
     assert q(n) == fx.FFT_ERR_UNSUPPORTED_SIZE
 
@@ -66,6 +66,17 @@ def test_any_length_rows_take_the_chirp_z_path(n, m):
     d = fx.query(n, 5, layout=2, direction=1)
     assert "path=bluestein" in d and f"mmax={(n - 1) // 2} " in d and "synthesis" in d
     assert q(n, dims=2) == fx.FFT_ERR_UNSUPPORTED_SIZE
+
+
+@pytest.mark.parametrize("n,m", [(8193, 1 << 15), (10000, 1 << 15), (16385, 1 << 16),
+                                 (100000, 1 << 18), ((1 << 20) - 1, 1 << 21)])
+def test_long_any_length_rows_take_the_multipass_chirp_z_path(n, m):
+    d = fx.query(n, 3)
+    assert "path=bluestein_multipass" in d and f"m={m} " in d and "kernels=7" in d
+    l = m.bit_length() - 1
+    assert f"n1={1 << (l // 2)} n2={1 << (l - l // 2)}" in d
+    d = fx.query(n, 3, layout=1)
+    assert "path=bluestein_multipass" in d and "rows_per_transform=2" in d
 
 
 def test_size_limits():
@@ -98,7 +109,7 @@ def test_batch_overflow_rejected():
 
 def test_create_rejects_before_touching_the_device():
     h = ctypes.c_void_p(1)
-    rc = fx.lib().fft_plan_create(8193, 1, 1, -1, 0, 0, ctypes.byref(h))
+    rc = fx.lib().fft_plan_create((1 << 20) + 1, 1, 1, -1, 0, 0, ctypes.byref(h))
     assert rc == fx.FFT_ERR_UNSUPPORTED_SIZE and not h.value
     assert fx.lib().fft_plan_create(8, 1, 1, -1, 0, 0, None) == fx.FFT_ERR_INVALID_ARG
 
@@ -106,6 +117,7 @@ def test_create_rejects_before_touching_the_device():
 def test_null_plan_calls():
     L = fx.lib()
     assert L.fft_plan_set_band_limit(None, 1) == fx.FFT_ERR_INVALID_ARG
+    assert L.fft_plan_set_real_pairing(None, 1) == fx.FFT_ERR_INVALID_ARG
     assert L.fft_plan_workspace_bytes(None, None) == fx.FFT_ERR_INVALID_ARG
     assert L.fft_plan_describe(None, None, 0) == fx.FFT_ERR_INVALID_ARG
     assert L.fft_exec_c2c(None, None, None, None) == fx.FFT_ERR_INVALID_ARG

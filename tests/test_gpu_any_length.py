@@ -174,3 +174,66 @@ def test_any_length_real_round_trip(n):
     ref = n * F.astype(np.complex128)
     ref[:, 0] = n * F[:, 0].real
     assert_parity(G, ref, mmax + 1, f"analysis(synthesis) n={n}")
+
+
+# ---- lengths above 8192: the multi-pass chirp-z (four-step m-point passes over a workspace) --
+# References come from the oracle's mixed-radix FFT (smallest prime factor first; a prime length
+# is its direct sum), pinned to numpy: the direct O(n^2) sum of oracle.transform is too slow here.
+LONG_LENGTHS = [8193, 10000, 12289, 65535, 100000, 531441, (1 << 20) - 1]
+
+
+def long_ref(x, direction, shift=False):
+    if not shift:
+        return oracle.fft_any(x, direction)
+    if direction == -1:
+        return oracle.fftshift_any(oracle.fft_any(x, -1))
+    return oracle.fft_any(oracle.fftshift_any(x, 1, inverse=True), +1)
+
+
+@pytest.mark.parametrize("n", LONG_LENGTHS)
+@pytest.mark.parametrize("direction", [-1, 1])
+def test_long_any_length_grid(n, direction):
+    """A prime (12289), products of small primes and the largest length (m = 2^21), both
+    directions, against the oracle's mixed-radix DFT."""
+    batch = 3 if n <= 100000 else 2
+    x = wl().normal(7500 + n, batch, n)
+    m = fx()
+    assert "path=bluestein_multipass" in m.query(n, batch, 1, direction)
+    got = gpu_c2c(x, n, batch, direction)
+    assert_parity(got, long_ref(x, direction), n, f"long n={n} dir={direction}")
+
+
+@pytest.mark.parametrize("n", [10000, 10001, 2 * 3 ** 10])
+@pytest.mark.parametrize("direction", [-1, 1])
+def test_long_any_length_shift_in_place(n, direction):
+    batch = 2
+    x = wl().uniform(7600 + n, batch, n)
+    got = gpu_c2c(x, n, batch, direction, shift=True, inplace=True)
+    assert_parity(got, long_ref(x, direction, True), n, f"long shift n={n}")
+
+
+def test_long_any_length_round_trip_and_tones():
+    n, batch = 100000, 2
+    x = wl().tones(7700, batch, n)
+    y = gpu_c2c(x, n, batch, -1)
+    assert_parity(y, long_ref(x, -1), n, "long tones n=100000")
+    z = gpu_c2c(y, n, batch, +1)
+    assert_parity(z, n * x.astype(np.complex128), n, "long round trip n=100000")
+
+
+@pytest.mark.parametrize("n,mmaxes", [(10000, (0, 3333, 4999, 5000)), (10001, (1, 5000)),
+                                      (100000, (0, 1000))])
+@pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
+def test_long_real_rows(n, mmaxes, layout):
+    """Band-limited real rows above 8192 points (two rows per chirp-z transform), odd and
+    even row counts, against the oracle's direct analysis and synthesis sums."""
+    for i, mmax in enumerate(mmaxes):
+        rows = (3, 4)[i % 2]
+        F = wl().spectrum(7800 + n + i, rows, mmax)
+        got = gpu_c2r(F, n, mmax, layout)
+        assert_parity(got, oracle.c2r_direct(F, n), n, f"long c2r n={n} mmax={mmax} {layout}")
+        x = wl().real_normal(7900 + n + i, rows, n)
+        G = gpu_r2c(x, mmax, layout)
+        assert_parity(G, oracle.r2c_direct(x, mmax), mmax + 1,
+                      f"long r2c n={n} mmax={mmax} {layout}",
+                      scale=np.linalg.norm(x.astype(np.float64), axis=1))
