@@ -249,8 +249,8 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
             else
                 snprintf(what, sizeof what, "%s shift=%d", dir, s.shift);
             snprintf(buf, sizeof buf,
-                     "path=bluestein_multipass n=%lld batch=%lld %s m=%d n1=%d n2=%d kernels=7 "
-                     "(chirp, fourstep fwd x2, filter, fourstep inv x2, chirp)",
+                     "path=bluestein_multipass n=%lld batch=%lld %s m=%d n1=%d n2=%d kernels=6 "
+                     "(chirp, fourstep fwd x2, fourstep inv x2 with the filter, chirp)",
                      (long long)s.n, (long long)s.batch, what, 1 << s.log2m, 1 << s.log2n1,
                      1 << s.log2n2);
             break;

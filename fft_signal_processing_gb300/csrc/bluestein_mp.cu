@@ -1,5 +1,6 @@
 // Host sequence of the multi-pass chirp-z transform (bluestein_mp.cuh): chirp premultiply,
-// four-step forward FFT, filter, four-step inverse FFT, chirp postmultiply, all on `s`.
+// four-step forward FFT, four-step inverse FFT with the filter on its first load, chirp
+// postmultiply, all on `s`.
 #include "bluestein_mp.cuh"
 #include "kernels.h"
 
@@ -29,12 +30,10 @@ cudaError_t run_bluestein_mp(int mode, const void* in, void* out, int64_t nrows,
     if (e == cudaSuccess)
         e = run_cols(l1, -1, A, B, ntr << l2, l2, t.tw_cols, 0, 0, t.hi, t.lo, t.lowbits, err, lim, s);
     if (e == cudaSuccess) e = run_rows_t(l2, -1, B, A, ntr << l1, l1, t.tw_rows, 0, err, lim, s);
-    if (e == cudaSuccess) {
-        k_chirp_filter<<<gm, kChirpThreads, 0, s>>>(A, ntr, m, t.bhat);
-        e = cudaGetLastError();
-    }
+    // inverse FFT_m of A * bhat, the filter fused into the first pass's load
     if (e == cudaSuccess)
-        e = run_cols(l1, +1, A, B, ntr << l2, l2, t.tw_cols, 0, 0, t.hi, t.lo, t.lowbits, err, lim, s);
+        e = run_cols(l1, +1, A, B, ntr << l2, l2, t.tw_cols, 0, 0, t.hi, t.lo, t.lowbits, err, lim, s,
+                     t.bhat);
     if (e == cudaSuccess) e = run_rows_t(l2, +1, B, A, ntr << l1, l1, t.tw_rows, 0, err, lim, s);
     if (e != cudaSuccess) return e;
     const dim3 go = chirp_grid(ntr, mode == BLU_R2C2 ? mmax + 1 : n);

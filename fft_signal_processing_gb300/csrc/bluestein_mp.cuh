@@ -7,17 +7,16 @@
 // a cyclic convolution of length m evaluated exactly on k < n (as in bluestein.cuh):
 //   1. k_chirp_pre:  A_j = x_j c_j for j < n, 0 for n <= j < m;
 //   2. four-step forward FFT_m of A (two passes through a second workspace);
-//   3. k_chirp_filter: A_q *= bhat_q, bhat = FFT_m(b)/m (plan table, double precision on the
-//      host);
-//   4. four-step inverse FFT_m;
-//   5. k_chirp_post: X_k = c_k A_k for k < n.
+//   3. four-step inverse FFT_m of A * bhat, bhat = FFT_m(b)/m (plan table, double precision
+//      on the host), the product taken on the load of its first pass;
+//   4. k_chirp_post: X_k = c_k A_k for k < n.
 // The fftshift is folded into the chirp tables exactly as in bluestein.cuh.  Band-limited real
 // rows take two rows per transform (Mota, "High Performance Fourier Transforms on GPUs with
 // GLSL", §2.6 Eq. 17-18): the analysis transforms y = x1 + i x2 and unpacks
-// X1_k = (Y_k + conj Y_{n-k})/2, X2_k = (Y_k - conj Y_{n-k})/(2i) in step 5; the synthesis
+// X1_k = (Y_k + conj Y_{n-k})/2, X2_k = (Y_k - conj Y_{n-k})/(2i) in step 4; the synthesis
 // assembles Y_k = X1_k + i X2_k from the two Hermitian spectra in step 1 (X_0 = Re F_0,
 // X_m = F_m and X_{n-m} = conj F_m for 1 <= m <= mmax, a Nyquist bin real) and stores Re y and
-// Im y in step 5.  Steps 1, 3 and 5 are elementwise passes with coalesced accesses along rows.
+// Im y in step 4.  Steps 1 and 4 are elementwise passes with coalesced accesses along rows.
 #pragma once
 
 #include "bluestein.cuh"
@@ -78,19 +77,7 @@ __global__ void __launch_bounds__(kChirpThreads)
     }
 }
 
-// Step 3.
-__global__ void __launch_bounds__(kChirpThreads)
-    k_chirp_filter(float2* A, int64_t ntr, int m, const float2* __restrict__ bhat) {
-    for (int64_t row = blockIdx.y; row < ntr; row += gridDim.y) {
-        for (int q = blockIdx.x * kChirpThreads + (int)threadIdx.x; q < m;
-             q += gridDim.x * kChirpThreads) {
-            float2* p = A + row * m + q;
-            stg_stream(p, cmul(ldg_stream(p), __ldg(bhat + q)));
-        }
-    }
-}
-
-// Step 5.  k runs over the outputs kept: n (complex rows, real synthesis) or mmax + 1 (real
+// Step 4.  k runs over the outputs kept: n (complex rows, real synthesis) or mmax + 1 (real
 // analysis).
 template <int MODE>
 __global__ void __launch_bounds__(kChirpThreads)

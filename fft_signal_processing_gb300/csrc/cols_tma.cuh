@@ -44,12 +44,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int 
         "r"(x), "r"(y), "r"(z), "r"(smem_addr(src_smem))
         : "memory");
 }
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// The issuing thread's bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_smem_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // 2-D tiled tensor copies (global -> shared on an mbarrier; shared -> global in a bulk group).
 __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
@@ -93,6 +87,7 @@ struct ColsTwiddle {
     const float2* hi;  // w_{L*S}^q = hi[q >> lowbits] * lo[q & lowmask]
     const float2* lo;
     int lowbits;
+    const float2* pre = nullptr;  // optional: input element q of each transform times pre[q]
 };
 
 // w_M^q for q reduced modulo M = 2^log2m, from the two-level table of the plan.
@@ -102,8 +97,9 @@ __device__ __forceinline__ float2 root2(const ColsTwiddle& t, uint32_t q, uint32
 }
 
 // IDX: the index-only diagnostic (identity_passes in place of the radix passes, no four-step
-// twiddle).
-template <class RC, int DIR, bool TW, bool IDX = false>
+// twiddle).  PRE: element q = row*S + column of each [L][S] transform is multiplied by
+// twd.pre[q] on the load (the chirp-z filter, fused into the inverse FFT's first pass).
+template <class RC, int DIR, bool TW, bool IDX = false, bool PRE = false>
 __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     k_cols_tma(const __grid_constant__ CUtensorMap imap, const __grid_constant__ CUtensorMap omap,
                int64_t nmat, int log2s, const float2* __restrict__ tw, int flags, int elem_parity,
@@ -188,6 +184,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
             for (int r = 0; r < R0; ++r) {
                 const int e = j + r * S0;
                 float2 xv = smem[e * W + w];  // dense [row][W] tile written by the copy engine
+                if constexpr (PRE) xv = cmul(xv, __ldg(twd.pre + ((int64_t)e << log2s) + c));
                 if (flags & KF_CHESS_LOAD) xv = neg_if(xv, (e * elem_parity + cp) & 1);
                 v[b * R0 + r] = xv;
             }
@@ -264,6 +261,21 @@ cudaError_t launch_cols_tma(const float2* in, float2* out, int64_t nmat, int log
                             int* err, uint64_t limit_ns, cudaStream_t stream) {
     const auto plain = k_cols_tma<RC, DIR, TW>;
     auto kern = plain;
+    if (twd.pre) {  // instantiated for the inverse column pass of the multi-pass chirp-z only
+        if constexpr (TW && DIR > 0 && RC::L >= 128 && RC::L <= 1024) {
+            kern = k_cols_tma<RC, DIR, TW, false, true>;
+            static LaunchCache pcache;
+            LaunchGeom g;
+            cudaError_t e = pcache.get(
+                [&](int dev, LaunchGeom* gg) {
+                    return setup_persistent(kern, RC::C::THREADS, RC::SMEM_BYTES, dev, gg);
+                },
+                &g);
+            if (e != cudaSuccess) return e;
+        } else {
+            return cudaErrorNotSupported;
+        }
+    }
     if (flags & KF_INDEX_ONLY) {  // instantiated for the 128-point pass of 2^15 only
         if constexpr (RC::L == 128) {
             kern = k_cols_tma<RC, DIR, TW, true>;

@@ -33,14 +33,15 @@ cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t 
 
 cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t count,
                      int log2s, const float2* tw, int flags, int ep, const float2* hi,
-                     const float2* lo, int lowbits, int* err, uint64_t lim, cudaStream_t s) {
+                     const float2* lo, int lowbits, int* err, uint64_t lim, cudaStream_t s,
+                     const float2* pre) {
     switch (log2l) {
 #define GBFFT_C(L)                                                                           \
     case L:                                                                                  \
         return hi ? cols_tw_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo,     \
-                                      lowbits, err, lim, s)                                  \
+                                      lowbits, err, lim, s, pre)                             \
                   : cols_entry_##L(dir, in, out, count, log2s, tw, flags, ep, hi, lo, lowbits, \
-                                   err, lim, s);
+                                   err, lim, s, pre);
         GBFFT_COLS_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;

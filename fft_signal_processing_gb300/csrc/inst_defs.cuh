@@ -40,7 +40,7 @@ cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2
 template <int L, int DIR, bool TW>
 cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, const float2* tw,
                       int flags, int ep, const float2* hi, const float2* lo, int lowbits,
-                      int* err, uint64_t lim, cudaStream_t s) {
+                      int* err, uint64_t lim, cudaStream_t s, const float2* pre) {
     if constexpr (L >= kColsTmaMinLog2 && L <= kColsTmaMaxLog2) {
         if (cols_use_tma(L, log2s)) {  // matrices at least one column tile wide
             if constexpr (L >= kBigTileMinLog2) {
@@ -51,14 +51,15 @@ cudaError_t cols_impl(const float2* in, float2* out, int64_t count, int log2s, c
             } else {
                 using RC = ColsTmaCfg<L, cols_tma_maxrb(L), cols_tma_log2w(L)>;
                 return launch_cols_tma<RC, DIR, TW>(in, out, count >> log2s, log2s, tw, flags,
-                                                    ep, ColsTwiddle{hi, lo, lowbits}, err, lim,
-                                                    s);
+                                                    ep, ColsTwiddle{hi, lo, lowbits, pre}, err,
+                                                    lim, s);
             }
         }
     }
     // short columns, and images narrower than a tile: the generic strided kernel
     (void)err;
     (void)lim;
+    if (pre) return cudaErrorNotSupported;
     using C = FftCfg<L, cols_maxrb(L), cols_log2w(L, 0), false>;
     MapCols<TW> m{count, log2s, L, ep, hi, lo, lowbits};
     return launch_fft<C, DIR, MapCols<TW>>(in, out, m, tw, flags, s);
@@ -95,11 +96,11 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
     cudaError_t gbfft::NAME##_##L(int dir, const float2* in, float2* out, int64_t count,        \
                                   int log2s, const float2* tw, int flags, int ep,               \
                                   const float2* hi, const float2* lo, int lowbits, int* err,    \
-                                  uint64_t lim, cudaStream_t s) {                               \
+                                  uint64_t lim, cudaStream_t s, const float2* pre) {            \
         return dir < 0 ? cols_impl<L, -1, TWV>(in, out, count, log2s, tw, flags, ep, hi, lo,    \
-                                               lowbits, err, lim, s)                            \
+                                               lowbits, err, lim, s, pre)                       \
                        : cols_impl<L, +1, TWV>(in, out, count, log2s, tw, flags, ep, hi, lo,    \
-                                               lowbits, err, lim, s);                           \
+                                               lowbits, err, lim, s, pre);                      \
     }
 #define GBFFT_DEF_COLS_PLAIN(L) GBFFT_DEF_COLS_VARIANT(L, cols_entry, false)
 #define GBFFT_DEF_COLS_TW(L) GBFFT_DEF_COLS_VARIANT(L, cols_tw_entry, true)

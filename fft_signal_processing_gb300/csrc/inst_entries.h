@@ -15,7 +15,7 @@ namespace gbfft {
     cudaError_t NAME##_##L(int dir, const float2* in, float2* out, int64_t count,           \
                                int log2s, const float2* tw, int flags, int ep,              \
                                const float2* hi, const float2* lo, int lowbits, int* err,   \
-                               uint64_t lim, cudaStream_t s);
+                               uint64_t lim, cudaStream_t s, const float2* pre);
 #define GBFFT_X_ROWS_T(L)                                                                  \
     cudaError_t rows_t_entry_##L(int dir, const float2* in, float2* out, int64_t count,     \
                                  int log2n1, const float2* tw, int flags, int* err,         \

@@ -63,9 +63,12 @@ constexpr int kRowsTmaStages = 1;  // one stage per CTA: six CTAs per SM at 2^12
 // With hi/lo non-NULL, output k1 of column c is multiplied by w_{L*S}^{c*k1} (four-step).
 // Columns of 2^7..2^12 points with at least one full tile per matrix run the persistent
 // TMA-staged tile kernel (bounded waits reporting into *err, which may be NULL).
+// pre (optional, four-step columns of 2^7..2^10 points, inverse): input element q of each
+// transform is multiplied by pre[q] on the load.
 cudaError_t run_cols(int log2l, int dir, const float2* in, float2* out, int64_t count,
                      int log2s, const float2* tw, int flags, int elem_parity, const float2* hi,
-                     const float2* lo, int lowbits, int* err, uint64_t limit_ns, cudaStream_t s);
+                     const float2* lo, int lowbits, int* err, uint64_t limit_ns, cudaStream_t s,
+                     const float2* pre = nullptr);
 
 // Column tiles of the TMA kernel: W = 4096/L columns up to 512 points (at most 64), 8 columns
 // at 1024 points and 4 above.  Wide row runs (32-64 bytes) were measured to matter more than

@@ -46,6 +46,12 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, 
         : "memory");
 }
 
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The issuing thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_smem_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -78,6 +84,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s for draining copies after a timeout
+
 
 // Error word values written by kernels (read and cleared by fft_plan_check).
 enum : int { KERR_WAIT_TIMEOUT = 1, KERR_STAGE_ALIGN = 2 };

@@ -78,8 +78,9 @@ enum {
  *             through power-of-two FFTs of length m >= 2n - 1 (the same unnormalised DFT of
  *             Mota, "High Performance Fourier Transforms on GPUs with GLSL", 2.2 Eq. 5, for
  *             lengths the radix-2^k passes cannot split): in one kernel for n <= 8192, as
- *             seven passes over a plan workspace of 2 * rows * m complex64 above that (chirp,
- *             four-step forward FFT, filter, four-step inverse FFT, chirp).  Real rows above
+ *             six passes over a plan workspace of 2 * rows * m complex64 above that (chirp,
+ *             four-step forward FFT, four-step inverse FFT with the filter on its first load,
+ *             chirp).  Real rows above
  *             8192 points always take two rows per transform (fft_plan_set_real_pairing).
  *   batch     number of rows (dims 1) or images (dims 2), >= 1.
  *   dims      1 or 2 (2 only with FFT_LAYOUT_C2C).

@@ -72,7 +72,7 @@ def test_any_length_rows_take_the_chirp_z_path(n, m):
                                  (100000, 1 << 18), ((1 << 20) - 1, 1 << 21)])
 def test_long_any_length_rows_take_the_multipass_chirp_z_path(n, m):
     d = fx.query(n, 3)
-    assert "path=bluestein_multipass" in d and f"m={m} " in d and "kernels=7" in d
+    assert "path=bluestein_multipass" in d and f"m={m} " in d and "kernels=6" in d
     l = m.bit_length() - 1
     assert f"n1={1 << (l // 2)} n2={1 << (l - l // 2)}" in d
     d = fx.query(n, 3, layout=1)
