@@ -8,9 +8,10 @@ resident in HBM.  The default workload is the batched 1-D C2C round trip: N = 40
 (-1)^j chessboard on its load, then the inverse transform (chessboard on its store) -- two
 kernel launches per step.  Other workloads (--workload): c2c_1024 (N = 1024 x 64 rows, forward),
 sweep_<log2n> (batch*N = 2^26 rows of 3 tones + noise, forward), any_<n> (the same for a
-length n <= 8192 that is not a power of two: the chirp-z path), realany_<n> (the real
-workload below for such a length, mmax = n/3), real (2048 rows x 4096,
-mmax = 1365, synthesis then analysis, m-major spectrum), 2d (4096 x 4096, forward with the 2-D
+length n <= 2^20 that is not a power of two: the chirp-z path), realany_<n> (the real
+workload below for such a length, mmax = n/3; realanypair_<n>: two rows per transform), real
+(2048 rows x 4096, mmax = 1365, synthesis then analysis, m-major spectrum; realpair: two rows
+per transform), 2d (4096 x 4096, forward with the 2-D
 chessboard then inverse), shift_<n> (standalone fftshift of 2^26 points in rows of n; this one
 reports GB/s, as it moves data and computes nothing).
 

@@ -220,7 +220,8 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
             break;
         }
         case PATH_BLUESTEIN: {
-            const int w = rows_log2w(s.log2m);
+            const bool light = blu_light(s.log2m, s.batch);
+            const int w = blu_log2w(s.log2m, light);
             const bool real = s.layout != FFT_LAYOUT_C2C;
             char what[96];
             if (real)
@@ -234,9 +235,9 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
                      "threads=%d rows_per_cta=%d smem=%zu",
                      (long long)s.n, (long long)s.batch, what,
                      real && real_pair ? " rows_per_transform=2" : "", 1 << s.log2m,
-                     radix_string(s.log2m, rows_maxrb(s.log2m)).c_str(),
-                     (1 << rows_log2t(s.log2m)) << w, 1 << w,
-                     padded_bytes(s.log2m, rows_maxrb(s.log2m), w));
+                     radix_string(s.log2m, blu_maxrb(s.log2m, light)).c_str(),
+                     (1 << blu_log2t(s.log2m, light)) << w, 1 << w,
+                     padded_bytes(s.log2m, blu_maxrb(s.log2m, light), w));
             break;
         }
         case PATH_BLUESTEIN_MP: {
@@ -298,6 +299,9 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
     }
     return buf;
 }
+
+// The chirp-z schedule of a plan, chosen from its batch (the tables follow the same choice).
+int blu_mode_light(const PlanSpec& s) { return blu_light(s.log2m, s.batch) ? BLU_LIGHT : 0; }
 
 int map_cuda(cudaError_t e) {
     if (e == cudaSuccess) return FFT_OK;
@@ -430,7 +434,7 @@ static int create_from_spec(const PlanSpec& s, fft_plan* out) {
             break;
         }
         case PATH_BLUESTEIN:
-            p->off_a = append_pass_tables(tw, s.log2m, rows_maxrb(s.log2m));
+            p->off_a = append_pass_tables(tw, s.log2m, blu_maxrb(s.log2m, blu_light(s.log2m, s.batch)));
             {
                 // fftshift folded in: exp(+2 pi i j h/n) on the forward load, exp(-2 pi i k h/n)
                 // on the inverse store, h = n/2 rounded down
@@ -603,7 +607,8 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
             break;
         }
         case PATH_BLUESTEIN: {  // the shift lives in the chirp tables
-            e = run_bluestein(s.log2m, 0, x, y, s.batch, (int)s.n, 0, 0, p->d_tw + p->off_chirp,
+            e = run_bluestein(s.log2m, BLU_C2C | blu_mode_light(s), x, y, s.batch, (int)s.n, 0, 0,
+                              p->d_tw + p->off_chirp,
                               p->d_tw + p->off_chirp_out, p->d_tw + p->off_bhat,
                               p->d_tw + p->off_a, st);
             break;
@@ -658,7 +663,8 @@ int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
     if (s.path == PATH_BLUESTEIN_MP)
         e = exec_chirp_mp(p, 3, in, out, (cudaStream_t)stream);
     else if (s.path == PATH_BLUESTEIN)
-        e = run_bluestein(s.log2m, p->real_pair ? 3 : 1, in, out, s.batch, (int)s.n,
+        e = run_bluestein(s.log2m, (p->real_pair ? BLU_R2C2 : BLU_R2C) | blu_mode_light(s), in, out,
+                          s.batch, (int)s.n,
                           (int)p->mmax, mmajor, p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
                           p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream);
     else if (p->real_pair)
@@ -666,7 +672,7 @@ int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
                           p->d_tw + p->off_pair, diag, (cudaStream_t)stream);
     else
         e = run_r2c(s.log2n - 1, in, (float2*)out, s.batch, (int)p->mmax, mmajor,
-                    p->d_tw + p->off_a, p->d_tw + p->off_r, diag, p->d_err,
+                    p->d_tw + p->off_a, p->d_tw + p->off_r, diag, p->d_err, p->wait_limit_ns,
                     (cudaStream_t)stream);
     return e == cudaSuccess ? FFT_OK : FFT_ERR_CUDA;
 }
@@ -686,7 +692,8 @@ int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
     if (s.path == PATH_BLUESTEIN_MP)
         e = exec_chirp_mp(p, 4, in, out, (cudaStream_t)stream);
     else if (s.path == PATH_BLUESTEIN)
-        e = run_bluestein(s.log2m, p->real_pair ? 4 : 2, in, out, s.batch, (int)s.n,
+        e = run_bluestein(s.log2m, (p->real_pair ? BLU_C2R2 : BLU_C2R) | blu_mode_light(s), in, out,
+                          s.batch, (int)s.n,
                           (int)p->mmax, mmajor, p->d_tw + p->off_chirp, p->d_tw + p->off_chirp_out,
                           p->d_tw + p->off_bhat, p->d_tw + p->off_a, (cudaStream_t)stream);
     else if (p->real_pair)

@@ -32,11 +32,11 @@
 #pragma once
 
 #include "fft_kernel.cuh"
+#include "kernels.h"
 #include "launch_cache.cuh"
 
 namespace gbfft {
 
-enum : int { BLU_C2C = 0, BLU_R2C = 1, BLU_C2R = 2, BLU_R2C2 = 3, BLU_C2R2 = 4 };
 
 // Shared-memory slots per transform: the padded exchange, and for the two-row analysis the
 // n outputs that the unpack reads.
@@ -45,8 +45,15 @@ __host__ __device__ constexpr int blu_slots() {
     return MODE == BLU_R2C2 ? (C::SROW > C::N ? C::SROW : C::N) : C::SROW;
 }
 
+// CTAs per SM the registers must allow: 512 threads per SM (128 registers a thread) for the
+// light radix-16 schedules of m >= 2^9, whose registers hold 16 points; no bound otherwise.
+template <class C>
+__host__ __device__ constexpr int blu_min_ctas() {
+    return C::LOG2N >= 9 && C::E <= 16 && C::THREADS <= 512 ? 512 / C::THREADS : 1;
+}
+
 template <class C, int MODE>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::THREADS, blu_min_ctas<C>())
     k_bluestein(const void* in_, void* out_, int64_t nrows, int n, int mmax, int mmajor,
                 const float2* __restrict__ chirp, const float2* __restrict__ chirp_out,
                 const float2* __restrict__ bhat, const float2* __restrict__ tw) {

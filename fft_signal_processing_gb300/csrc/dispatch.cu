@@ -87,10 +87,10 @@ cudaError_t run_real_pair(int log2n, bool analysis, const void* in, void* out, i
 
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
                     int mmajor, const float2* tw, const float2* twr, int flags, int* err,
-                    cudaStream_t s) {
+                    uint64_t lim, cudaStream_t s) {
     switch (log2h) {
 #define GBFFT_C(L) \
-    case L: return r2c_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, flags, err, s);
+    case L: return r2c_entry_##L(in, out, nrows, mmax, mmajor, tw, twr, flags, err, lim, s);
         GBFFT_REAL_SIZES(GBFFT_C)
 #undef GBFFT_C
         default: return cudaErrorInvalidValue;

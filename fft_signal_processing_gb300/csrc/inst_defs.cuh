@@ -28,6 +28,11 @@ cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2
         (void)lim;
         return launch_small<L, DIR>(in, out, nrows, flags, rp, s);
     } else if constexpr (L >= kRowsTmaMinLog2 && L <= kRowsTmaMaxLog2) {
+        if constexpr (L == 12 && k2dRowStages != kRowsTmaStages) {
+            if (rp)  // the row pass of a 4096-wide image (a short batch of rows)
+                return launch_rows_tma<RowsTmaCfg<L, rows_maxrb(L), k2dRowStages>, DIR>(
+                    in, out, nrows, tw, flags, rp, err, lim, s);
+        }
         return launch_rows_tma<RowsTmaCfg<L, rows_maxrb(L), kRowsTmaStages>, DIR>(
             in, out, nrows, tw, flags, rp, err, lim, s);
     } else {
@@ -77,6 +82,26 @@ cudaError_t rows_t_impl(const float2* in, float2* out, int64_t count, int log2n1
     }
 }
 
+// The chirp-z kernel in each of its modes, for one m-point schedule C.
+template <class C>
+cudaError_t bluestein_modes(int mode, const void* in, void* out, int64_t nrows, int n, int mmax,
+                            int mmajor, const float2* chirp, const float2* chirp_out,
+                            const float2* bhat, const float2* tw, cudaStream_t s) {
+    switch (mode) {
+        case BLU_C2C:
+            return launch_bluestein<C, BLU_C2C>(in, out, nrows, n, mmax, mmajor, chirp, chirp_out, bhat, tw, s);
+        case BLU_R2C:
+            return launch_bluestein<C, BLU_R2C>(in, out, nrows, n, mmax, mmajor, chirp, chirp_out, bhat, tw, s);
+        case BLU_C2R:
+            return launch_bluestein<C, BLU_C2R>(in, out, nrows, n, mmax, mmajor, chirp, chirp_out, bhat, tw, s);
+        case BLU_R2C2:
+            return launch_bluestein<C, BLU_R2C2>(in, out, nrows, n, mmax, mmajor, chirp, chirp_out, bhat, tw, s);
+        case BLU_C2R2:
+            return launch_bluestein<C, BLU_C2R2>(in, out, nrows, n, mmax, mmajor, chirp, chirp_out, bhat, tw, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <int LH>
 using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
 
@@ -116,8 +141,8 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
 #define GBFFT_DEF_REAL(L)                                                                      \
     cudaError_t gbfft::r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,     \
                                      int mmajor, const float2* tw, const float2* twr,           \
-                                     int flags, int* err, cudaStream_t s) {                     \
-        return launch_r2c<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, flags, err, s);      \
+                                     int flags, int* err, uint64_t lim, cudaStream_t s) {       \
+        return launch_r2c<RealC<L>>(in, out, nrows, mmax, mmajor, tw, twr, flags, err, lim, s); \
     }                                                                                           \
     cudaError_t gbfft::c2r_entry_##L(const float2* in, float* out, int64_t nrows, int mmax,     \
                                      int mmajor, const float2* tw, const float2* twr,           \
@@ -140,23 +165,10 @@ using RealC = FftCfg<LH, real_maxrb(LH), real_log2w(LH), false>;
                                            int n, int mmax, int mmajor, const float2* chirp,    \
                                            const float2* chirp_out, const float2* bhat,         \
                                            const float2* tw, cudaStream_t s) {                  \
-        using C = FftCfg<L, rows_maxrb(L), rows_log2w(L), true>;                               \
-        switch (mode) {                                                                        \
-            case BLU_C2C:                                                                      \
-                return launch_bluestein<C, BLU_C2C>(in, out, nrows, n, mmax, mmajor, chirp,    \
-                                                    chirp_out, bhat, tw, s);                   \
-            case BLU_R2C:                                                                      \
-                return launch_bluestein<C, BLU_R2C>(in, out, nrows, n, mmax, mmajor, chirp,    \
-                                                    chirp_out, bhat, tw, s);                   \
-            case BLU_C2R:                                                                      \
-                return launch_bluestein<C, BLU_C2R>(in, out, nrows, n, mmax, mmajor, chirp,    \
-                                                    chirp_out, bhat, tw, s);                   \
-            case BLU_R2C2:                                                                     \
-                return launch_bluestein<C, BLU_R2C2>(in, out, nrows, n, mmax, mmajor, chirp,   \
-                                                     chirp_out, bhat, tw, s);                  \
-            case BLU_C2R2:                                                                     \
-                return launch_bluestein<C, BLU_C2R2>(in, out, nrows, n, mmax, mmajor, chirp,   \
-                                                     chirp_out, bhat, tw, s);                  \
-            default: return cudaErrorInvalidValue;                                             \
-        }                                                                                      \
+        constexpr bool two = blu_maxrb(L, true) != blu_maxrb(L, false);                          \
+        if ((mode & BLU_LIGHT) && two)                                                          \
+            return bluestein_modes<FftCfg<L, blu_maxrb(L, true), blu_log2w(L, true), true>>(    \
+                mode & ~BLU_LIGHT, in, out, nrows, n, mmax, mmajor, chirp, chirp_out, bhat, tw, s); \
+        return bluestein_modes<FftCfg<L, blu_maxrb(L, false), blu_log2w(L, false), true>>(      \
+            mode & ~BLU_LIGHT, in, out, nrows, n, mmax, mmajor, chirp, chirp_out, bhat, tw, s);  \
     }

@@ -23,7 +23,7 @@ namespace gbfft {
 #define GBFFT_X_REAL(L)                                                                    \
     cudaError_t r2c_entry_##L(const float* in, float2* out, int64_t nrows, int mmax,        \
                               int mmajor, const float2* tw, const float2* twr, int flags,   \
-                              int* err, cudaStream_t s);                                    \
+                              int* err, uint64_t lim, cudaStream_t s);                      \
     cudaError_t c2r_entry_##L(const float2* in, float* out, int64_t nrows, int mmax,        \
                               int mmajor, const float2* tw, const float2* twr, int flags,   \
                               int* err, uint64_t lim, cudaStream_t s);

@@ -57,6 +57,8 @@ cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t 
 constexpr int kRowsTmaMinLog2 = 5;
 constexpr int kRowsTmaMaxLog2 = 12;
 constexpr int kRowsTmaStages = 1;  // one stage per CTA: six CTAs per SM at 2^12
+// Stages of the row pass of 4096-wide images (4096 rows an image: about 4.5 rows per CTA).
+constexpr int k2dRowStages = 1;
 
 // Strided columns: count columns of matrices [2^log2l][2^log2s] stored back to back.
 // elem_parity: 1 for the 2-D chessboard (-1)^(row+col), 0 for the four-step one (-1)^col.
@@ -117,6 +119,30 @@ cudaError_t run_bluestein(int log2m, int mode, const void* in, void* out, int64_
                           int mmax, int mmajor, const float2* chirp, const float2* chirp_out,
                           const float2* bhat, const float2* tw, cudaStream_t s);
 constexpr int kMaxBluesteinN = 8192;  // 2n - 1 <= 2^14: one pass, the m-point row in one CTA
+// Radix and rows per CTA of the one-pass chirp-z kernel's m-point transforms.  The kernel does
+// two m-point transforms per row and is bound by latency and issue, not HBM.  Light schedules
+// (radix 16: more threads, at most 128 registers, two CTAs per SM) serve m = 2^12 and 2^13
+// always, and m = 2^9..2^11 for batches too small to give the radix-64 schedule 8 CTAs per SM
+// (measured: m = 2^11 large batches 0.74 vs 0.81 ms with radix 64; 2048 real rows 2x faster
+// light; m = 2^12, 2^13 20% and 34% faster light).  At m = 2^14 a row's 1024 radix-16 threads
+// would leave 64 registers each, so it keeps radix 32.
+// Modes of run_bluestein: complex rows; real rows -> spectrum; spectrum -> real rows; the same
+// two with two real rows per transform.  BLU_LIGHT (or'ed in) selects the light schedule.
+enum : int { BLU_C2C = 0, BLU_R2C = 1, BLU_C2R = 2, BLU_R2C2 = 3, BLU_C2R2 = 4, BLU_LIGHT = 256 };
+__host__ __device__ constexpr int blu_maxrb(int l, bool light) {
+    return l >= 9 && l <= 13 && (light || l >= 12) ? 4 : rows_maxrb(l);
+}
+__host__ __device__ constexpr int blu_log2t(int l, bool light) {
+    return l - sched_rbits(l, blu_maxrb(l, light), 0);
+}
+__host__ __device__ constexpr int blu_log2w(int l, bool light) {
+    return clampi(8 - blu_log2t(l, light), 0, 8);
+}
+// Light schedule for a batch of `transforms` m-point transforms (m = 2^l)?
+constexpr int64_t kBluLightCtas = 8 * 152;  // 8 CTAs per SM of a 152-SM GB300
+__host__ __device__ constexpr bool blu_light(int l, int64_t transforms) {
+    return l >= 12 || (transforms >> blu_log2w(l, false)) < kBluLightCtas;
+}
 __host__ __device__ constexpr int bluestein_log2m(int64_t n) {
     int l = 0;
     while ((int64_t(1) << l) < 2 * n - 1) ++l;
@@ -151,7 +177,10 @@ constexpr int kMaxLog2RealPair = 14;
 // flags: KF_INDEX_ONLY (the diagnostic, real rows of 4096 and 2^15 points) or 0.
 cudaError_t run_r2c(int log2h, const float* in, float2* out, int64_t nrows, int mmax,
                     int mmajor, const float2* tw, const float2* twr, int flags, int* err,
-                    cudaStream_t s);
+                    uint64_t limit_ns, cudaStream_t s);
+// Real rows with a core of 2^8..2^11 points and an m-major spectrum (even row count) run
+// persistent kernels that overlap each tile's copy with the previous tile's transform.
+constexpr bool kRealPersistent = true;
 cudaError_t run_c2r(int log2h, const float2* in, float* out, int64_t nrows, int mmax,
                     int mmajor, const float2* tw, const float2* twr, int flags, int* err,
                     uint64_t limit_ns, cudaStream_t s);

@@ -350,17 +350,282 @@ cudaError_t launch_c2r_impl(const float2* in, float* out, int64_t nrows, int mma
     return cudaGetLastError();
 }
 
+// ---- persistent kernels for the m-major spectrum (tensor copies) --------------------------------
+// Real rows whose core is at most 2^11 points (the 2048 x 4096 real workload) are too few to
+// fill the GPU in one wave of the kernels above, and each of those CTAs loads, transforms and
+// stores in turn.  These persistent CTAs walk a strided sequence of tiles of W = 2 rows and keep
+// the copy stage apart from the exchange area: as soon as a tile is in registers the next
+// tile's copy is issued into the stage, so that it overlaps the transform and the stores.  C2R
+// stages the spectrum tile [k][W] (k < H) by 2-D tensor copies (zero fill above mmax and past
+// the last row); R2C stages W real rows by bulk copies into padded row slots and sends the
+// spectrum out by tensor stores from the exchange area (clipped at mmax).  Every mbarrier wait
+// is bounded; on expiry the CTA records KERR_WAIT_TIMEOUT, drains its copy and exits.
+template <class C>
+struct RealPCfg {
+    static constexpr int H = C::N;
+    static constexpr int W = C::W;
+    static constexpr int SLOTS = C::SROW > H + 1 ? C::SROW : H + 1;
+    static constexpr int WORK = SLOTS * W;                 // exchange area (float2)
+    static constexpr int NB = H < 256 ? 1 : H / 256;       // tensor boxes per tile
+    static constexpr int BK = H / NB;                      // coefficients per box
+    static constexpr int C2R_STAGE = H * W;                // spectrum tile [k][W], k < H
+    static constexpr int INROW = H + (W >= 8 ? 2 : 16 / W);  // padded real-row slot (float2)
+    static constexpr int R2C_STAGE = W * INROW;
+    static constexpr size_t C2R_SMEM = (size_t)(C2R_STAGE + WORK) * sizeof(float2);
+    static constexpr size_t R2C_SMEM = (size_t)(R2C_STAGE + WORK) * sizeof(float2);
+    static_assert(W >= 2, "tensor boxes are at least 16 bytes wide");
+    static_assert((C2R_STAGE * 8) % 128 == 0 && (R2C_STAGE * 8) % 128 == 0,
+                  "the exchange area stays 128-byte aligned");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    k_c2r_p(const __grid_constant__ CUtensorMap fmap, const float2* in, float* out,
+            int64_t nrows, int mmax, const float2* __restrict__ tw,
+            const float2* __restrict__ twr, int* err, uint64_t limit_ns) {
+    using P = RealPCfg<C>;
+    constexpr int H = C::N;
+    constexpr int W = C::W;
+    extern __shared__ __align__(128) float2 smem[];
+    float2* stage = smem;
+    float2* work = smem + P::C2R_STAGE;
+    __shared__ uint64_t bar;
+    __shared__ int stage_bad;
+    const int tid = (int)threadIdx.x;
+    const int w = tid % W;
+    const int t = tid / W;
+    const int64_t ntiles = (nrows + W - 1) / W;
+    const int64_t t0 = blockIdx.x, tstride = gridDim.x;
+
+    auto issue = [&](int64_t tile) {  // the full box counts toward the bytes, OOB fill included
+        mbar_arrive_expect_tx(&bar, (uint32_t)(H * W * 8));
+#pragma unroll 1
+        for (int b = 0; b < P::NB; ++b)
+            tma_load_2d(stage + b * P::BK * W, &fmap, (int)(tile * W), b * P::BK, &bar);
+    };
+    if (tid == 0) {
+        stage_bad = stage_misaligned(stage, err) | stage_misaligned(work, err);
+        prefetch_tensormap(&fmap);
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (stage_bad) return;  // uniform: never copy into a misaligned stage
+    if (tid == 0 && t0 < ntiles) issue(t0);
+
+    constexpr int R0 = C::radix(0);
+    constexpr int B0 = C::E / R0;
+    constexpr int S0 = C::N / R0;
+    constexpr int RL = C::radix(C::NPASS - 1);
+    constexpr int BL = C::E / RL;
+    constexpr int SL = C::N / RL;
+    for (int64_t it = 0;; ++it) {
+        const int64_t tile = t0 + it * tstride;
+        if (tile >= ntiles) break;
+        const bool ok = mbar_wait_bounded(&bar, (uint32_t)(it & 1), limit_ns);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                if (err) atomicExch(err, KERR_WAIT_TIMEOUT);
+                mbar_wait_bounded(&bar, (uint32_t)(it & 1), kDrainLimitNs);
+            }
+            return;
+        }
+        const int64_t row = tile * W + w;
+        const bool active = row < nrows;
+        // X_H: the Nyquist bin (real) when mmax = H, else 0 (the stage holds k < H)
+        float2 xh = make_float2(0.f, 0.f);
+        if (mmax == H && active) xh.x = ldg_stream(in + (int64_t)H * nrows + row).x;
+        // Z_k = (X_k + conj X_{H-k}) + i e^{+i th_k} (X_k - conj X_{H-k}), X_0 real
+        float2 v[C::E];
+#pragma unroll
+        for (int b = 0; b < B0; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < R0; ++r) {
+                const int k = j + r * S0;
+                float2 xk = stage[k * W + w];
+                if (k == 0) xk.y = 0.f;
+                const float2 xm = k == 0 ? xh : stage[(H - k) * W + w];
+                const float2 xc = make_float2(xm.x, -xm.y);
+                const float2 sum = cadd(xk, xc);
+                const float2 wd = ctw<+1>(csub(xk, xc), __ldg(twr + k));
+                v[b * R0 + r] = make_float2(sum.x - wd.y, sum.y + wd.x);
+            }
+        }
+        __syncthreads();  // the stage has been read: refill it with the next tile now
+        if (tid == 0) {
+            const int64_t nt = tile + tstride;
+            if (nt < ntiles) {
+                fence_proxy_async_smem();
+                issue(nt);
+            }
+        }
+        run_passes<C, +1, 0>(v, t, work + w, tw);
+        if (active) {
+            float2* dst = reinterpret_cast<float2*>(out) + row * H;  // x_{2m}, x_{2m+1} = z_m
+#pragma unroll
+            for (int b = 0; b < BL; ++b) {
+                const int j = t + b * C::T;
+#pragma unroll
+                for (int r = 0; r < RL; ++r) stg_stream(dst + j + r * SL, v[b * RL + r]);
+            }
+        }
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS)
+    k_r2c_p(const float* in, float2* out, const __grid_constant__ CUtensorMap fmap,
+            int64_t nrows, int mmax, const float2* __restrict__ tw,
+            const float2* __restrict__ twr, int* err, uint64_t limit_ns) {
+    using P = RealPCfg<C>;
+    constexpr int H = C::N;
+    constexpr int W = C::W;
+    extern __shared__ __align__(128) float2 smem[];
+    float2* stage = smem;
+    float2* work = smem + P::R2C_STAGE;
+    __shared__ uint64_t bar;
+    __shared__ int stage_bad;
+    const int tid = (int)threadIdx.x;
+    const int w = tid % W;
+    const int t = tid / W;
+    const int64_t ntiles = (nrows + W - 1) / W;
+    const int64_t t0 = blockIdx.x, tstride = gridDim.x;
+    const float2* zin = reinterpret_cast<const float2*>(in);  // z_m = x_{2m} + i x_{2m+1}
+
+    auto issue = [&](int64_t tile) {
+        const int64_t r0 = tile * W;
+        const int rows = nrows - r0 < W ? (int)(nrows - r0) : W;
+        mbar_arrive_expect_tx(&bar, (uint32_t)rows * H * 8u);
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r)
+            bulk_load(stage + r * P::INROW, zin + (r0 + r) * H, (uint32_t)H * 8u, &bar);
+    };
+    if (tid == 0) {
+        stage_bad = stage_misaligned(stage, err) | stage_misaligned(work, err);
+        prefetch_tensormap(&fmap);
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (stage_bad) return;  // uniform: never copy into a misaligned stage
+    if (tid == 0 && t0 < ntiles) issue(t0);
+
+    constexpr int R0 = C::radix(0);
+    constexpr int B0 = C::E / R0;
+    constexpr int S0 = C::N / R0;
+    constexpr int RL = C::radix(C::NPASS - 1);
+    constexpr int BL = C::E / RL;
+    constexpr int SL = C::N / RL;
+    auto recombine = [&](float2 zk, float2 zm, int k) {  // X_k from Z_k and Z_{H-k}
+        const float2 zc = make_float2(zm.x, -zm.y);
+        const float2 xe = make_float2(0.5f * (zk.x + zc.x), 0.5f * (zk.y + zc.y));
+        const float2 d = make_float2(0.5f * (zk.x - zc.x), 0.5f * (zk.y - zc.y));
+        const float2 xo = make_float2(d.y, -d.x);
+        return cadd(xe, ctw<-1>(xo, __ldg(twr + k)));
+    };
+    for (int64_t it = 0;; ++it) {
+        const int64_t tile = t0 + it * tstride;
+        if (tile >= ntiles) break;
+        const bool ok = mbar_wait_bounded(&bar, (uint32_t)(it & 1), limit_ns);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                if (err) atomicExch(err, KERR_WAIT_TIMEOUT);
+                mbar_wait_bounded(&bar, (uint32_t)(it & 1), kDrainLimitNs);
+            }
+            return;
+        }
+        const int64_t row0 = tile * W;
+        const bool active = row0 + w < nrows;
+        float2 v[C::E];
+#pragma unroll
+        for (int b = 0; b < B0; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < R0; ++r)
+                v[b * R0 + r] = active ? stage[w * P::INROW + j + r * S0] : make_float2(0.f, 0.f);
+        }
+        // the stage has been read (and the previous tile's spectrum stores have read the
+        // exchange area: thread 0 waited for them before arriving here): refill the stage now
+        __syncthreads();
+        if (tid == 0) {
+            const int64_t nt = tile + tstride;
+            if (nt < ntiles) {
+                fence_proxy_async_smem();
+                issue(nt);
+            }
+        }
+        run_passes<C, -1, 0>(v, t, work + w, tw);
+        if constexpr (C::NPASS > 1) __syncthreads();  // last exchange fully read
+#pragma unroll
+        for (int b = 0; b < BL; ++b) {
+            const int j = t + b * C::T;
+#pragma unroll
+            for (int r = 0; r < RL; ++r) work[(j + r * SL) * W + w] = v[b * RL + r];  // Z_k
+        }
+        __syncthreads();
+        // pairs {k, H-k} recombined in place; threads tid < W keep Z_0 for the Nyquist bin
+        const float2 z0 = tid < W ? work[tid] : make_float2(0.f, 0.f);
+        const int npair = W * (H / 2 + 1);
+        for (int i = tid; i < npair; i += C::THREADS) {
+            const int wr = i % W, k = i / W;
+            const int km = (H - k) & (H - 1);
+            const float2 zk = work[k * W + wr], zm = work[km * W + wr];
+            work[k * W + wr] = recombine(zk, zm, k);
+            if (km != k) work[km * W + wr] = recombine(zm, zk, km);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            for (int b = 0; b < P::NB && b * P::BK <= mmax; ++b)
+                tma_store_2d(&fmap, (int)row0, b * P::BK, work + b * P::BK * W);
+            bulk_commit();
+            bulk_wait_smem_read();  // the exchange area may be rewritten once the stores read it
+        }
+        if (mmax == H && tid < W && row0 + tid < nrows)  // X_H = Re Z_0 - Im Z_0, real
+            stg_stream(out + (int64_t)H * nrows + row0 + tid, make_float2(z0.x - z0.y, 0.f));
+    }
+}
+
+// Persistent launch: one CTA per resident slot, at most one per tile.
+template <class C, class K, class... Args>
+cudaError_t launch_real_p(K kern, size_t smem, int64_t nrows, cudaStream_t stream,
+                          Args... args) {
+    static LaunchCache cache;
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int dev, LaunchGeom* g) { return setup_persistent(kern, C::THREADS, smem, dev, g); },
+        &geo);
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (nrows + C::W - 1) / C::W;
+    const int64_t resident = (int64_t)geo.per_sm * geo.num_sms;
+    const int64_t grid = ntiles < resident ? ntiles : resident;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<(unsigned)grid, C::THREADS, smem, stream>>>(args...);
+    return cudaGetLastError();
+}
+
 // The index-only diagnostic (KF_INDEX_ONLY in flags) is instantiated for real rows of 4096 and
 // 2^15 points only.
 template <class C>
 cudaError_t launch_r2c(const float* in, float2* out, int64_t nrows, int mmax, int mmajor,
                        const float2* tw, const float2* twr, int flags, int* err,
-                       cudaStream_t stream) {
+                       uint64_t limit_ns, cudaStream_t stream) {
     if (flags & KF_INDEX_ONLY) {
         if constexpr (C::LOG2N == 11 || C::LOG2N == 14)
             return launch_r2c_impl<C, true>(in, out, nrows, mmax, mmajor, tw, twr, err, stream);
         else
             return cudaErrorNotSupported;
+    }
+    if constexpr (kRealPersistent && C::LOG2N >= 8 && C::LOG2N <= 11) {
+        using PC = FftCfg<C::LOG2N, C::MAXRB, 1, false>;  // two rows per tile
+        if (real_use_tma<PC>(nrows, mmajor)) {
+            CUtensorMap map;
+            cudaError_t e = encode_spectrum_map<PC>(&map, out, nrows, mmax);
+            if (e != cudaSuccess) return e;
+            return launch_real_p<PC>(k_r2c_p<PC>, RealPCfg<PC>::R2C_SMEM, nrows, stream, in, out,
+                                     map, nrows, mmax, tw, twr, err, limit_ns);
+        }
     }
     return launch_r2c_impl<C, false>(in, out, nrows, mmax, mmajor, tw, twr, err, stream);
 }
@@ -375,6 +640,16 @@ cudaError_t launch_c2r(const float2* in, float* out, int64_t nrows, int mmax, in
                                             limit_ns, stream);
         else
             return cudaErrorNotSupported;
+    }
+    if constexpr (kRealPersistent && C::LOG2N >= 8 && C::LOG2N <= 11) {
+        using PC = FftCfg<C::LOG2N, C::MAXRB, 1, false>;  // two rows per tile
+        if (real_use_tma<PC>(nrows, mmajor)) {
+            CUtensorMap map;
+            cudaError_t e = encode_spectrum_map<PC>(&map, in, nrows, mmax);
+            if (e != cudaSuccess) return e;
+            return launch_real_p<PC>(k_c2r_p<PC>, RealPCfg<PC>::C2R_SMEM, nrows, stream, map, in,
+                                     out, nrows, mmax, tw, twr, err, limit_ns);
+        }
     }
     return launch_c2r_impl<C, false>(in, out, nrows, mmax, mmajor, tw, twr, err, limit_ns,
                                      stream);

@@ -237,3 +237,34 @@ def test_long_real_rows(n, mmaxes, layout):
         assert_parity(G, oracle.r2c_direct(x, mmax), mmax + 1,
                       f"long r2c n={n} mmax={mmax} {layout}",
                       scale=np.linalg.norm(x.astype(np.float64), axis=1))
+
+
+@pytest.mark.parametrize("pairing", [False, True])
+def test_any_length_real_large_batch_sampled(pairing):
+    """Real rows of 1000 points in a batch large enough for the radix-64 chirp-z schedule (the
+    small batches above take the radix-16 one): sampled rows against the direct sums."""
+    m = fx()
+    n, rows, mmax = 1000, 12000, 333
+    assert "radix=64x32" in m.query(n, rows, 1, m.INVERSE, m.LAYOUT_REAL_MMAJOR)
+    F = wl().spectrum(7950, rows, mmax)
+    syn = m.Plan(n, rows, 1, m.INVERSE, layout=m.LAYOUT_REAL_MMAJOR, mmax=mmax, pairing=pairing)
+    ana = m.Plan(n, rows, 1, m.FORWARD, layout=m.LAYOUT_REAL_MMAJOR, mmax=mmax, pairing=pairing)
+    x = syn.c2r(torch.from_numpy(np.ascontiguousarray(oracle.to_mmajor(F), dtype=np.complex64)).cuda())
+    G = ana.r2c(x)
+    torch.cuda.synchronize()
+    syn.check()
+    ana.check()
+    pick = np.array(sorted({0, 1, rows - 2, rows - 1, *np.random.default_rng(7950).integers(0, rows, 28).tolist()}))
+    xs = x.cpu().numpy()[pick]
+    ref_x = oracle.c2r_direct(F[pick], n)
+    scale_x = np.sqrt(np.mean(ref_x ** 2, axis=1))
+    if pairing:  # a row's error is set by its pair (rows 2p, 2p+1 share one transform)
+        xall = oracle.c2r_direct(F[pick ^ 1], n)
+        scale_x = np.hypot(scale_x, np.sqrt(np.mean(xall ** 2, axis=1)))
+    assert_parity(xs, ref_x, n, f"large real batch synthesis pairing={pairing}", scale=scale_x)
+    Gs = oracle.from_mmajor(G.cpu().numpy())[pick]
+    ref_G = oracle.r2c_direct(xs.astype(np.float64), mmax)
+    scale_G = np.linalg.norm(xs.astype(np.float64), axis=1)
+    if pairing:
+        scale_G = np.hypot(scale_G, np.linalg.norm(x.cpu().numpy()[pick ^ 1].astype(np.float64), axis=1))
+    assert_parity(Gs, ref_G, mmax + 1, f"large real batch analysis pairing={pairing}", scale=scale_G)

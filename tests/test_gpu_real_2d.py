@@ -207,6 +207,27 @@ def test_wait_timeout_real_synthesis():
     assert_parity(x.cpu().numpy(), oracle.c2r(F, n), n, "after timeout")
 
 
+def test_wait_timeout_real_analysis():
+    """The persistent analysis kernel (m-major spectrum, even row count) waits on bulk copies of
+    its real rows: a forced timeout is reported, and the next run is correct."""
+    m = fx()
+    n, rows, mmax = 4096, 64, 1365
+    p = m.Plan(n, rows, 1, m.FORWARD, layout=LAYOUTS["mmajor"], mmax=mmax)
+    x = wl().real_normal(960, rows, n)
+    xd = torch.from_numpy(x).cuda()
+    p.set_wait_timeout(0)
+    p.r2c(xd)
+    with pytest.raises(m.GbfftError) as ei:
+        p.check()
+    assert ei.value.status == m.FFT_ERR_TIMEOUT
+    p.set_wait_timeout(2_000_000_000)
+    F = p.r2c(xd)
+    torch.cuda.synchronize()
+    p.check()
+    assert_parity(oracle.from_mmajor(F.cpu().numpy()), oracle.r2c(x, mmax), mmax + 1,
+                  "analysis after timeout", scale=np.linalg.norm(x.astype(np.float64), axis=1))
+
+
 # ---- the Nyquist bin: mmax = n/2, the full n/2 + 1 half spectrum -----------------------------
 @pytest.mark.parametrize("n", [4, 8, 64, 4096, 1 << 15, 1000, 6000])
 @pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
