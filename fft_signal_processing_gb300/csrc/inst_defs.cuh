@@ -28,11 +28,6 @@ cudaError_t rows_impl(const float2* in, float2* out, int64_t nrows, const float2
         (void)lim;
         return launch_small<L, DIR>(in, out, nrows, flags, rp, s);
     } else if constexpr (L >= kRowsTmaMinLog2 && L <= kRowsTmaMaxLog2) {
-        if constexpr (L == 12 && k2dRowStages != kRowsTmaStages) {
-            if (rp)  // the row pass of a 4096-wide image (a short batch of rows)
-                return launch_rows_tma<RowsTmaCfg<L, rows_maxrb(L), k2dRowStages>, DIR>(
-                    in, out, nrows, tw, flags, rp, err, lim, s);
-        }
         return launch_rows_tma<RowsTmaCfg<L, rows_maxrb(L), kRowsTmaStages>, DIR>(
             in, out, nrows, tw, flags, rp, err, lim, s);
     } else {

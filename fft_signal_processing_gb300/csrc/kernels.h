@@ -57,8 +57,6 @@ cudaError_t run_rows(int log2n, int dir, const float2* in, float2* out, int64_t 
 constexpr int kRowsTmaMinLog2 = 5;
 constexpr int kRowsTmaMaxLog2 = 12;
 constexpr int kRowsTmaStages = 1;  // one stage per CTA: six CTAs per SM at 2^12
-// Stages of the row pass of 4096-wide images (4096 rows an image: about 4.5 rows per CTA).
-constexpr int k2dRowStages = 1;
 
 // Strided columns: count columns of matrices [2^log2l][2^log2s] stored back to back.
 // elem_parity: 1 for the 2-D chessboard (-1)^(row+col), 0 for the four-step one (-1)^col.
