@@ -4,7 +4,8 @@
 // Paths (chosen at plan creation, as the WGSL "src/sht/wgsl/fourier.ts" selects its 'fft' or
 // 'dft' implementation at plan creation):
 //   onepass   dims 1, n <= 2^14: one kernel, each row resident in one CTA.
-//   fourstep  dims 1, 2^15 <= n <= 2^24: n = N1*N2 with n = n1*N2 + n2 and k = k1 + N1*k2.
+//   fourstep  dims 1, 2^15 <= n <= 2^24 (from 2^12 when GBFFT_FORCE_PATH=fourstep):
+//             n = N1*N2 with n = n1*N2 + n2 and k = k1 + N1*k2.
 //             Pass 1 does the N1-point transforms down the N2 columns and multiplies output
 //             (k1, n2) by w_n^{n2*k1}; pass 2 does the N2-point row transforms and writes row
 //             k1's output k2 to X[k1 + N1*k2].  This is the four-step FFT the CS598 project page
@@ -25,6 +26,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -61,6 +63,19 @@ struct PlanSpec {
     int log2ny = 0;
 };
 
+// Test override of the path choice (environment variable GBFFT_FORCE_PATH, read at every plan
+// creation or query): "fourstep" plans C2C rows of 2^12..2^14 points, whose default is the
+// one-pass kernel, as the two-pass four-step transform (N2 = 2^8, N1 = n/2^8: the smallest
+// split both passes serve); "onepass" or unset keeps the default choice everywhere.  Returns
+// 1 to force the four-step path, 0 for the default, -1 for any other value.
+int forced_path() {
+    const char* v = std::getenv("GBFFT_FORCE_PATH");
+    if (!v || !*v || !std::strcmp(v, "onepass")) return 0;
+    return std::strcmp(v, "fourstep") ? -1 : 1;
+}
+constexpr int kForcedFourStepMinLog2 = 12;  // N1 = 2^4 is the row pass's block of 16 rows
+constexpr int kForcedFourStepLog2N2 = 8;    // the smallest four-step row pass
+
 int ilog2_exact(int64_t n) {
     if (n < 1 || (n & (n - 1))) return -1;
     int l = 0;
@@ -80,6 +95,8 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
         return FFT_ERR_INVALID_ARG;
     if (shift != 0 && shift != 1) return FFT_ERR_INVALID_ARG;
     if (layout != FFT_LAYOUT_C2C && (dims != 1 || shift)) return FFT_ERR_INVALID_ARG;
+    const int force = forced_path();
+    if (force < 0) return FFT_ERR_INVALID_ARG;
     const int l = ilog2_exact(n);
     // lengths that are not powers of two: rows (complex or real) up to kMaxBluesteinMpN
     const bool any_length = l < 0 && dims == 1 && n >= 3 && n <= kMaxBluesteinMpN;
@@ -111,7 +128,12 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
         s.path = PATH_2D;
     } else {
         if (l > FFT_MAX_LOG2N_1D) return FFT_ERR_UNSUPPORTED_SIZE;
-        if (l <= kMaxLog2OnePass) {
+        if (force == 1 && l >= kForcedFourStepMinLog2 && l <= kMaxLog2OnePass) {
+            s.path = PATH_FOURSTEP;
+            s.log2n2 = kForcedFourStepLog2N2;
+            s.log2n1 = l - kForcedFourStepLog2N2;
+            s.lowbits = (l + 1) / 2;
+        } else if (l <= kMaxLog2OnePass) {
             s.path = PATH_ONEPASS;
         } else {
             s.path = PATH_FOURSTEP;

@@ -100,6 +100,11 @@ enum {
  * The plan allocates its device twiddle tables, its workspace (large 1-D sizes only) and a
  * device error word with cudaMalloc on the current device, and copies the tables (computed on
  * the host in double precision and rounded once to float) synchronously.
+ * Test override: the environment variable GBFFT_FORCE_PATH, read at every plan creation and
+ * query, set to "fourstep" plans C2C rows of 2^12 <= n <= 2^14 points (whose default is a
+ * single kernel per row) as the two-pass four-step transform with N2 = 256, N1 = n/256, with a
+ * workspace of batch*n complex64; "onepass" or unset leaves every choice at its default; any
+ * other value makes plan creation and query return FFT_ERR_INVALID_ARG.
  * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_UNSUPPORTED_SIZE, FFT_ERR_OOM or FFT_ERR_CUDA;
  * on error *out is set to NULL and nothing is left allocated.
  */

@@ -142,6 +142,27 @@ def test_path_choice(n, path, radix):
         assert f"n1={1 << (l // 2)} n2={1 << (l - l // 2)}" in d
 
 
+def test_forced_path_override(monkeypatch):
+    """GBFFT_FORCE_PATH (test override, read at each plan creation or query): "fourstep" plans
+    C2C rows of 2^12..2^14 points as N1 x 256 four-step transforms and changes nothing else;
+    "onepass" or an empty value keeps the default; any other value is an argument error."""
+    monkeypatch.setenv("GBFFT_FORCE_PATH", "fourstep")
+    for l in (12, 13, 14):
+        d = fx.query(1 << l, 3)
+        assert "path=fourstep" in d and f"n1={1 << (l - 8)} n2=256" in d
+    assert "path=onepass" in fx.query(2048, 3)
+    assert f"n1={1 << 7} n2={1 << 8}" in fx.query(1 << 15, 3)
+    assert "path=2d" in fx.query(4096, 1, dims=2)
+    assert "path=real" in fx.query(4096, 8, layout=2, direction=1)
+    for v in ("onepass", ""):
+        monkeypatch.setenv("GBFFT_FORCE_PATH", v)
+        assert "path=onepass" in fx.query(4096, 3)
+    monkeypatch.setenv("GBFFT_FORCE_PATH", "four-step")
+    assert q(4096) == fx.FFT_ERR_INVALID_ARG
+    monkeypatch.delenv("GBFFT_FORCE_PATH")
+    assert "path=onepass" in fx.query(4096, 3)
+
+
 def test_2d_and_real_paths():
     assert "path=2d" in fx.query(4096, 1, dims=2, shift=True)
     d = fx.query(4096, 2048, layout=2, direction=1)

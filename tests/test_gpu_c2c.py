@@ -98,6 +98,34 @@ def test_fourstep_shift_and_in_place(log2n, direction):
     assert_parity(got, oracle.transform(x, direction, 1, True), n, f"four-step shift n={n}")
 
 
+# ---- the four-step path forced at one-pass sizes (GBFFT_FORCE_PATH, test override) -----------
+@pytest.mark.parametrize("log2n", [12, 13, 14])
+@pytest.mark.parametrize("direction", [-1, 1])
+@pytest.mark.parametrize("shift", [False, True])
+def test_forced_fourstep_matches_oracle(log2n, direction, shift, monkeypatch):
+    """n = 2^12..2^14 planned as N1 x 256 four-step transforms (short strided columns with the
+    twiddle w_n^{n2*k1} on their store, then transposed 256-point rows), compared with the
+    oracle and with the default one-pass plan on the same input; normalised as well."""
+    m = fx()
+    n, batch = 1 << log2n, 5
+    x = rng_c64(6000 + log2n + 10 * (direction > 0) + 20 * shift, batch, n)
+    ref = oracle.transform(x, direction, 1, shift)
+    monkeypatch.setenv("GBFFT_FORCE_PATH", "fourstep")
+    p = m.Plan(n, batch, 1, direction, shift=shift)
+    assert f"path=fourstep n={n}" in p.describe() and f"n1={n >> 8} n2=256" in p.describe()
+    xd = torch.from_numpy(np.ascontiguousarray(x, dtype=np.complex64)).cuda()
+    y = p.c2c(xd)
+    p.set_normalization(True)
+    yn = p.c2c(xd)
+    torch.cuda.synchronize()
+    p.check()
+    p.close()
+    assert_parity(y.cpu().numpy(), ref, n, f"forced four-step n={n} dir={direction} shift={shift}")
+    assert_parity(yn.cpu().numpy(), ref / n, n, f"forced four-step normalised n={n}")
+    monkeypatch.delenv("GBFFT_FORCE_PATH")
+    assert_parity(gpu_c2c(x, n, batch, direction, shift), ref, n, f"one-pass n={n}")
+
+
 # ---- bit-exact cases (exact fp32 arithmetic) --------------------------------------------------
 @pytest.mark.parametrize("n", [1, 2, 4])
 @pytest.mark.parametrize("direction", [-1, 1])
