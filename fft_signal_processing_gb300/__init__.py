@@ -29,8 +29,13 @@ FFT_ERR_MISALIGNED = -3
 FFT_ERR_OOM = -4
 FFT_ERR_CUDA = -5
 FFT_ERR_TIMEOUT = -6
+FFT_ERR_BOUNDS = -7
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgbfft.so")
+# GBFFT_CHECKED=1 in the environment (tests) loads the checked build, libgbfft_checked.so:
+# the same kernels with device-side index checks that report FFT_ERR_BOUNDS.
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libgbfft_checked.so" if os.environ.get("GBFFT_CHECKED") == "1"
+                        else "libgbfft.so")
 
 # Exported C symbols (kept in step with include/gbfft.h; checked by the tests).
 ABI_SYMBOLS = (
@@ -57,8 +62,9 @@ def lib():
     global _LIB
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libgbfft.so is not built ({LIB_PATH}); "
-                               "run `python -c 'import __graft_entry__ as g; g.build()'`")
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); "
+                               "run `python -c 'import __graft_entry__ as g; g.build()'` "
+                               "(or `python fft_signal_processing_gb300/_build.py --checked`)")
         L = ctypes.CDLL(LIB_PATH)
         i64, ci, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
         L.fft_plan_create.argtypes = [i64, i64, ci, ci, ci, ci, ctypes.POINTER(vp)]

@@ -379,6 +379,8 @@ const char* fft_status_string(int status) {
         case FFT_ERR_OOM: return "FFT_ERR_OOM: device allocation failed";
         case FFT_ERR_CUDA: return "FFT_ERR_CUDA: CUDA runtime or launch error";
         case FFT_ERR_TIMEOUT: return "FFT_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case FFT_ERR_BOUNDS:
+            return "FFT_ERR_BOUNDS: a device index check of the checked build failed";
         default: return "unknown status";
     }
 }
@@ -736,7 +738,7 @@ int fft_plan_check(fft_plan p) {
         return FFT_ERR_CUDA;
     if (h != 0) {
         if (cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess) return FFT_ERR_CUDA;
-        return h == KERR_WAIT_TIMEOUT ? FFT_ERR_TIMEOUT : FFT_ERR_CUDA;
+        return kerr_status(h);
     }
     return FFT_OK;
 }

@@ -128,7 +128,9 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     auto issue = [&](int64_t tile) {
         const int z = (int)(tile / tiles_per_mat);
         const int x = (int)((tile % tiles_per_mat) * W);
-        mbar_arrive_expect_tx(&bar, RC::TILE_BYTES);
+        const bool ok = check_box(x, W, S, 0, RC::NBOX * RC::BH, C::N, z, nmat, 8, err);
+        mbar_arrive_expect_tx(&bar, ok ? (uint32_t)RC::TILE_BYTES : 0u);
+        if (!ok) return;
 #pragma unroll 1
         for (int b = 0; b < RC::NBOX; ++b)
             tma_load_3d(smem + b * RC::BH * W, &imap, x, b * RC::BH, z, &bar);
@@ -184,7 +186,10 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
             for (int r = 0; r < R0; ++r) {
                 const int e = j + r * S0;
                 float2 xv = smem[e * W + w];  // dense [row][W] tile written by the copy engine
-                if constexpr (PRE) xv = cmul(xv, __ldg(twd.pre + ((int64_t)e << log2s) + c));
+                if constexpr (PRE) {
+                    const int64_t q = ((int64_t)e << log2s) + c;
+                    if (check_range(q, 1, S << C::LOG2N, err)) xv = cmul(xv, __ldg(twd.pre + q));
+                }
                 if (flags & KF_CHESS_LOAD) xv = neg_if(xv, (e * elem_parity + cp) & 1);
                 v[b * R0 + r] = xv;
             }
@@ -236,9 +241,11 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         fence_proxy_async_smem();  // make this thread's tile writes visible to the copy engine
         __syncthreads();
         if (tid == 0) {
+            if (check_box(x, W, S, 0, RC::NBOX * RC::BH, C::N, z, nmat, 8, err)) {
 #pragma unroll 1
-            for (int b = 0; b < RC::NBOX; ++b)
-                tma_store_3d(&omap, x, b * RC::BH, z, smem + b * RC::BH * W);
+                for (int b = 0; b < RC::NBOX; ++b)
+                    tma_store_3d(&omap, x, b * RC::BH, z, smem + b * RC::BH * W);
+            }
             bulk_commit();
             bulk_wait_smem_read();  // the stage may be refilled once the stores have read it
             const int64_t nt = tile + tstride;

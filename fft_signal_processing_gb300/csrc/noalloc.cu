@@ -113,7 +113,7 @@ int query_status(cudaStream_t s) {
         return FFT_ERR_CUDA;
     if (h == 0) return FFT_OK;
     if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return FFT_ERR_CUDA;
-    return h == KERR_WAIT_TIMEOUT ? FFT_ERR_TIMEOUT : FFT_ERR_CUDA;
+    return kerr_status(h);
 }
 
 }  // namespace

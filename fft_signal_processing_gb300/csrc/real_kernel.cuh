@@ -60,13 +60,14 @@ __global__ void __launch_bounds__(C::THREADS)
     constexpr int B0 = C::E / R0;
     constexpr int S0 = C::N / R0;
     float2 v[C::E];
-    const float2* src = reinterpret_cast<const float2*>(in) + (active ? row * H : 0);
+    const bool inside = active && check_range(row * H, H, nrows * H, err);
+    const float2* src = reinterpret_cast<const float2*>(in) + (inside ? row * H : 0);
 #pragma unroll
     for (int b = 0; b < B0; ++b) {
         const int j = t + b * C::T;
 #pragma unroll
         for (int r = 0; r < R0; ++r)
-            v[b * R0 + r] = active ? ldg_stream(src + j + r * S0) : make_float2(0.f, 0.f);
+            v[b * R0 + r] = inside ? ldg_stream(src + j + r * S0) : make_float2(0.f, 0.f);
     }
     if constexpr (IDX)
         identity_passes<C>(v, t, smem + w);
@@ -112,11 +113,13 @@ __global__ void __launch_bounds__(C::THREADS)
         __syncthreads();
         if (threadIdx.x == 0) {
             for (int b = 0; b < NB && b * BK <= mmax; ++b)
-                tma_store_2d(&fmap, (int)row0, b * BK, smem + b * BK * W);
+                if (check_box(row0, 1, nrows, b * BK, 1, mmax + 1, 0, 1, 8, err))
+                    tma_store_2d(&fmap, (int)row0, b * BK, smem + b * BK * W);
             bulk_commit();
             bulk_wait_smem_read();  // shared memory stays valid until the stores have read it
         }
-        if (mmax == H && (int)threadIdx.x < W && row0 + threadIdx.x < nrows)  // X_H, real
+        if (mmax == H && (int)threadIdx.x < W && row0 + threadIdx.x < nrows &&  // X_H, real
+            check_range((int64_t)H * nrows + row0 + threadIdx.x, 1, (int64_t)(mmax + 1) * nrows, err))
             stg_stream(out + (int64_t)H * nrows + row0 + threadIdx.x,
                        IDX ? z0 : make_float2(z0.x - z0.y, 0.f));
     } else {
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(C::THREADS)
                 y = recombine(smem[k * W + wr], smem[((H - k) & (H - 1)) * W + wr], k);
             }
             const int64_t o = mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k;
-            stg_stream(out + o, y);
+            if (check_range(o, 1, (int64_t)(mmax + 1) * nrows, err)) stg_stream(out + o, y);
         }
     }
 }
@@ -171,8 +174,10 @@ __global__ void __launch_bounds__(C::THREADS)
             prefetch_tensormap(&fmap);
             mbar_init(&bar, 1);
             fence_mbar_init();
-            mbar_arrive_expect_tx(&bar, (uint32_t)(H * W * 8));
-            for (int b = 0; b < NB; ++b) tma_load_2d(smem + b * BK * W, &fmap, (int)row0, b * BK, &bar);
+            const bool ok = check_box(row0, 1, nrows, 0, NB * BK, H, 0, 1, 8, err);
+            mbar_arrive_expect_tx(&bar, ok ? (uint32_t)(H * W * 8) : 0u);
+            if (ok)
+                for (int b = 0; b < NB; ++b) tma_load_2d(smem + b * BK * W, &fmap, (int)row0, b * BK, &bar);
         }
         __syncthreads();
         const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
@@ -187,7 +192,8 @@ __global__ void __launch_bounds__(C::THREADS)
             smem[threadIdx.x].y = 0.f;  // X_0 = Re F_0
             // X_H = Re F_H with the Nyquist bin, else 0 (the tensor copies stop below H)
             float2 xh = make_float2(0.f, 0.f);
-            if (mmax == H && row0 + threadIdx.x < nrows)
+            if (mmax == H && row0 + threadIdx.x < nrows &&
+                check_range((int64_t)H * nrows + row0 + threadIdx.x, 1, (int64_t)(mmax + 1) * nrows, err))
                 xh.x = ldg_stream(in + (int64_t)H * nrows + row0 + threadIdx.x).x;
             smem[H * W + threadIdx.x] = xh;
         }
@@ -200,8 +206,9 @@ __global__ void __launch_bounds__(C::THREADS)
             const int wr = i % W, k = i / W;
             const int64_t rr = row0 + wr;
             float2 x = make_float2(0.f, 0.f);
-            if (rr < nrows && k <= mmax) {
-                x = ldg_stream(in + (mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k));
+            const int64_t o = mmajor ? (int64_t)k * nrows + rr : rr * (mmax + 1) + k;
+            if (rr < nrows && k <= mmax && check_range(o, 1, (int64_t)(mmax + 1) * nrows, err)) {
+                x = ldg_stream(in + o);
                 if (k == 0 || k == H) x.y = 0.f;  // X_0, X_H real
             }
             smem[k * W + wr] = x;
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(C::THREADS)
     constexpr int RL = C::radix(C::NPASS - 1);
     constexpr int BL = C::E / RL;
     constexpr int SL = C::N / RL;
-    if (active) {
+    if (active && check_range(row * H, H, nrows * H, err)) {
         float2* dst = reinterpret_cast<float2*>(out) + row * H;  // x_{2m}, x_{2m+1} = z_m
 #pragma unroll
         for (int b = 0; b < BL; ++b) {
@@ -377,9 +384,13 @@ struct RealPCfg {
     static_assert((C2R_STAGE * 8) % 128 == 0 && (R2C_STAGE * 8) % 128 == 0,
                   "the exchange area stays 128-byte aligned");
 };
+// CTAs per SM the registers must allow: the shared memory holds three tiles' worth at the
+// 2048-point core (67.6 KB each), and the synthesis would otherwise take 105 registers and run
+// two CTAs per SM (80 registers at this bound, no spills).
+constexpr int kRealPMinCtas = 3;
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::THREADS, kRealPMinCtas)
     k_c2r_p(const __grid_constant__ CUtensorMap fmap, const float2* in, float* out,
             int64_t nrows, int mmax, const float2* __restrict__ tw,
             const float2* __restrict__ twr, int* err, uint64_t limit_ns) {
@@ -398,7 +409,9 @@ __global__ void __launch_bounds__(C::THREADS)
     const int64_t t0 = blockIdx.x, tstride = gridDim.x;
 
     auto issue = [&](int64_t tile) {  // the full box counts toward the bytes, OOB fill included
-        mbar_arrive_expect_tx(&bar, (uint32_t)(H * W * 8));
+        const bool ok = check_box(tile * W, 1, nrows, 0, P::NB * P::BK, H, 0, 1, 8, err);
+        mbar_arrive_expect_tx(&bar, ok ? (uint32_t)(H * W * 8) : 0u);
+        if (!ok) return;
 #pragma unroll 1
         for (int b = 0; b < P::NB; ++b)
             tma_load_2d(stage + b * P::BK * W, &fmap, (int)(tile * W), b * P::BK, &bar);
@@ -434,7 +447,9 @@ __global__ void __launch_bounds__(C::THREADS)
         const bool active = row < nrows;
         // X_H: the Nyquist bin (real) when mmax = H, else 0 (the stage holds k < H)
         float2 xh = make_float2(0.f, 0.f);
-        if (mmax == H && active) xh.x = ldg_stream(in + (int64_t)H * nrows + row).x;
+        if (mmax == H && active &&
+            check_range((int64_t)H * nrows + row, 1, (int64_t)(mmax + 1) * nrows, err))
+            xh.x = ldg_stream(in + (int64_t)H * nrows + row).x;
         // Z_k = (X_k + conj X_{H-k}) + i e^{+i th_k} (X_k - conj X_{H-k}), X_0 real
         float2 v[C::E];
 #pragma unroll
@@ -461,7 +476,7 @@ __global__ void __launch_bounds__(C::THREADS)
             }
         }
         run_passes<C, +1, 0>(v, t, work + w, tw);
-        if (active) {
+        if (active && check_range(row * H, H, nrows * H, err)) {
             float2* dst = reinterpret_cast<float2*>(out) + row * H;  // x_{2m}, x_{2m+1} = z_m
 #pragma unroll
             for (int b = 0; b < BL; ++b) {
@@ -474,7 +489,7 @@ __global__ void __launch_bounds__(C::THREADS)
 }
 
 template <class C>
-__global__ void __launch_bounds__(C::THREADS)
+__global__ void __launch_bounds__(C::THREADS, kRealPMinCtas)
     k_r2c_p(const float* in, float2* out, const __grid_constant__ CUtensorMap fmap,
             int64_t nrows, int mmax, const float2* __restrict__ tw,
             const float2* __restrict__ twr, int* err, uint64_t limit_ns) {
@@ -496,7 +511,9 @@ __global__ void __launch_bounds__(C::THREADS)
     auto issue = [&](int64_t tile) {
         const int64_t r0 = tile * W;
         const int rows = nrows - r0 < W ? (int)(nrows - r0) : W;
-        mbar_arrive_expect_tx(&bar, (uint32_t)rows * H * 8u);
+        const bool ok = check_range(r0 * H, (int64_t)rows * H, nrows * H, err);
+        mbar_arrive_expect_tx(&bar, ok ? (uint32_t)rows * H * 8u : 0u);
+        if (!ok) return;
 #pragma unroll 1
         for (int r = 0; r < rows; ++r)
             bulk_load(stage + r * P::INROW, zin + (r0 + r) * H, (uint32_t)H * 8u, &bar);
@@ -578,11 +595,13 @@ __global__ void __launch_bounds__(C::THREADS)
         __syncthreads();
         if (tid == 0) {
             for (int b = 0; b < P::NB && b * P::BK <= mmax; ++b)
-                tma_store_2d(&fmap, (int)row0, b * P::BK, work + b * P::BK * W);
+                if (check_box(row0, 1, nrows, b * P::BK, 1, mmax + 1, 0, 1, 8, err))
+                    tma_store_2d(&fmap, (int)row0, b * P::BK, work + b * P::BK * W);
             bulk_commit();
             bulk_wait_smem_read();  // the exchange area may be rewritten once the stores read it
         }
-        if (mmax == H && tid < W && row0 + tid < nrows)  // X_H = Re Z_0 - Im Z_0, real
+        if (mmax == H && tid < W && row0 + tid < nrows &&  // X_H = Re Z_0 - Im Z_0, real
+            check_range((int64_t)H * nrows + row0 + tid, 1, (int64_t)(mmax + 1) * nrows, err))
             stg_stream(out + (int64_t)H * nrows + row0 + tid, make_float2(z0.x - z0.y, 0.f));
     }
 }

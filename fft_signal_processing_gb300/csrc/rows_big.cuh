@@ -104,8 +104,9 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     const int64_t r0 = blockIdx.x, rstride = gridDim.x;
 
     auto issue = [&](int64_t row) {
-        mbar_arrive_expect_tx(&bar, (uint32_t)RC::STAGE_BYTES);
-        bulk_load(stage, in + row * N, (uint32_t)RC::STAGE_BYTES, &bar);
+        const bool ok = check_range(row * N, N, nrows * N, err);
+        mbar_arrive_expect_tx(&bar, ok ? (uint32_t)RC::STAGE_BYTES : 0u);
+        if (ok) bulk_load(stage, in + row * N, (uint32_t)RC::STAGE_BYTES, &bar);
     };
 
     if (t == 0) {
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
 
         run_passes_split<C, DIR, 0>(v, t, xb, tw);
 
+        if (!check_range(row * N, N, nrows * N, err)) continue;
         float2* dst = out + row * N;
 #pragma unroll
         for (int b = 0; b < BL; ++b) {

@@ -61,8 +61,10 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     auto issue = [&](int s, int64_t blk) {  // never copy into a misaligned stage; the waits will give up
         const int64_t rows = nrows - blk * RC::W < RC::W ? nrows - blk * RC::W : RC::W;
         const uint32_t bytes = (uint32_t)rows * N * 8u;
-        mbar_arrive_expect_tx(&bars[s], bytes);
-        bulk_load(smem + s * RC::STAGE, in + blk * RC::W * N, bytes, &bars[s]);
+        const bool ok = check_range(blk * RC::W * N, rows * N, nrows * N, err) &&
+                        check_range(s * RC::STAGE, rows * N, NST * RC::STAGE, err);
+        mbar_arrive_expect_tx(&bars[s], ok ? bytes : 0u);
+        if (ok) bulk_load(smem + s * RC::STAGE, in + blk * RC::W * N, bytes, &bars[s]);
     };
 
     __shared__ int stage_bad;
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         else
             run_passes<C, DIR, 0>(v, t, sbuf + w * RC::SROW, tw);
 
-        if (active) {
+        if (active && check_range(row * N, N, nrows * N, err)) {
             float2* dst = out + row * N;
 #pragma unroll
             for (int b = 0; b < BL; ++b) {

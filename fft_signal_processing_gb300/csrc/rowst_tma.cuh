@@ -58,7 +58,9 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     const int64_t n1 = int64_t(1) << log2n1;
 
     auto issue = [&](int64_t blk) {
-        mbar_arrive_expect_tx(&bar, RC::BLOCK_BYTES);
+        const bool ok = check_range(blk * W * N, W * N, nrows * N, err);
+        mbar_arrive_expect_tx(&bar, ok ? (uint32_t)RC::BLOCK_BYTES : 0u);
+        if (!ok) return;
 #pragma unroll 1
         for (int r = 0; r < W; ++r)
             bulk_load(smem + r * RC::INROW, in + (blk * W + r) * N, (uint32_t)N * 8u, &bar);
@@ -128,9 +130,11 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
+            if (check_box(x, W, n1, 0, RC::NBOX * RC::BH, N, z, nrows >> log2n1, 8, err)) {
 #pragma unroll 1
-            for (int b = 0; b < RC::NBOX; ++b)
-                tma_store_3d(&omap, x, b * RC::BH, z, smem + b * RC::BH * W);
+                for (int b = 0; b < RC::NBOX; ++b)
+                    tma_store_3d(&omap, x, b * RC::BH, z, smem + b * RC::BH * W);
+            }
             bulk_commit();
             bulk_wait_smem_read();
             const int64_t nb = blk + bstride;

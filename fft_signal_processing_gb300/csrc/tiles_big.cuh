@@ -74,7 +74,9 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     auto issue = [&](int64_t tile) {
         const int z = (int)(tile / tiles_per_mat);
         const int x = (int)((tile % tiles_per_mat) * W);
-        mbar_arrive_expect_tx(&bar, RC::TILE_BYTES);
+        const bool ok = check_box(x, W, S, 0, RC::NBOX * RC::BH, C::N, z, nmat, 8, err);
+        mbar_arrive_expect_tx(&bar, ok ? (uint32_t)RC::TILE_BYTES : 0u);
+        if (!ok) return;
 #pragma unroll 1
         for (int b = 0; b < RC::NBOX; ++b)
             tma_load_3d(stage + b * RC::BH * W, &imap, x, b * RC::BH, z, &bar);
@@ -167,6 +169,9 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
                 }
             }
         }
+        if (!check_range(((int64_t)z << (log2s + C::LOG2N)) + c, 1, nmat << (log2s + C::LOG2N), err) ||
+            !check_range(c, 1, S, err))
+            continue;
         float2* dst = out + ((int64_t)z << (log2s + C::LOG2N)) + c;
 #pragma unroll
         for (int b = 0; b < BL; ++b) {
@@ -260,7 +265,9 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
     const int64_t n1 = int64_t(1) << log2n1;
 
     auto issue = [&](int64_t blk) {
-        mbar_arrive_expect_tx(&bar, RC::BLOCK_BYTES);
+        const bool ok = check_range(blk * W * N, W * N, nrows * N, err);
+        mbar_arrive_expect_tx(&bar, ok ? (uint32_t)RC::BLOCK_BYTES : 0u);
+        if (!ok) return;
 #pragma unroll 1
         for (int r = 0; r < W; ++r)
             bulk_load(stage + r * RC::INROW, in + (blk * W + r) * N, (uint32_t)N * 8u, &bar);
@@ -316,6 +323,9 @@ __global__ void __launch_bounds__(RC::C::THREADS, RC::MIN_CTAS)
 
         run_passes_split<C, DIR, 0>(v, t, xb + w, tw);
 
+        // output k2 of this row lands at k1 + N1*k2 of its transform
+        if (!check_range(((zt << log2n1) << C::LOG2N) + k1, (int64_t)(N - 1) * n1 + 1, nrows * N, err))
+            continue;
         float2* dst = out + ((zt << log2n1) << C::LOG2N) + k1;
 #pragma unroll
         for (int b = 0; b < BL; ++b) {

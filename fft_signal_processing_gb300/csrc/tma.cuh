@@ -5,6 +5,7 @@
 
 #include <stdint.h>
 
+#include "../../include/gbfft.h"
 #include "launch_cache.cuh"
 
 namespace gbfft {
@@ -87,7 +88,54 @@ constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s for draining copies af
 
 
 // Error word values written by kernels (read and cleared by fft_plan_check).
-enum : int { KERR_WAIT_TIMEOUT = 1, KERR_STAGE_ALIGN = 2 };
+enum : int { KERR_WAIT_TIMEOUT = 1, KERR_STAGE_ALIGN = 2, KERR_BOUNDS = 3 };
+// The status an exec call's error word maps to (a misaligned stage is a CUDA-level failure).
+inline int kerr_status(int h) {
+    return h == 0                   ? FFT_OK
+           : h == KERR_WAIT_TIMEOUT ? FFT_ERR_TIMEOUT
+           : h == KERR_BOUNDS       ? FFT_ERR_BOUNDS
+                                    : FFT_ERR_CUDA;
+}
+
+// ---- checked build ------------------------------------------------------------------------
+// Built with -DGBFFT_CHECKED (libgbfft_checked.so), the copy-engine kernels test each run-time
+// index of a global access, and each tensor-copy coordinate, against the extent of its buffer or
+// tensor before using it.  A failing test records KERR_BOUNDS in *err (the first error kept;
+// err may be NULL) and the access is skipped; a skipped load still completes its barrier phase,
+// without data, so that no wait runs out.  In the normal build every test compiles away.
+#ifdef GBFFT_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+__device__ __forceinline__ bool bounds_fail(int* err) {
+    if (err) atomicCAS(err, 0, KERR_BOUNDS);
+    return false;
+}
+// [first, first + count) inside [0, extent)
+__device__ __forceinline__ bool check_range(int64_t first, int64_t count, int64_t extent,
+                                            int* err) {
+    if constexpr (!kChecked) {
+        return true;
+    } else {
+        return (first >= 0 && count >= 0 && first <= extent - count) || bounds_fail(err);
+    }
+}
+// A tensor-copy box of w x h elements of `elem` bytes at (x, y) inside an xext x yext plane,
+// with x * elem a multiple of 16 bytes (the copy engine's rule for the innermost coordinate),
+// and a third coordinate z in [0, zext).
+__device__ __forceinline__ bool check_box(int64_t x, int w, int64_t xext, int64_t y, int h,
+                                          int64_t yext, int64_t z, int64_t zext, int elem,
+                                          int* err) {
+    if constexpr (!kChecked) {
+        return true;
+    } else {
+        return ((x * elem) % 16 == 0 && x >= 0 && x <= xext - w && y >= 0 && y <= yext - h &&
+                z >= 0 && z < zext) ||
+               bounds_fail(err);
+    }
+}
 
 // Self-check run once per CTA before its first asynchronous copy: the shared-memory stage must
 // start on a 128-byte boundary (copies need 16).  On failure the CTA records KERR_STAGE_ALIGN

@@ -57,7 +57,10 @@ enum {
     FFT_ERR_MISALIGNED = -3,       /* a data pointer is not 16-byte aligned */
     FFT_ERR_OOM = -4,              /* device allocation of tables or workspace failed */
     FFT_ERR_CUDA = -5,             /* a CUDA runtime call or kernel launch failed */
-    FFT_ERR_TIMEOUT = -6           /* a bounded device-side wait gave up (fft_plan_check) */
+    FFT_ERR_TIMEOUT = -6,          /* a bounded device-side wait gave up (fft_plan_check) */
+    FFT_ERR_BOUNDS = -7            /* checked build only (libgbfft_checked.so, compiled with
+                                      -DGBFFT_CHECKED): a device-side index or copy-coordinate
+                                      check failed and the access was skipped (fft_plan_check) */
 };
 
 /* Largest supported transform sizes. */
@@ -249,8 +252,9 @@ int fft_exec_c2r(fft_plan plan, const void* in, float* out, void* stream);
 /*
  * fft_plan_check - synchronise the device, then read and clear the plan's device error word.
  * Kernels that wait on device-side events give up after a bounded number of polls and set
- * this word instead of hanging.  Returns FFT_OK, FFT_ERR_TIMEOUT, FFT_ERR_INVALID_ARG or
- * FFT_ERR_CUDA (the synchronisation itself reported an error).
+ * this word instead of hanging.  Returns FFT_OK, FFT_ERR_TIMEOUT, FFT_ERR_INVALID_ARG,
+ * FFT_ERR_BOUNDS (checked build only: an index check failed) or FFT_ERR_CUDA (the
+ * synchronisation itself reported an error, or a copy stage was misaligned).
  */
 int fft_plan_check(fft_plan plan);
 

@@ -36,8 +36,9 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    for st in (0, -1, -2, -3, -4, -5, -6):
+    for st in (0, -1, -2, -3, -4, -5, -6, -7):
         assert fx.status_string(st).startswith("FFT_")
+    assert fx.status_string(fx.FFT_ERR_BOUNDS).startswith("FFT_ERR_BOUNDS")
     assert fx.status_string(-99) == "unknown status"
     assert fx.lib().fft_version() >= 10000
 
@@ -140,6 +141,19 @@ def test_path_choice(n, path, radix):
     l = n.bit_length() - 1
     if path == "fourstep":
         assert f"n1={1 << (l // 2)} n2={1 << (l - l // 2)}" in d
+
+
+def test_checked_build_links_and_exports_every_symbol():
+    """The checked variant (-DGBFFT_CHECKED) builds from the same sources and exports the same
+    ABI; its GPU behaviour is covered by tests/test_gpu_checked.py."""
+    import ctypes
+    from fft_signal_processing_gb300 import _build
+
+    path = _build.build(checked=True)
+    assert path.endswith("libgbfft_checked.so")
+    L = ctypes.CDLL(path)
+    for name in fx.ABI_SYMBOLS:
+        assert hasattr(L, name), name
 
 
 def test_forced_path_override(monkeypatch):
