@@ -8,7 +8,8 @@ resident in HBM.  The default workload is the batched 1-D C2C round trip: N = 40
 (-1)^j chessboard on its load, then the inverse transform (chessboard on its store) -- two
 kernel launches per step.  Other workloads (--workload): c2c_1024 (N = 1024 x 64 rows, forward),
 sweep_<log2n> (batch*N = 2^26 rows of 3 tones + noise, forward), any_<n> (the same for a
-length n <= 2^20 that is not a power of two: the chirp-z path), realany_<n> (the real
+length n <= 2^20 that is not a power of two: the mixed-radix path for n <= 8192 with prime
+factors 2, 3, 5, 7 only, else the chirp-z path), realany_<n> (the real
 workload below for such a length, mmax = n/3; realanypair_<n>: two rows per transform), real
 (2048 rows x 4096, mmax = 1365, synthesis then analysis, m-major spectrum; realpair: two rows
 per transform), 2d (4096 x 4096, forward with the 2-D
@@ -63,6 +64,15 @@ def parse():
 
 
 # ---- workloads ----------------------------------------------------------------------------------
+def any_length_path(n):
+    """The library's path for a length that is not a power of two (its planner's rule)."""
+    m = n
+    for f in (2, 3, 5, 7):
+        while m % f == 0:
+            m //= f
+    return "mixed-radix path" if m == 1 and n <= 8192 else "chirp-z path"
+
+
 class Workload:
     """Sizes, flop count and minimum traffic of one step."""
 
@@ -83,7 +93,7 @@ class Workload:
         elif name.startswith("any_"):
             n = int(name.split("_")[1])
             self.kind, self.n, self.batch, self.dims, self.shift = "c2c_fwd", n, (1 << 26) // n, 1, False
-            self.desc = (f"1-D C2C fp32 forward N={n} (not a power of two: chirp-z path) x "
+            self.desc = (f"1-D C2C fp32 forward N={n} (not a power of two: {any_length_path(n)}) x "
                          f"{(1 << 26) // n} rows (3 tones + noise)")
         elif name.startswith("shift_"):
             n = int(name.split("_")[1])
@@ -95,7 +105,7 @@ class Workload:
             self.kind, self.n, self.batch, self.dims, self.shift = "real_rt", n, 2048, 1, False
             self.mmax = n // 3
             self.pairing = name.startswith("realanypair_")
-            self.desc = (f"real rows 2048 x {n} (any length: chirp-z path), mmax={n // 3}: C2R "
+            self.desc = (f"real rows 2048 x {n} (any length: {any_length_path(n)}), mmax={n // 3}: C2R "
                          "synthesis then R2C analysis, m-major spectrum" +
                          (", two rows per transform" if self.pairing else ""))
         elif name in ("real", "realpair"):

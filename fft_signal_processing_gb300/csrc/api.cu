@@ -14,9 +14,13 @@
 //   2d        n x n images: all rows, then all columns (Mota, "High Performance Fourier
 //             Transforms on GPUs with GLSL", §2.7 Eq. 19), both in place in the output.
 //   real      band-limited real rows through an n/2-point complex core (fourier.ts).
-//   bluestein dims 1, complex or band-limited real rows of any length n <= 8192 that is not a
-//             power of two: the chirp-z transform through m-point FFTs (m >= 2n - 1) in one
-//             kernel (bluestein.cuh); chirp and filter tables in double precision on the host.
+//   mixed     dims 1, complex or band-limited real rows of any length n <= 8192 that is not a
+//             power of two but factors over {2, 3, 5, 7}: mixed-radix Stockham passes in one
+//             kernel (mixed.cuh).
+//   bluestein dims 1, complex or band-limited real rows of any other length n <= 8192 that is
+//             not a power of two: the chirp-z transform through m-point FFTs (m >= 2n - 1) in
+//             one kernel (bluestein.cuh); chirp and filter tables in double precision on the
+//             host.  Longer rows: the same transform over four-step passes (bluestein_mp.cu).
 //
 // Twiddles are computed on the host in double precision from cos/sin of 2*pi*q/M with q
 // reduced modulo M in integers, and rounded once to float (fourier.ts header comment: device
@@ -49,6 +53,7 @@ enum Path {
     PATH_REAL = 3,
     PATH_BLUESTEIN = 4,
     PATH_BLUESTEIN_MP = 5,  // any length above kMaxBluesteinN: chirp-z over four-step passes
+    PATH_MIXED = 6,         // lengths n <= kMaxMixedN with prime factors 2, 3, 5, 7 only
 };
 
 struct PlanSpec {
@@ -57,6 +62,8 @@ struct PlanSpec {
     int log2n = 0;
     Path path = PATH_ONEPASS;
     int log2n1 = 0, log2n2 = 0;  // four-step split
+    int nmix = 0;                // mixed-radix passes and their radices
+    int mix_radix[kMaxMixedPasses] = {};
     int lowbits = 0;             // four-step two-level twiddle split
     int log2m = 0;               // chirp-z transform length
     int64_t ny = 1;              // 2-D: rows per image (ny x n images; ny = n when square)
@@ -66,12 +73,39 @@ struct PlanSpec {
 // Test override of the path choice (environment variable GBFFT_FORCE_PATH, read at every plan
 // creation or query): "fourstep" plans C2C rows of 2^12..2^14 points, whose default is the
 // one-pass kernel, as the two-pass four-step transform (N2 = 2^8, N1 = n/2^8: the smallest
-// split both passes serve); "onepass" or unset keeps the default choice everywhere.  Returns
-// 1 to force the four-step path, 0 for the default, -1 for any other value.
+// split both passes serve); "chirpz" plans rows of lengths n <= kMaxMixedN whose default is the
+// mixed-radix kernel as chirp-z transforms; "default" or unset keeps the default choice
+// everywhere ("onepass" is accepted as a synonym).  Returns the FORCE_* value, or -1 for any
+// other value.
+enum { FORCE_NONE = 0, FORCE_FOURSTEP = 1, FORCE_CHIRPZ = 2 };
 int forced_path() {
     const char* v = std::getenv("GBFFT_FORCE_PATH");
-    if (!v || !*v || !std::strcmp(v, "onepass")) return 0;
-    return std::strcmp(v, "fourstep") ? -1 : 1;
+    if (!v || !*v || !std::strcmp(v, "default") || !std::strcmp(v, "onepass")) return FORCE_NONE;
+    if (!std::strcmp(v, "fourstep")) return FORCE_FOURSTEP;
+    if (!std::strcmp(v, "chirpz")) return FORCE_CHIRPZ;
+    return -1;
+}
+
+// Radices of the mixed-radix schedule of n: the factors 7, 5 and 3 first (odd strides keep the
+// first passes' shared-memory writes free of bank conflicts), then 8s and a last 4 or 2.
+// Returns the number of passes, or 0 if n has a prime factor above 7.
+int mixed_schedule(int64_t n, int* radix) {
+    int np = 0;
+    int64_t m = n;
+    for (int r : {7, 5, 3})
+        while (m % r == 0 && np < kMaxMixedPasses) {
+            radix[np++] = r;
+            m /= r;
+        }
+    while (m % 8 == 0 && np < kMaxMixedPasses) {
+        radix[np++] = 8;
+        m /= 8;
+    }
+    if ((m == 4 || m == 2) && np < kMaxMixedPasses) {
+        radix[np++] = (int)m;
+        m = 1;
+    }
+    return m == 1 ? np : 0;
 }
 constexpr int kForcedFourStepMinLog2 = 12;  // N1 = 2^4 is the row pass's block of 16 rows
 constexpr int kForcedFourStepLog2N2 = 8;    // the smallest four-step row pass
@@ -110,7 +144,13 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     s.layout = layout;
     s.shift = shift;
     s.log2n = l;
-    if (any_length) {
+    int rad[kMaxMixedPasses];
+    const int nmix = any_length && n <= kMaxMixedN ? mixed_schedule(n, rad) : 0;
+    if (nmix > 0 && force != FORCE_CHIRPZ) {
+        s.path = PATH_MIXED;
+        s.nmix = nmix;
+        for (int p = 0; p < nmix; ++p) s.mix_radix[p] = rad[p];
+    } else if (any_length) {
         s.path = n <= kMaxBluesteinN ? PATH_BLUESTEIN : PATH_BLUESTEIN_MP;
         s.log2m = bluestein_log2m(n);
         s.log2n1 = s.log2m / 2;  // four-step split of the m-point transforms (multi-pass)
@@ -128,7 +168,7 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
         s.path = PATH_2D;
     } else {
         if (l > FFT_MAX_LOG2N_1D) return FFT_ERR_UNSUPPORTED_SIZE;
-        if (force == 1 && l >= kForcedFourStepMinLog2 && l <= kMaxLog2OnePass) {
+        if (force == FORCE_FOURSTEP && l >= kForcedFourStepMinLog2 && l <= kMaxLog2OnePass) {
             s.path = PATH_FOURSTEP;
             s.log2n2 = kForcedFourStepLog2N2;
             s.log2n1 = l - kForcedFourStepLog2N2;
@@ -262,6 +302,26 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
                      padded_bytes(s.log2m, blu_maxrb(s.log2m, light), w));
             break;
         }
+        case PATH_MIXED: {
+            const bool real = s.layout != FFT_LAYOUT_C2C;
+            char what[96];
+            if (real)
+                snprintf(what, sizeof what, "%s mmax=%lld layout=%s",
+                         s.direction < 0 ? "analysis(r2c)" : "synthesis(c2r)", (long long)mmax,
+                         s.layout == FFT_LAYOUT_REAL_MMAJOR ? "mmajor" : "rowmajor");
+            else
+                snprintf(what, sizeof what, "%s shift=%d", dir, s.shift);
+            std::string rs;
+            for (int p = 0; p < s.nmix; ++p) rs += (p ? "x" : "") + std::to_string(s.mix_radix[p]);
+            snprintf(buf, sizeof buf,
+                     "path=mixed n=%lld batch=%lld %s%s radix=%s kernels=1 threads=%d "
+                     "rows_per_cta=%d smem=%zu",
+                     (long long)s.n, (long long)s.batch, what,
+                     real && real_pair ? " rows_per_transform=2" : "", rs.c_str(),
+                     kMixedThreadsHost, mixed_rows_per_cta((int)s.n),
+                     mixed_smem_bytes((int)s.n));
+            break;
+        }
         case PATH_BLUESTEIN_MP: {
             const bool real = s.layout != FFT_LAYOUT_C2C;
             char what[128];
@@ -355,6 +415,7 @@ struct gbfft_plan_s {
     int normalize = 0;                       // 1: output scaled by 1/n (1/(nx*ny) for 2-D)
     int real_pair = 0;                       // 1: two real rows per complex transform
     int index_only = 0;                      // diagnostic: epilogues only (fft_plan_set_diagnostic)
+    MixedSched mix = {};                     // mixed-radix schedule (offsets relative to off_a)
 };
 
 static void free_plan(gbfft_plan_s* p) {
@@ -470,6 +531,12 @@ static int create_from_spec(const PlanSpec& s, fft_plan* out) {
             }
             p->off_bhat = host::append_chirp_filter(tw, s.n, int64_t(1) << s.log2m, s.direction);
             break;
+        case PATH_MIXED: {
+            p->off_a = host::append_mixed_tables(tw, s.nmix, s.mix_radix, &p->mix);
+            if (s.shift)  // (cos, sin)(2*pi*(j*h mod n)/n), h = floor(n/2)
+                p->off_chirp = host::append_phase(tw, s.n, s.n / 2);
+            break;
+        }
         case PATH_BLUESTEIN_MP: {
             p->off_a = append_pass_tables(tw, s.log2n1, cols_pass_maxrb(s.log2n1, s.log2n2));
             p->off_b = append_pass_tables(tw, s.log2n2, rowst_maxrb(s.log2n2));
@@ -637,6 +704,12 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                               p->d_tw + p->off_a, st);
             break;
         }
+        case PATH_MIXED:  // in == out is fine: each CTA reads its rows before writing them
+            e = run_mixed(BLU_C2C, s.direction, x, y, s.batch, (int)s.n, p->mix,
+                          p->d_tw + p->off_a, p->d_tw + p->off_chirp, s.shift && fwd,
+                          s.shift && !fwd, p->normalize ? (float)(1.0 / (double)s.n) : 1.f, 0, 0,
+                          st);
+            break;
         case PATH_BLUESTEIN_MP:  // in == out is fine: the input is read into the workspace first
             e = exec_chirp_mp(p, 0, x, y, st);
             break;
@@ -684,7 +757,11 @@ int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
     if (p->index_only && !index_only_supported(p)) return FFT_ERR_UNSUPPORTED_SIZE;
     const int diag = p->index_only ? KF_INDEX_ONLY : 0;
     cudaError_t e;
-    if (s.path == PATH_BLUESTEIN_MP)
+    if (s.path == PATH_MIXED)
+        e = run_mixed(p->real_pair ? BLU_R2C2 : BLU_R2C, -1, in, out, s.batch, (int)s.n, p->mix,
+                      p->d_tw + p->off_a, nullptr, 0, 0, 1.f, (int)p->mmax, mmajor,
+                      (cudaStream_t)stream);
+    else if (s.path == PATH_BLUESTEIN_MP)
         e = exec_chirp_mp(p, 3, in, out, (cudaStream_t)stream);
     else if (s.path == PATH_BLUESTEIN)
         e = run_bluestein(s.log2m, (p->real_pair ? BLU_R2C2 : BLU_R2C) | blu_mode_light(s), in, out,
@@ -713,7 +790,11 @@ int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
     if (p->index_only && !index_only_supported(p)) return FFT_ERR_UNSUPPORTED_SIZE;
     const int diag = p->index_only ? KF_INDEX_ONLY : 0;
     cudaError_t e;
-    if (s.path == PATH_BLUESTEIN_MP)
+    if (s.path == PATH_MIXED)
+        e = run_mixed(p->real_pair ? BLU_C2R2 : BLU_C2R, +1, in, out, s.batch, (int)s.n, p->mix,
+                      p->d_tw + p->off_a, nullptr, 0, 0, 1.f, (int)p->mmax, mmajor,
+                      (cudaStream_t)stream);
+    else if (s.path == PATH_BLUESTEIN_MP)
         e = exec_chirp_mp(p, 4, in, out, (cudaStream_t)stream);
     else if (s.path == PATH_BLUESTEIN)
         e = run_bluestein(s.log2m, (p->real_pair ? BLU_C2R2 : BLU_C2R) | blu_mode_light(s), in, out,

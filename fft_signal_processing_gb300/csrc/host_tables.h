@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "fft_common.cuh"
+#include "kernels.h"
 
 namespace gbfft {
 namespace host {
@@ -45,6 +46,21 @@ inline float2 root_of_unity(int64_t q, int64_t m) {
     return make_float2((float)x, (float)y);
 }
 
+// (cos, sin)(2*pi*q/m) for any m >= 1: the power-of-two moduli through root_of_unity; others
+// with q reduced modulo m in integers and the angle folded to [0, pi] (sin changes sign), in
+// double precision rounded once to float.
+inline float2 root_any(int64_t q, int64_t m) {
+    q %= m;
+    if (q < 0) q += m;
+    if ((m & (m - 1)) == 0) return root_of_unity(q, m);
+    const double two_pi = 6.283185307179586476925286766559005768;
+    const bool upper = 2 * q > m;
+    const int64_t a = upper ? m - q : q;
+    const double th = two_pi * (double)a / (double)m;
+    const double s = std::sin(th);
+    return make_float2((float)std::cos(th), (float)(upper ? -s : s));
+}
+
 inline void align_table(std::vector<float2>& v) {
     while (v.size() % 32) v.push_back(make_float2(0.f, 0.f));
 }
@@ -73,6 +89,38 @@ inline size_t append_roots(std::vector<float2>& v, int64_t count, int64_t step, 
     align_table(v);
     const size_t off = v.size();
     for (int64_t q = 0; q < count; ++q) v.push_back(root_of_unity(q * step, m));
+    return off;
+}
+
+// ---- mixed-radix schedule tables ----------------------------------------------------------
+// Pass p of radix R and span Ns: (cos, sin)(2*pi*m*r/(Ns*R)) at m*(R-1) + r-1, m < Ns,
+// 1 <= r < R.  Fills sch (spans, radices, offsets relative to the returned offset).
+inline size_t append_mixed_tables(std::vector<float2>& v, int npass, const int* radix,
+                                  MixedSched* sch) {
+    align_table(v);
+    const size_t off = v.size();
+    sch->npass = npass;
+    int64_t ns = 1;
+    for (int p = 0; p < npass; ++p) {
+        const int R = radix[p];
+        sch->radix[p] = R;
+        sch->span[p] = (int)ns;
+        sch->smagic[p] = div_magic((uint32_t)ns);
+        sch->off[p] = (int)(v.size() - off);
+        for (int64_t m = 0; m < ns; ++m)
+            for (int r = 1; r < R; ++r) v.push_back(root_any(m * r, ns * R));
+        ns *= R;
+    }
+    for (int p = 0; p < npass; ++p) sch->qmagic[p] = div_magic((uint32_t)(ns / radix[p]));
+    sch->nmagic = div_magic((uint32_t)ns);
+    return off;
+}
+
+// (cos, sin)(2*pi*(j*h mod n)/n) for j < n: the fftshift phase of a length-n row.
+inline size_t append_phase(std::vector<float2>& v, int64_t n, int64_t h) {
+    align_table(v);
+    const size_t off = v.size();
+    for (int64_t j = 0; j < n; ++j) v.push_back(root_any((int64_t)(((__int128)j * h) % n), n));
     return off;
 }
 

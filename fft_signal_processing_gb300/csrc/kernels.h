@@ -166,6 +166,46 @@ cudaError_t run_bluestein_mp(int mode, const void* in, void* out, int64_t nrows,
                              float2* B, int* err, uint64_t lim, cudaStream_t s);
 constexpr int64_t kMaxBluesteinMpN = int64_t(1) << 20;  // m = 2^21 at most
 
+// Rows of any length 2 <= n <= kMaxMixedN that factors over {2, 3, 5, 7} (and is not a power of
+// two): the mixed-radix Stockham kernel (mixed.cuh).  A plan's schedule: radix[p] in
+// {2, 3, 4, 5, 7, 8}, span[p] = radix[0]*...*radix[p-1], off[p] the offset of pass p's twiddle
+// table ((cos, sin) of 2*pi*m*r/(span*radix) at m*(radix-1) + r-1) in the plan table.
+constexpr int kMaxMixedN = 8192;
+constexpr int kMaxMixedPasses = 16;
+struct MixedSched {
+    int npass;
+    int radix[kMaxMixedPasses];
+    int span[kMaxMixedPasses];
+    int off[kMaxMixedPasses];
+    // Division by the pass's butterflies per row n/radix and by its span, and by n: x / d is
+    // umulhi(x, magic) with magic = ceil(2^32 / d), exact for x * d < 2^32 (every index here
+    // is below 2^14 and every divisor at most 2^13); magic 0 stands for d = 1.
+    uint32_t qmagic[kMaxMixedPasses];
+    uint32_t smagic[kMaxMixedPasses];
+    uint32_t nmagic;
+};
+__host__ __device__ constexpr uint32_t div_magic(uint32_t d) {
+    return d <= 1 ? 0u : (uint32_t)((((uint64_t)1 << 32) + d - 1) / d);
+}
+constexpr int kMixedThreadsHost = 256;  // threads per CTA of the mixed-radix kernel
+// Rows per CTA (about 2048 points a CTA: measured faster than 4096, n = 100 and 1000 0.50
+// and 0.55 ms against 0.56 and 0.64 ms per 2^26 points) and the two shared-memory buffers
+// they take (the pass twiddles stay in global memory, read through L1: staging them in shared
+// memory measured no faster at n = 1000 and slower at n = 3000, 0.79 vs 0.66 ms).
+__host__ __device__ constexpr int mixed_rows_per_cta(int n) { return n >= 2048 ? 1 : 2048 / n; }
+__host__ __device__ constexpr size_t mixed_smem_bytes(int n) {
+    return 2 * (size_t)mixed_rows_per_cta(n) * (size_t)n * 8u;
+}
+static_assert(mixed_smem_bytes(2047) <= mixed_smem_bytes(kMaxMixedN),
+              "the launcher's shared-memory limit covers every length");
+// mode: BLU_C2C, BLU_R2C, BLU_C2R, BLU_R2C2, BLU_C2R2 (as run_bluestein); dir the sign of
+// the C2C transform (the real modes imply theirs).  ph: (cos, sin)(2*pi*(j*h mod n)/n), the
+// fftshift phase applied on the forward load (shift_in) or, conjugated, on the inverse store
+// (shift_out); scale multiplies the C2C output.
+cudaError_t run_mixed(int mode, int dir, const void* in, void* out, int64_t nrows, int n,
+                      const MixedSched& sch, const float2* tw, const float2* ph, int shift_in,
+                      int shift_out, float scale, int mmax, int mmajor, cudaStream_t s);
+
 // Real rows of 2^log2n points, two per n-point complex transform (rows 2p, 2p+1).
 cudaError_t run_real_pair(int log2n, bool analysis, const void* in, void* out, int64_t nrows,
                           int mmax, int mmajor, const float2* tw, int flags, cudaStream_t s);

@@ -76,7 +76,10 @@ enum {
  *             2 <= n <= 2^12 (dims 2); or, for rows (dims 1) only,
  *             any length 3 <= n <= FFT_MAX_N_ANY_LENGTH (complex rows and band-limited real
  *             rows, dims 1; for real rows this is the any-nphi role of the direct-sum 'dft'
- *             mode of fourier.ts), computed as the chirp-z (Bluestein)
+ *             mode of fourier.ts).  Lengths n <= 8192 whose prime factors are 2, 3, 5 and 7
+ *             run mixed-radix Stockham passes (radices 2, 3, 4, 5, 7, 8) in one kernel (the
+ *             mixed-radix extension of the radix-2^k passes, Mota §2.3); every other length
+ *             is computed as the chirp-z (Bluestein)
  *             transform X_k = c_k sum_j (x_j c_j) conj(c_{k-j}), c_j = exp(s*pi*i*j^2/n),
  *             through power-of-two FFTs of length m >= 2n - 1 (the same unnormalised DFT of
  *             Mota, "High Performance Fourier Transforms on GPUs with GLSL", 2.2 Eq. 5, for
@@ -96,9 +99,10 @@ enum {
  *             CUDA by chessboard multiplication", the chessboard section).  Inverse: the output
  *             is post-multiplied by the same chessboard, i.e. it is IFFT(ifftshift(X)), so
  *             inverse-shift(forward-shift(x)) = n*x (dims 1) or n^2*x (dims 2).  For odd n
- *             (chirp-z path) the factors are exp(+2*pi*i*j*h/n) on the forward load and
- *             exp(-2*pi*i*k*h/n) on the inverse store, h = (n-1)/2, with the same meaning
- *             (fftshift moves bin 0 to index h); they are folded into the chirp tables.
+ *             (mixed-radix and chirp-z paths) the factors are exp(+2*pi*i*j*h/n) on the
+ *             forward load and exp(-2*pi*i*k*h/n) on the inverse store, h = (n-1)/2, with the
+ *             same meaning (fftshift moves bin 0 to index h); they come from a plan table
+ *             (folded into the chirp tables on the chirp-z path).
  *   out       receives the plan.
  * The plan allocates its device twiddle tables, its workspace (large 1-D sizes only) and a
  * device error word with cudaMalloc on the current device, and copies the tables (computed on
@@ -106,8 +110,9 @@ enum {
  * Test override: the environment variable GBFFT_FORCE_PATH, read at every plan creation and
  * query, set to "fourstep" plans C2C rows of 2^12 <= n <= 2^14 points (whose default is a
  * single kernel per row) as the two-pass four-step transform with N2 = 256, N1 = n/256, with a
- * workspace of batch*n complex64; "onepass" or unset leaves every choice at its default; any
- * other value makes plan creation and query return FFT_ERR_INVALID_ARG.
+ * workspace of batch*n complex64; "chirpz" plans the lengths whose default is the mixed-radix
+ * kernel as chirp-z transforms; "default", "onepass" or unset leaves every choice at its
+ * default; any other value makes plan creation and query return FFT_ERR_INVALID_ARG.
  * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_UNSUPPORTED_SIZE, FFT_ERR_OOM or FFT_ERR_CUDA;
  * on error *out is set to NULL and nothing is left allocated.
  */

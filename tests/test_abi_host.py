@@ -56,9 +56,11 @@ def test_lengths_outside_the_supported_set_rejected(n):
     assert q(n) == fx.FFT_ERR_UNSUPPORTED_SIZE
 
 
-@pytest.mark.parametrize("n,m", [(3, 8), (5, 16), (6, 16), (100, 256), (1000, 2048),
-                                 (1025, 4096), (4096 + 1, 16384), (8191, 16384)])
+@pytest.mark.parametrize("n,m", [(11, 32), (13 * 3, 128), (1001, 2048), (1025, 4096),
+                                 (4096 + 1, 16384), (8191, 16384)])
 def test_any_length_rows_take_the_chirp_z_path(n, m):
+    """Lengths with a prime factor above 7 (11, 13, 1001 = 7*11*13, 1025 = 25*41, 4097,
+    8191) take the one-pass chirp-z kernel."""
     d = fx.query(n, 5)
     assert "path=bluestein" in d and f"m={m} " in d and "kernels=1" in d
     assert m >= 2 * n - 1 and m // 2 < 2 * n - 1  # the smallest power of two that suffices
@@ -67,6 +69,23 @@ def test_any_length_rows_take_the_chirp_z_path(n, m):
     d = fx.query(n, 5, layout=2, direction=1)
     assert "path=bluestein" in d and f"mmax={(n - 1) // 2} " in d and "synthesis" in d
     assert q(n, dims=2) == fx.FFT_ERR_UNSUPPORTED_SIZE
+
+
+@pytest.mark.parametrize("n,radix", [(3, "3"), (5, "5"), (6, "3x2"), (12, "3x4"), (100, "5x5x4"),
+                                     (1000, "5x5x5x8"), (3000, "5x5x5x3x8"), (6561, "3x" * 7 + "3"),
+                                     (7168, "7x8x8x8x2"), (8000, "5x5x5x8x8")])
+def test_smooth_lengths_take_the_mixed_radix_path(n, radix, monkeypatch):
+    """Lengths up to 8192 whose prime factors are 2, 3, 5 and 7 take the mixed-radix kernel
+    (radices 7, 5, 3 first, then 8s and a last 4 or 2), complex and real, shift allowed;
+    GBFFT_FORCE_PATH=chirpz sends them to the chirp-z kernel instead."""
+    d = fx.query(n, 5)
+    assert "path=mixed" in d and f"radix={radix} " in d and "kernels=1" in d
+    assert q(n, shift=1) == fx.FFT_OK
+    d = fx.query(n, 6, layout=2, direction=1)
+    assert "path=mixed" in d and f"mmax={(n - 1) // 2} " in d and "synthesis" in d
+    monkeypatch.setenv("GBFFT_FORCE_PATH", "chirpz")
+    assert "path=bluestein" in fx.query(n, 5)
+    assert "path=bluestein" in fx.query(n, 5, layout=1)
 
 
 @pytest.mark.parametrize("n,m", [(8193, 1 << 15), (10000, 1 << 15), (16385, 1 << 16),
@@ -168,9 +187,13 @@ def test_forced_path_override(monkeypatch):
     assert f"n1={1 << 7} n2={1 << 8}" in fx.query(1 << 15, 3)
     assert "path=2d" in fx.query(4096, 1, dims=2)
     assert "path=real" in fx.query(4096, 8, layout=2, direction=1)
-    for v in ("onepass", ""):
+    assert "path=mixed" in fx.query(1000, 3)
+    for v in ("onepass", "default", ""):
         monkeypatch.setenv("GBFFT_FORCE_PATH", v)
         assert "path=onepass" in fx.query(4096, 3)
+        assert "path=mixed" in fx.query(1000, 3)
+    monkeypatch.setenv("GBFFT_FORCE_PATH", "chirpz")
+    assert "path=bluestein" in fx.query(1000, 3) and "path=onepass" in fx.query(4096, 3)
     monkeypatch.setenv("GBFFT_FORCE_PATH", "four-step")
     assert q(4096) == fx.FFT_ERR_INVALID_ARG
     monkeypatch.delenv("GBFFT_FORCE_PATH")

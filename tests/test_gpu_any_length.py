@@ -1,13 +1,17 @@
-"""GPU parity of rows whose length is not a power of two (the chirp-z path) against the fp64
-oracle's direct sums, through the C ABI: complex rows against the DFT of Mota, "High
-Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5; band-limited real rows against
-the direct analysis/synthesis sums of fourier.ts (dftAnalysWGSL / dftSynthWGSL), both spectrum
-layouts.
+"""GPU parity of rows whose length is not a power of two (the mixed-radix and chirp-z paths)
+against the fp64 oracle's direct sums, through the C ABI: complex rows against the DFT of Mota,
+"High Performance Fourier Transforms on GPUs with GLSL", §2.2 Eq. 5; band-limited real rows
+against the direct analysis/synthesis sums of fourier.ts (dftAnalysWGSL / dftSynthWGSL), both
+spectrum layouts.
 
 Lengths span every chirp-z size m = 8 .. 16384 (m the power of two >= 2n - 1), including
 n just above and below powers of two, odd and even n, ragged batches, both directions, the
 chessboard shift (even n), in place, and one full benchmark-sized batch with sampled rows.
+Lengths whose prime factors are 2, 3, 5 and 7 (up to 8192) run both on their default
+mixed-radix path and, forced with GBFFT_FORCE_PATH=chirpz, on the chirp-z path.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -38,10 +42,36 @@ def wl():
     return workloads
 
 
+def smooth(n):
+    for f in (2, 3, 5, 7):
+        while n % f == 0:
+            n //= f
+    return n == 1
+
+
+def expected_path(n):
+    mixed = smooth(n) and n <= 8192 and os.environ.get("GBFFT_FORCE_PATH") != "chirpz"
+    return "path=mixed" if mixed else "path=bluestein"
+
+
+@pytest.fixture(params=["default", "chirpz"])
+def route(request, monkeypatch):
+    """The default path choice, and the chirp-z path forced (GBFFT_FORCE_PATH=chirpz); lengths
+    with a prime factor above 7 take the chirp-z path either way and run once."""
+    if request.param == "chirpz":
+        monkeypatch.setenv("GBFFT_FORCE_PATH", "chirpz")
+    return request.param
+
+
+def skip_same(n, route):
+    if route == "chirpz" and not smooth(n):
+        pytest.skip("the default path of this length is the chirp-z path")
+
+
 def gpu_c2c(x, n, batch, direction, shift=False, inplace=False):
     m = fx()
     p = m.Plan(n, batch, 1, direction, shift=shift)
-    assert "path=bluestein" in p.describe()
+    assert expected_path(n) in p.describe()
     xd = torch.from_numpy(np.ascontiguousarray(x, dtype=np.complex64)).cuda()
     if inplace:
         p.c2c(xd, out=xd)
@@ -59,18 +89,21 @@ LENGTHS = [3, 5, 6, 7, 12, 31, 33, 100, 127, 129, 255, 257, 1000, 1023, 1025, 20
 
 @pytest.mark.parametrize("n", LENGTHS)
 @pytest.mark.parametrize("direction", [-1, 1])
-def test_any_length_grid(n, direction):
+def test_any_length_grid(n, direction, route):
+    skip_same(n, route)
     batch = 37 if n <= 1100 else 3  # ragged against every rows-per-CTA count
     x = wl().normal(7000 + n, batch, n)
     got = gpu_c2c(x, n, batch, direction)
     assert_parity(got, oracle.transform(x, direction), n, f"n={n} dir={direction}")
 
 
-@pytest.mark.parametrize("n", [3, 6, 7, 100, 1000, 1001, 4098, 4099, 8190, 8191])
+@pytest.mark.parametrize("n", [3, 6, 7, 100, 1000, 1001, 4098, 4099, 8190, 8191, 3 * 5 * 7 * 9])
 @pytest.mark.parametrize("direction", [-1, 1])
-def test_any_length_shift_in_place(n, direction):
-    """Even lengths: the chessboard; odd lengths: the complex exponentials, both folded into
-    the chirp tables; against fftshift(DFT(x)) and IFFT(ifftshift(X)) of the oracle."""
+def test_any_length_shift_in_place(n, direction, route):
+    """Even lengths: the chessboard; odd lengths: the complex exponentials (folded into the
+    chirp tables, or the phase table of the mixed-radix path); against fftshift(DFT(x)) and
+    IFFT(ifftshift(X)) of the oracle."""
+    skip_same(n, route)
     batch = 5
     x = wl().uniform(7100 + n, batch, n)
     got = gpu_c2c(x, n, batch, direction, shift=True, inplace=True)
@@ -80,8 +113,9 @@ def test_any_length_shift_in_place(n, direction):
         assert np.argmax(np.abs(y[0])) == n // 2
 
 
-@pytest.mark.parametrize("n", [3, 1000, 8191])
-def test_any_length_round_trip_and_tones(n):
+@pytest.mark.parametrize("n", [3, 1000, 8191, 7168])
+def test_any_length_round_trip_and_tones(n, route):
+    skip_same(n, route)
     batch = 4
     x = wl().tones(7200 + n, batch, n)
     y = gpu_c2c(x, n, batch, -1)
@@ -119,7 +153,7 @@ def gpu_c2r(F_rowmajor, n, mmax, layout):
     m = fx()
     rows = F_rowmajor.shape[0]
     p = m.Plan(n, rows, 1, m.INVERSE, layout=LAYOUTS[layout], mmax=mmax)
-    assert "path=bluestein" in p.describe()
+    assert expected_path(n) in p.describe()
     Fin = oracle.to_mmajor(F_rowmajor) if layout == "mmajor" else F_rowmajor
     x = p.c2r(torch.from_numpy(np.ascontiguousarray(Fin, dtype=np.complex64)).cuda())
     torch.cuda.synchronize()
@@ -131,7 +165,7 @@ def gpu_r2c(x, mmax, layout):
     m = fx()
     rows, n = x.shape
     p = m.Plan(n, rows, 1, m.FORWARD, layout=LAYOUTS[layout], mmax=mmax)
-    assert "path=bluestein" in p.describe()
+    assert expected_path(n) in p.describe()
     F = p.r2c(torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda())
     torch.cuda.synchronize()
     p.check()
@@ -144,8 +178,9 @@ REAL_LENGTHS = [3, 5, 6, 100, 999, 1000, 3000, 6000, 8191]
 
 @pytest.mark.parametrize("n", REAL_LENGTHS)
 @pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
-def test_any_length_real_synthesis(n, layout):
-    for mmax in sorted({0, (n - 1) // 2, max(0, n // 7)}):
+def test_any_length_real_synthesis(n, layout, route):
+    skip_same(n, route)
+    for mmax in sorted({0, (n - 1) // 2, max(0, n // 7)} | ({n // 2} if n % 2 == 0 else set())):
         rows = 33 if n <= 1000 else 3
         F = wl().spectrum(7400 + n + mmax, rows, mmax)
         got = gpu_c2r(F, n, mmax, layout)
@@ -154,8 +189,9 @@ def test_any_length_real_synthesis(n, layout):
 
 @pytest.mark.parametrize("n", REAL_LENGTHS)
 @pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
-def test_any_length_real_analysis(n, layout):
-    for mmax in sorted({0, (n - 1) // 2, max(0, n // 7)}):
+def test_any_length_real_analysis(n, layout, route):
+    skip_same(n, route)
+    for mmax in sorted({0, (n - 1) // 2, max(0, n // 7)} | ({n // 2} if n % 2 == 0 else set())):
         rows = 33 if n <= 1000 else 3
         x = wl().real_normal(7500 + n + mmax, rows, n)
         got = gpu_r2c(x, mmax, layout)
@@ -166,7 +202,7 @@ def test_any_length_real_analysis(n, layout):
 
 
 @pytest.mark.parametrize("n", [1000, 6000])
-def test_any_length_real_round_trip(n):
+def test_any_length_real_round_trip(n, route):
     mmax = (n - 1) // 2
     F = wl().spectrum(7600 + n, 4, mmax)
     x = gpu_c2r(F, n, mmax, "mmajor")
@@ -241,10 +277,11 @@ def test_long_real_rows(n, mmaxes, layout):
 
 @pytest.mark.parametrize("pairing", [False, True])
 def test_any_length_real_large_batch_sampled(pairing):
-    """Real rows of 1000 points in a batch large enough for the radix-64 chirp-z schedule (the
-    small batches above take the radix-16 one): sampled rows against the direct sums."""
+    """Real rows of 1001 points (7 * 11 * 13: the chirp-z path) in a batch large enough for the
+    radix-64 chirp-z schedule (the small batches above take the radix-16 one): sampled rows
+    against the direct sums."""
     m = fx()
-    n, rows, mmax = 1000, 12000, 333
+    n, rows, mmax = 1001, 12000, 333
     assert "radix=64x32" in m.query(n, rows, 1, m.INVERSE, m.LAYOUT_REAL_MMAJOR)
     F = wl().spectrum(7950, rows, mmax)
     syn = m.Plan(n, rows, 1, m.INVERSE, layout=m.LAYOUT_REAL_MMAJOR, mmax=mmax, pairing=pairing)

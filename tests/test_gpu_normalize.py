@@ -34,7 +34,7 @@ def data(seed, *shape):
 
 CASES = [  # (n, batch, ny or None)
     (16, 33, None), (1024, 9, None), (8192, 3, None), (1 << 16, 2, None), (1 << 22, 1, None),
-    (1000, 5, None), (64, 2, 64), (4096, 1, 4096), (4096, 1, 8),
+    (1000, 5, None), (1001, 5, None), (64, 2, 64), (4096, 1, 4096), (4096, 1, 8),
 ]
 
 
