@@ -54,6 +54,7 @@ enum Path {
     PATH_BLUESTEIN = 4,
     PATH_BLUESTEIN_MP = 5,  // any length above kMaxBluesteinN: chirp-z over four-step passes
     PATH_MIXED = 6,         // lengths n <= kMaxMixedN with prime factors 2, 3, 5, 7 only
+    PATH_MIXED_FS = 7,      // such lengths above kMaxMixedN (complex rows): two mixed-radix passes
 };
 
 struct PlanSpec {
@@ -64,6 +65,9 @@ struct PlanSpec {
     int log2n1 = 0, log2n2 = 0;  // four-step split
     int nmix = 0;                // mixed-radix passes and their radices
     int mix_radix[kMaxMixedPasses] = {};
+    int mix_n1 = 0, mix_n2 = 0;  // mixed-radix four-step split n = N1*N2
+    int nmix1 = 0;               // ... and the N1-point schedule (the N2-point one in mix_radix)
+    int mix_radix1[kMaxMixedPasses] = {};
     int lowbits = 0;             // four-step two-level twiddle split
     int log2m = 0;               // chirp-z transform length
     int64_t ny = 1;              // 2-D: rows per image (ny x n images; ny = n when square)
@@ -107,6 +111,15 @@ int mixed_schedule(int64_t n, int* radix) {
     }
     return m == 1 ? np : 0;
 }
+
+// Four-step split of a length whose prime factors are 2, 3, 5, 7: the largest divisor N1 of n
+// with N1 <= min(kMaxMixedN1, sqrt(n)) and N2 = n/N1 <= kMaxMixedN (both passes near the
+// mixed-radix kernel's best lengths); 0 if there is none.
+int mixed_split(int64_t n) {
+    for (int64_t d = std::min<int64_t>(kMaxMixedN1, (int64_t)std::sqrt((double)n)); d >= 2; --d)
+        if (n % d == 0 && n / d <= kMaxMixedN) return (int)d;
+    return 0;
+}
 constexpr int kForcedFourStepMinLog2 = 12;  // N1 = 2^4 is the row pass's block of 16 rows
 constexpr int kForcedFourStepLog2N2 = 8;    // the smallest four-step row pass
 
@@ -144,12 +157,27 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     s.layout = layout;
     s.shift = shift;
     s.log2n = l;
-    int rad[kMaxMixedPasses];
+    int rad[kMaxMixedPasses], rad1[kMaxMixedPasses];
     const int nmix = any_length && n <= kMaxMixedN ? mixed_schedule(n, rad) : 0;
+    // long rows: the split and both schedules (complex rows; real rows keep the chirp-z path)
+    int n1 = 0, nmix1 = 0, nmix2 = 0;
+    if (any_length && n > kMaxMixedN && n <= kMaxMixedFourStepN && layout == FFT_LAYOUT_C2C &&
+        force != FORCE_CHIRPZ && (n1 = mixed_split(n)) > 0) {
+        nmix1 = mixed_schedule(n1, rad1);
+        nmix2 = mixed_schedule(n / n1, rad);
+    }
     if (nmix > 0 && force != FORCE_CHIRPZ) {
         s.path = PATH_MIXED;
         s.nmix = nmix;
         for (int p = 0; p < nmix; ++p) s.mix_radix[p] = rad[p];
+    } else if (nmix1 > 0 && nmix2 > 0) {
+        s.path = PATH_MIXED_FS;
+        s.mix_n1 = n1;
+        s.mix_n2 = (int)(n / n1);
+        s.nmix1 = nmix1;
+        s.nmix = nmix2;
+        for (int p = 0; p < nmix1; ++p) s.mix_radix1[p] = rad1[p];
+        for (int p = 0; p < nmix2; ++p) s.mix_radix[p] = rad[p];
     } else if (any_length) {
         s.path = n <= kMaxBluesteinN ? PATH_BLUESTEIN : PATH_BLUESTEIN_MP;
         s.log2m = bluestein_log2m(n);
@@ -322,6 +350,19 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
                      mixed_smem_bytes((int)s.n));
             break;
         }
+        case PATH_MIXED_FS: {
+            std::string r1, r2;
+            for (int p = 0; p < s.nmix1; ++p) r1 += (p ? "x" : "") + std::to_string(s.mix_radix1[p]);
+            for (int p = 0; p < s.nmix; ++p) r2 += (p ? "x" : "") + std::to_string(s.mix_radix[p]);
+            snprintf(buf, sizeof buf,
+                     "path=mixed_fourstep n=%lld batch=%lld %s shift=%d n1=%d n2=%d kernels=2 "
+                     "pass1=columns(radix=%s cols_per_cta=%d smem=%zu) "
+                     "pass2=rows_transposed(radix=%s rows_per_cta=%d smem=%zu)",
+                     (long long)s.n, (long long)s.batch, dir, s.shift, s.mix_n1, s.mix_n2,
+                     r1.c_str(), mixed_cols_per_cta(s.mix_n1), mixed_cols_smem_bytes(s.mix_n1),
+                     r2.c_str(), mixed_rows_per_cta(s.mix_n2), mixed_smem_bytes(s.mix_n2));
+            break;
+        }
         case PATH_BLUESTEIN_MP: {
             const bool real = s.layout != FFT_LAYOUT_C2C;
             char what[128];
@@ -415,7 +456,9 @@ struct gbfft_plan_s {
     int normalize = 0;                       // 1: output scaled by 1/n (1/(nx*ny) for 2-D)
     int real_pair = 0;                       // 1: two real rows per complex transform
     int index_only = 0;                      // diagnostic: epilogues only (fft_plan_set_diagnostic)
-    MixedSched mix = {};                     // mixed-radix schedule (offsets relative to off_a)
+    MixedSched mix = {};                     // mixed-radix schedule (offsets relative to off_a;
+                                             // four-step: the N2 pass, relative to off_b)
+    MixedSched mix1 = {};                    // four-step: the N1 pass (relative to off_a)
 };
 
 static void free_plan(gbfft_plan_s* p) {
@@ -531,6 +574,16 @@ static int create_from_spec(const PlanSpec& s, fft_plan* out) {
             }
             p->off_bhat = host::append_chirp_filter(tw, s.n, int64_t(1) << s.log2m, s.direction);
             break;
+        case PATH_MIXED_FS: {
+            p->off_a = host::append_mixed_tables(tw, s.nmix1, s.mix_radix1, &p->mix1);
+            p->off_b = host::append_mixed_tables(tw, s.nmix, s.mix_radix, &p->mix);
+            const int64_t nlo = int64_t(1) << kMixedTwLoBits;
+            p->off_lo = host::append_roots_any(tw, nlo, 1, s.n);                  // w_n^{ql}
+            p->off_hi = host::append_roots_any(tw, (s.n + nlo - 1) / nlo, nlo, s.n);  // w_n^{qh*nlo}
+            if (s.shift) p->off_chirp = host::append_phase(tw, s.n, s.n / 2);
+            p->work_bytes = (size_t)s.batch * (size_t)s.n * sizeof(float2);
+            break;
+        }
         case PATH_MIXED: {
             p->off_a = host::append_mixed_tables(tw, s.nmix, s.mix_radix, &p->mix);
             if (s.shift)  // (cos, sin)(2*pi*(j*h mod n)/n), h = floor(n/2)
@@ -702,6 +755,18 @@ int fft_exec_c2c(fft_plan p, const void* in, void* out, void* stream) {
                               p->d_tw + p->off_chirp,
                               p->d_tw + p->off_chirp_out, p->d_tw + p->off_bhat,
                               p->d_tw + p->off_a, st);
+            break;
+        }
+        case PATH_MIXED_FS: {  // in == out is fine: pass 1 writes only the workspace
+            float2* wk = (float2*)p->d_work;
+            e = run_mixed_cols(s.direction, x, wk, s.batch, s.mix_n1, s.mix_n2, p->mix1,
+                               p->d_tw + p->off_a, p->d_tw + p->off_hi, p->d_tw + p->off_lo,
+                               kMixedTwLoBits, p->d_tw + p->off_chirp, s.shift && fwd, st);
+            if (e == cudaSuccess)
+                e = run_mixed(kMixedRowsT, s.direction, wk, y, s.batch * s.mix_n1, s.mix_n2,
+                              p->mix, p->d_tw + p->off_b, p->d_tw + p->off_chirp, 0,
+                              s.shift && !fwd, p->normalize ? (float)(1.0 / (double)s.n) : 1.f,
+                              0, 0, st, s.mix_n1);
             break;
         }
         case PATH_MIXED:  // in == out is fine: each CTA reads its rows before writing them

@@ -116,6 +116,15 @@ inline size_t append_mixed_tables(std::vector<float2>& v, int npass, const int* 
     return off;
 }
 
+// (cos, sin)(2*pi*q*step/m) for q < count, any m; returns the offset.
+inline size_t append_roots_any(std::vector<float2>& v, int64_t count, int64_t step, int64_t m) {
+    align_table(v);
+    const size_t off = v.size();
+    for (int64_t q = 0; q < count; ++q)
+        v.push_back(root_any((int64_t)(((__int128)q * step) % m), m));
+    return off;
+}
+
 // (cos, sin)(2*pi*(j*h mod n)/n) for j < n: the fftshift phase of a length-n row.
 inline size_t append_phase(std::vector<float2>& v, int64_t n, int64_t h) {
     align_table(v);

@@ -198,13 +198,36 @@ __host__ __device__ constexpr size_t mixed_smem_bytes(int n) {
 }
 static_assert(mixed_smem_bytes(2047) <= mixed_smem_bytes(kMaxMixedN),
               "the launcher's shared-memory limit covers every length");
-// mode: BLU_C2C, BLU_R2C, BLU_C2R, BLU_R2C2, BLU_C2R2 (as run_bluestein); dir the sign of
-// the C2C transform (the real modes imply theirs).  ph: (cos, sin)(2*pi*(j*h mod n)/n), the
-// fftshift phase applied on the forward load (shift_in) or, conjugated, on the inverse store
-// (shift_out); scale multiplies the C2C output.
+// mode: BLU_C2C, BLU_R2C, BLU_C2R, BLU_R2C2, BLU_C2R2 (as run_bluestein), or kMixedRowsT (the
+// second pass of the four-step form below: nrows = batch*N1 rows of n = N2 points, row
+// b*N1 + k1's output k2 stored at b*N1*N2 + k1 + N1*k2; tn1 = N1); dir the sign of the C2C
+// transform (the real modes imply theirs).  ph: (cos, sin)(2*pi*(j*h mod N)/N) over the
+// transform length N, the fftshift phase applied on the forward load (shift_in) or,
+// conjugated, on the inverse store (shift_out); scale multiplies the C2C output.
+constexpr int kMixedRowsT = 5;
 cudaError_t run_mixed(int mode, int dir, const void* in, void* out, int64_t nrows, int n,
                       const MixedSched& sch, const float2* tw, const float2* ph, int shift_in,
-                      int shift_out, float scale, int mmax, int mmajor, cudaStream_t s);
+                      int shift_out, float scale, int mmax, int mmajor, cudaStream_t s,
+                      int tn1 = 0);
+
+// Complex rows of length kMaxMixedN < n <= kMaxMixedFourStepN whose prime factors are 2, 3, 5
+// and 7, as n = N1*N2 with N1 <= kMaxMixedN1 and N2 <= kMaxMixedN: pass 1 (run_mixed_cols)
+// transforms the N2 columns of each [N1][N2] transform into a workspace, times w_n^{n2*k1}
+// (two-level table hi/lo of w_n, lobits low bits); pass 2 is run_mixed in mode kMixedRowsT.
+constexpr int kMaxMixedN1 = 512;
+constexpr int kMixedTwLoBits = 10;  // w_n^q = hi[q >> 10] * lo[q & 1023]
+constexpr int64_t kMaxMixedFourStepN = int64_t(1) << 20;
+// columns per CTA of pass 1: about 2048 points, at least 8 columns (64-byte row runs)
+__host__ __device__ constexpr int mixed_cols_per_cta(int n1) {
+    return clampi(2048 / n1, 8, 128);
+}
+__host__ __device__ constexpr size_t mixed_cols_smem_bytes(int n1) {
+    return 2 * (size_t)mixed_cols_per_cta(n1) * (size_t)n1 * 8u;
+}
+cudaError_t run_mixed_cols(int dir, const float2* in, float2* out, int64_t batch, int n1, int n2,
+                           const MixedSched& sch, const float2* tw, const float2* hi,
+                           const float2* lo, int lobits, const float2* ph, int shift_in,
+                           cudaStream_t s);
 
 // Real rows of 2^log2n points, two per n-point complex transform (rows 2p, 2p+1).
 cudaError_t run_real_pair(int log2n, bool analysis, const void* in, void* out, int64_t nrows,

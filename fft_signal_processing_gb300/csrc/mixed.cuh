@@ -162,12 +162,42 @@ __device__ __forceinline__ void mixed_pass(const float2* A, float2* B, int n, in
     }
 }
 
+// MODE: BLU_C2C, BLU_R2C, BLU_C2R, BLU_R2C2, BLU_C2R2, or kMixedRowsT: the second pass of the
+// mixed-radix four-step transform (rows tr = b*N1 + k1 of n = N2 points; output k2 of the row
+// stored at X[b*N1*N2 + k1 + N1*k2], with the inverse fftshift phase of index k1 + N1*k2 and
+// the scale; tn1 = N1).
+// Every pass of the schedule over W rows of n points, A -> B -> A ...; returns the buffer that
+// holds the result (every thread's writes visible after the closing barrier).
+template <int DIR>
+__device__ __forceinline__ float2* mixed_passes(float2* A, float2* B, int n, int W,
+                                                const MixedSched& sch,
+                                                const float2* __restrict__ tw) {
+    for (int p = 0; p < sch.npass; ++p) {
+        const float2* twp = tw + sch.off[p];
+        const int ns = sch.span[p];
+        const uint32_t qm = sch.qmagic[p], sm = sch.smagic[p];
+        switch (sch.radix[p]) {
+            case 2: mixed_pass<2, DIR>(A, B, n, W, ns, qm, sm, twp); break;
+            case 3: mixed_pass<3, DIR>(A, B, n, W, ns, qm, sm, twp); break;
+            case 4: mixed_pass<4, DIR>(A, B, n, W, ns, qm, sm, twp); break;
+            case 5: mixed_pass<5, DIR>(A, B, n, W, ns, qm, sm, twp); break;
+            case 7: mixed_pass<7, DIR>(A, B, n, W, ns, qm, sm, twp); break;
+            default: mixed_pass<8, DIR>(A, B, n, W, ns, qm, sm, twp); break;
+        }
+        __syncthreads();
+        float2* t = A;
+        A = B;
+        B = t;
+    }
+    return A;
+}
+
 template <int MODE, int DIR>
 __global__ void __launch_bounds__(kMixedThreads)
     k_mixed(const void* in_, void* out_, int64_t nrows, int n, int W, MixedSched sch,
             const float2* __restrict__ tw, const float2* __restrict__ ph, int shift_in,
             int shift_out, float scale, int mmax, int mmajor, uint32_t wmagic,
-            uint32_t kmagic) {
+            uint32_t kmagic, int tn1) {
     constexpr bool PAIR = MODE == BLU_R2C2 || MODE == BLU_C2R2;
     constexpr bool SYN = MODE == BLU_C2R || MODE == BLU_C2R2;
     extern __shared__ float2 smem[];
@@ -193,7 +223,9 @@ __global__ void __launch_bounds__(kMixedThreads)
         const int64_t tr = tr0 + w;
         float2 a = make_float2(0.f, 0.f);
         if (tr < ntr) {
-            if constexpr (MODE == BLU_C2C) {
+            if constexpr (MODE == kMixedRowsT) {
+                a = ldg_stream(static_cast<const float2*>(in_) + tr * n + e);
+            } else if constexpr (MODE == BLU_C2C) {
                 a = ldg_stream(static_cast<const float2*>(in_) + tr * n + e);
                 if (shift_in) a = ctw<+1>(a, __ldg(ph + e));
             } else if constexpr (MODE == BLU_R2C) {
@@ -225,27 +257,32 @@ __global__ void __launch_bounds__(kMixedThreads)
     }
     __syncthreads();
 
-    // ---- the radix passes, A -> B -> A ... ----
-    for (int p = 0; p < sch.npass; ++p) {
-        const float2* twp = tw + sch.off[p];
-        const int ns = sch.span[p];
-        const uint32_t qm = sch.qmagic[p], sm = sch.smagic[p];
-        switch (sch.radix[p]) {
-            case 2: mixed_pass<2, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 3: mixed_pass<3, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 4: mixed_pass<4, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 5: mixed_pass<5, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 7: mixed_pass<7, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            default: mixed_pass<8, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-        }
-        __syncthreads();
-        float2* t = A;
-        A = B;
-        B = t;
-    }
+    A = mixed_passes<DIR>(A, B, n, W, sch, tw);
 
     // ---- store from A ----
-    if constexpr (MODE == BLU_C2C || MODE == BLU_C2R || MODE == BLU_C2R2) {
+    if constexpr (MODE == kMixedRowsT) {
+        // consecutive threads take consecutive rows k1 (adjacent outputs) when W > 1
+        const int64_t nfull = (int64_t)tn1 * n;
+        const int64_t b0 = tr0 / tn1;  // transform and k1 of the CTA's first row
+        const int k10 = (int)(tr0 - b0 * tn1);
+#pragma unroll 4
+        for (int idx = tid; idx < W * n; idx += kMixedThreads) {
+            const int k = mdiv(idx, wmagic), w = idx - k * W;
+            const int64_t tr = tr0 + w;
+            if (tr >= ntr) continue;
+            int k1 = k10 + w;
+            int64_t b = b0;
+            while (k1 >= tn1) {  // rows of the next transform(s)
+                k1 -= tn1;
+                ++b;
+            }
+            const int64_t kk = k1 + (int64_t)tn1 * k;  // frequency index within the transform
+            float2 y = A[w * n + k];
+            if (shift_out) y = ctw<-1>(y, __ldg(ph + kk));
+            stg_stream(static_cast<float2*>(out_) + b * nfull + kk,
+                       make_float2(y.x * scale, y.y * scale));
+        }
+    } else if constexpr (MODE == BLU_C2C || MODE == BLU_C2R || MODE == BLU_C2R2) {
 #pragma unroll 4
         for (int idx = tid; idx < W * n; idx += kMixedThreads) {
             const int w = mdiv(idx, nm), k = idx - w * n;
@@ -294,10 +331,83 @@ __global__ void __launch_bounds__(kMixedThreads)
     }
 }
 
+// First pass of the mixed-radix four-step transform of n = N1*N2 points (the four-step split
+// the CS598 page names, with both factors over {2, 3, 5, 7}): element n1*N2 + n2 of each
+// transform.  CTA (b, t) takes the columns n2 in [t*C, t*C + C) of transform b: it loads the
+// [N1][C] tile with coalesced row runs (the forward fftshift phase of index n1*N2 + n2 on the
+// load) into C rows of N1 points in shared memory, runs the N1-point passes, and writes output
+// (k1, n2) times w_n^{n2*k1} to out[b*n + k1*N2 + n2].  w_n^q = hi[q >> lobits] * lo[q & mask]
+// (plan tables, (cos, sin) of the positive angle, the sign applied at use).
+template <int DIR>
+__global__ void __launch_bounds__(kMixedThreads)
+    k_mixed_cols(const float2* in, float2* out, int n1, int n2, int C, uint32_t cmagic,
+                 int64_t tiles, MixedSched sch, const float2* __restrict__ tw,
+                 const float2* __restrict__ hi, const float2* __restrict__ lo, int lobits,
+                 const float2* __restrict__ ph, int shift_in) {
+    extern __shared__ float2 smem[];
+    float2* A = smem;
+    float2* B = smem + C * n1;
+    const int64_t b = blockIdx.x / tiles;
+    const int c0 = (int)(blockIdx.x - b * tiles) * C;
+    const int64_t n = (int64_t)n1 * n2;
+    const float2* x = in + b * n;
+    float2* y = out + b * n;
+    const int tid = (int)threadIdx.x;
+#pragma unroll 4
+    for (int idx = tid; idx < C * n1; idx += kMixedThreads) {
+        const int r = mdiv(idx, cmagic), c = idx - r * C;
+        float2 a = make_float2(0.f, 0.f);
+        if (c0 + c < n2) {
+            const int64_t j = (int64_t)r * n2 + c0 + c;
+            a = ldg_stream(x + j);
+            if (shift_in) a = ctw<+1>(a, __ldg(ph + j));
+        }
+        A[c * n1 + r] = a;
+    }
+    __syncthreads();
+    A = mixed_passes<DIR>(A, B, n1, C, sch, tw);
+    const uint32_t lomask = (1u << lobits) - 1u;
+#pragma unroll 4
+    for (int idx = tid; idx < C * n1; idx += kMixedThreads) {
+        const int k1 = mdiv(idx, cmagic), c = idx - k1 * C;
+        if (c0 + c >= n2) continue;
+        const uint32_t q = (uint32_t)(c0 + c) * (uint32_t)k1;  // < n: no reduction needed
+        const float2 w = cmul(__ldg(hi + (q >> lobits)), __ldg(lo + (q & lomask)));
+        stg_stream(y + (int64_t)k1 * n2 + c0 + c, ctw<DIR>(A[c * n1 + k1], w));
+    }
+}
+
+template <int DIR>
+cudaError_t launch_mixed_cols(const float2* in, float2* out, int64_t batch, int n1, int n2,
+                              const MixedSched& sch, const float2* tw, const float2* hi,
+                              const float2* lo, int lobits, const float2* ph, int shift_in,
+                              cudaStream_t stream) {
+    auto kern = k_mixed_cols<DIR>;
+    static LaunchCache cache;
+    LaunchGeom geo;
+    cudaError_t e = cache.get(
+        [&](int, LaunchGeom*) {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)mixed_cols_smem_bytes(kMaxMixedN1));
+        },
+        &geo);
+    if (e != cudaSuccess) return e;
+    if (n1 < 2 || n1 > kMaxMixedN1 || n2 < 2) return cudaErrorInvalidValue;
+    const int C = mixed_cols_per_cta(n1);
+    const int64_t tiles = (n2 + C - 1) / C;
+    const int64_t grid = batch * tiles;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, kMixedThreads, mixed_cols_smem_bytes(n1), stream>>>(
+        in, out, n1, n2, C, div_magic((uint32_t)C), tiles, sch, tw, hi, lo, lobits, ph,
+        shift_in);
+    return cudaGetLastError();
+}
+
 template <int MODE, int DIR>
 cudaError_t launch_mixed(const void* in, void* out, int64_t nrows, int n, const MixedSched& sch,
                          const float2* tw, const float2* ph, int shift_in, int shift_out,
-                         float scale, int mmax, int mmajor, cudaStream_t stream) {
+                         float scale, int mmax, int mmajor, int tn1, cudaStream_t stream) {
     if (n < 2 || n > kMaxMixedN) return cudaErrorInvalidValue;
     auto kern = k_mixed<MODE, DIR>;
     static LaunchCache cache;
@@ -317,7 +427,7 @@ cudaError_t launch_mixed(const void* in, void* out, int64_t nrows, int n, const 
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kMixedThreads, mixed_smem_bytes(n), stream>>>(
         in, out, nrows, n, W, sch, tw, ph, shift_in, shift_out, scale, mmax, mmajor,
-        div_magic((uint32_t)W), div_magic((uint32_t)(mmax + 1)));
+        div_magic((uint32_t)W), div_magic((uint32_t)(mmax + 1)), tn1);
     return cudaGetLastError();
 }
 

@@ -49,9 +49,21 @@ def smooth(n):
     return n == 1
 
 
-def expected_path(n):
-    mixed = smooth(n) and n <= 8192 and os.environ.get("GBFFT_FORCE_PATH") != "chirpz"
-    return "path=mixed" if mixed else "path=bluestein"
+def mixed_split_exists(n):
+    """The planner's four-step split of a long smooth length: a divisor N1 <= min(512, sqrt n)
+    with n / N1 <= 8192."""
+    return any(n % d == 0 and n // d <= 8192 for d in range(2, min(512, int(n ** 0.5)) + 1))
+
+
+def expected_path(n, real=False):
+    """The path prefix the planner must choose: mixed-radix (one pass up to 8192 points, two
+    passes above for complex rows) for lengths whose prime factors are 2, 3, 5, 7, chirp-z
+    otherwise or when forced."""
+    if os.environ.get("GBFFT_FORCE_PATH") == "chirpz" or not smooth(n):
+        return "path=bluestein"
+    if n <= 8192 or (not real and n <= 1 << 20 and mixed_split_exists(n)):
+        return "path=mixed"
+    return "path=bluestein"
 
 
 @pytest.fixture(params=["default", "chirpz"])
@@ -153,7 +165,7 @@ def gpu_c2r(F_rowmajor, n, mmax, layout):
     m = fx()
     rows = F_rowmajor.shape[0]
     p = m.Plan(n, rows, 1, m.INVERSE, layout=LAYOUTS[layout], mmax=mmax)
-    assert expected_path(n) in p.describe()
+    assert expected_path(n, real=True) in p.describe()
     Fin = oracle.to_mmajor(F_rowmajor) if layout == "mmajor" else F_rowmajor
     x = p.c2r(torch.from_numpy(np.ascontiguousarray(Fin, dtype=np.complex64)).cuda())
     torch.cuda.synchronize()
@@ -165,7 +177,7 @@ def gpu_r2c(x, mmax, layout):
     m = fx()
     rows, n = x.shape
     p = m.Plan(n, rows, 1, m.FORWARD, layout=LAYOUTS[layout], mmax=mmax)
-    assert expected_path(n) in p.describe()
+    assert expected_path(n, real=True) in p.describe()
     F = p.r2c(torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda())
     torch.cuda.synchronize()
     p.check()
@@ -215,7 +227,7 @@ def test_any_length_real_round_trip(n, route):
 # ---- lengths above 8192: the multi-pass chirp-z (four-step m-point passes over a workspace) --
 # References come from the oracle's mixed-radix FFT (smallest prime factor first; a prime length
 # is its direct sum), pinned to numpy: the direct O(n^2) sum of oracle.transform is too slow here.
-LONG_LENGTHS = [8193, 10000, 12289, 65535, 100000, 531441, (1 << 20) - 1]
+LONG_LENGTHS = [8193, 9000, 10000, 12289, 65535, 100000, 531441, 1000000, (1 << 20) - 1]
 
 
 def long_ref(x, direction, shift=False):
@@ -228,27 +240,49 @@ def long_ref(x, direction, shift=False):
 
 @pytest.mark.parametrize("n", LONG_LENGTHS)
 @pytest.mark.parametrize("direction", [-1, 1])
-def test_long_any_length_grid(n, direction):
-    """A prime (12289), products of small primes and the largest length (m = 2^21), both
-    directions, against the oracle's mixed-radix DFT."""
+def test_long_any_length_grid(n, direction, route):
+    """A prime (12289), products of small primes (the mixed-radix four-step path, and forced
+    onto the multi-pass chirp-z) and the largest length (m = 2^21), both directions, against
+    the oracle's mixed-radix DFT."""
+    skip_same(n, route)
     batch = 3 if n <= 100000 else 2
     x = wl().normal(7500 + n, batch, n)
     m = fx()
-    assert "path=bluestein_multipass" in m.query(n, batch, 1, direction)
+    want = "path=mixed_fourstep" if expected_path(n) == "path=mixed" else "path=bluestein_multipass"
+    assert want in m.query(n, batch, 1, direction)
     got = gpu_c2c(x, n, batch, direction)
     assert_parity(got, long_ref(x, direction), n, f"long n={n} dir={direction}")
 
 
-@pytest.mark.parametrize("n", [10000, 10001, 2 * 3 ** 10])
+@pytest.mark.parametrize("n", [10000, 10001, 2 * 3 ** 10, 7 ** 5 * 5])
 @pytest.mark.parametrize("direction", [-1, 1])
-def test_long_any_length_shift_in_place(n, direction):
+def test_long_any_length_shift_in_place(n, direction, route):
+    skip_same(n, route)
     batch = 2
     x = wl().uniform(7600 + n, batch, n)
     got = gpu_c2c(x, n, batch, direction, shift=True, inplace=True)
     assert_parity(got, long_ref(x, direction, True), n, f"long shift n={n}")
 
 
-def test_long_any_length_round_trip_and_tones():
+def test_long_full_batch_sampled():
+    """The benchmark's long any-length workload at full size (n = 100000, batch = 671: the
+    mixed-radix four-step path over a 537 MB workspace), sampled rows against the oracle."""
+    m = fx()
+    n = 100000
+    batch = (1 << 26) // n
+    x = wl().tones(7350, batch, n)
+    p = m.Plan(n, batch, 1, m.FORWARD)
+    assert "path=mixed_fourstep" in p.describe()
+    y = p.c2c(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    p.check()
+    rng = np.random.default_rng(7350)
+    rows = np.array(sorted({0, batch - 1, batch // 2, *rng.integers(0, batch, 9).tolist()}))
+    ys = y[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_parity(ys, long_ref(x[rows], -1), n, "n=100000 full batch")
+
+
+def test_long_any_length_round_trip_and_tones(route):
     n, batch = 100000, 2
     x = wl().tones(7700, batch, n)
     y = gpu_c2c(x, n, batch, -1)
