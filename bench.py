@@ -8,7 +8,7 @@ resident in HBM.  The default workload is the batched 1-D C2C round trip: N = 40
 (-1)^j chessboard on its load, then the inverse transform (chessboard on its store) -- two
 kernel launches per step.  Other workloads (--workload): c2c_1024 (N = 1024 x 64 rows, forward),
 sweep_<log2n> (batch*N = 2^26 rows of 3 tones + noise, forward), any_<n> (the same for a
-length n <= 2^20 that is not a power of two: the mixed-radix path for n <= 8192 with prime
+length n <= 2^20 that is not a power of two: the mixed-radix path for lengths with prime
 factors 2, 3, 5, 7 only, else the chirp-z path), realany_<n> (the real
 workload below for such a length, mmax = n/3; realanypair_<n>: two rows per transform), real
 (2048 rows x 4096, mmax = 1365, synthesis then analysis, m-major spectrum; realpair: two rows
@@ -70,7 +70,12 @@ def any_length_path(n):
     for f in (2, 3, 5, 7):
         while m % f == 0:
             m //= f
-    return "mixed-radix path" if m == 1 and n <= 8192 else "chirp-z path"
+    if m == 1 and n <= 8192:
+        return "mixed-radix path"
+    if m == 1 and n <= 1 << 20 and any(n % d == 0 and n // d <= 8192
+                                       for d in range(2, min(512, int(n ** 0.5)) + 1)):
+        return "mixed-radix four-step path"
+    return "chirp-z path"
 
 
 class Workload:

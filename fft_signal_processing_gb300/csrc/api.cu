@@ -40,6 +40,7 @@
 #include "fft_kernel.cuh"
 #include "host_tables.h"
 #include "kernels.h"
+#include "mixed.h"
 #include "tma.cuh"
 
 using namespace gbfft;
@@ -159,10 +160,10 @@ int plan_spec(int64_t n, int64_t batch, int dims, int direction, int layout, int
     s.log2n = l;
     int rad[kMaxMixedPasses], rad1[kMaxMixedPasses];
     const int nmix = any_length && n <= kMaxMixedN ? mixed_schedule(n, rad) : 0;
-    // long rows: the split and both schedules (complex rows; real rows keep the chirp-z path)
+    // long rows: the split and both schedules (real rows two per transform)
     int n1 = 0, nmix1 = 0, nmix2 = 0;
-    if (any_length && n > kMaxMixedN && n <= kMaxMixedFourStepN && layout == FFT_LAYOUT_C2C &&
-        force != FORCE_CHIRPZ && (n1 = mixed_split(n)) > 0) {
+    if (any_length && n > kMaxMixedN && n <= kMaxMixedFourStepN && force != FORCE_CHIRPZ &&
+        (n1 = mixed_split(n)) > 0) {
         nmix1 = mixed_schedule(n1, rad1);
         nmix2 = mixed_schedule(n / n1, rad);
     }
@@ -354,13 +355,23 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
             std::string r1, r2;
             for (int p = 0; p < s.nmix1; ++p) r1 += (p ? "x" : "") + std::to_string(s.mix_radix1[p]);
             for (int p = 0; p < s.nmix; ++p) r2 += (p ? "x" : "") + std::to_string(s.mix_radix[p]);
+            const bool real = s.layout != FFT_LAYOUT_C2C;
+            char what[128];
+            if (real)
+                snprintf(what, sizeof what, "%s mmax=%lld layout=%s rows_per_transform=2 kernels=%d",
+                         s.direction < 0 ? "analysis(r2c)" : "synthesis(c2r)", (long long)mmax,
+                         s.layout == FFT_LAYOUT_REAL_MMAJOR ? "mmajor" : "rowmajor",
+                         s.direction < 0 ? 3 : 2);
+            else
+                snprintf(what, sizeof what, "%s shift=%d kernels=2", dir, s.shift);
             snprintf(buf, sizeof buf,
-                     "path=mixed_fourstep n=%lld batch=%lld %s shift=%d n1=%d n2=%d kernels=2 "
+                     "path=mixed_fourstep n=%lld batch=%lld %s n1=%d n2=%d "
                      "pass1=columns(radix=%s cols_per_cta=%d smem=%zu) "
-                     "pass2=rows_transposed(radix=%s rows_per_cta=%d smem=%zu)",
-                     (long long)s.n, (long long)s.batch, dir, s.shift, s.mix_n1, s.mix_n2,
+                     "pass2=rows_transposed(radix=%s rows_per_cta=%d smem=%zu)%s",
+                     (long long)s.n, (long long)s.batch, what, s.mix_n1, s.mix_n2,
                      r1.c_str(), mixed_cols_per_cta(s.mix_n1), mixed_cols_smem_bytes(s.mix_n1),
-                     r2.c_str(), mixed_rows_per_cta(s.mix_n2), mixed_smem_bytes(s.mix_n2));
+                     r2.c_str(), mixed_rows_per_cta(s.mix_n2), mixed_smem_bytes(s.mix_n2),
+                     real && s.direction < 0 ? " pass3=unpack" : "");
             break;
         }
         case PATH_BLUESTEIN_MP: {
@@ -581,7 +592,10 @@ static int create_from_spec(const PlanSpec& s, fft_plan* out) {
             p->off_lo = host::append_roots_any(tw, nlo, 1, s.n);                  // w_n^{ql}
             p->off_hi = host::append_roots_any(tw, (s.n + nlo - 1) / nlo, nlo, s.n);  // w_n^{qh*nlo}
             if (s.shift) p->off_chirp = host::append_phase(tw, s.n, s.n / 2);
-            p->work_bytes = (size_t)s.batch * (size_t)s.n * sizeof(float2);
+            // complex rows: one workspace; real rows (two per transform): the column pass's
+            // output and, for the analysis, the row pass's spectra before the unpack
+            const int64_t ntr = s.layout == FFT_LAYOUT_C2C ? s.batch : 2 * ((s.batch + 1) / 2);
+            p->work_bytes = (size_t)ntr * (size_t)s.n * sizeof(float2);
             break;
         }
         case PATH_MIXED: {
@@ -822,7 +836,20 @@ int fft_exec_r2c(fft_plan p, const float* in, void* out, void* stream) {
     if (p->index_only && !index_only_supported(p)) return FFT_ERR_UNSUPPORTED_SIZE;
     const int diag = p->index_only ? KF_INDEX_ONLY : 0;
     cudaError_t e;
-    if (s.path == PATH_MIXED)
+    if (s.path == PATH_MIXED_FS) {  // pack, columns; rows; unpack
+        const cudaStream_t st = (cudaStream_t)stream;
+        const int64_t ntr = (s.batch + 1) / 2;
+        float2* A = (float2*)p->d_work;
+        float2* B = A + ntr * s.n;
+        e = run_mixed_cols_real(BLU_R2C2, in, A, s.batch, s.mix_n1, s.mix_n2, p->mix1,
+                                p->d_tw + p->off_a, p->d_tw + p->off_hi, p->d_tw + p->off_lo,
+                                kMixedTwLoBits, (int)p->mmax, mmajor, st);
+        if (e == cudaSuccess)
+            e = run_mixed(kMixedRowsT, -1, A, B, ntr * s.mix_n1, s.mix_n2, p->mix,
+                          p->d_tw + p->off_b, p->d_tw, 0, 0, 1.f, 0, 0, st, s.mix_n1);
+        if (e == cudaSuccess)
+            e = run_mixed_unpack(B, (float2*)out, s.batch, (int)s.n, (int)p->mmax, mmajor, st);
+    } else if (s.path == PATH_MIXED)
         e = run_mixed(p->real_pair ? BLU_R2C2 : BLU_R2C, -1, in, out, s.batch, (int)s.n, p->mix,
                       p->d_tw + p->off_a, nullptr, 0, 0, 1.f, (int)p->mmax, mmajor,
                       (cudaStream_t)stream);
@@ -855,7 +882,16 @@ int fft_exec_c2r(fft_plan p, const void* in, float* out, void* stream) {
     if (p->index_only && !index_only_supported(p)) return FFT_ERR_UNSUPPORTED_SIZE;
     const int diag = p->index_only ? KF_INDEX_ONLY : 0;
     cudaError_t e;
-    if (s.path == PATH_MIXED)
+    if (s.path == PATH_MIXED_FS) {  // assemble, columns; rows split into the real rows
+        const cudaStream_t st = (cudaStream_t)stream;
+        float2* A = (float2*)p->d_work;
+        e = run_mixed_cols_real(BLU_C2R2, in, A, s.batch, s.mix_n1, s.mix_n2, p->mix1,
+                                p->d_tw + p->off_a, p->d_tw + p->off_hi, p->d_tw + p->off_lo,
+                                kMixedTwLoBits, (int)p->mmax, mmajor, st);
+        if (e == cudaSuccess)
+            e = run_mixed_rows_split(A, out, s.batch, s.mix_n1, s.mix_n2, p->mix,
+                                     p->d_tw + p->off_b, st);
+    } else if (s.path == PATH_MIXED)
         e = run_mixed(p->real_pair ? BLU_C2R2 : BLU_C2R, +1, in, out, s.batch, (int)s.n, p->mix,
                       p->d_tw + p->off_a, nullptr, 0, 0, 1.f, (int)p->mmax, mmajor,
                       (cudaStream_t)stream);

@@ -31,6 +31,7 @@
 #include "fft_common.cuh"
 #include "kernels.h"
 #include "launch_cache.cuh"
+#include "mixed.h"
 
 namespace gbfft {
 
@@ -165,7 +166,8 @@ __device__ __forceinline__ void mixed_pass(const float2* A, float2* B, int n, in
 // MODE: BLU_C2C, BLU_R2C, BLU_C2R, BLU_R2C2, BLU_C2R2, or kMixedRowsT: the second pass of the
 // mixed-radix four-step transform (rows tr = b*N1 + k1 of n = N2 points; output k2 of the row
 // stored at X[b*N1*N2 + k1 + N1*k2], with the inverse fftshift phase of index k1 + N1*k2 and
-// the scale; tn1 = N1).
+// the scale; tn1 = N1), or kMixedRowsT2: the same for the synthesis of two real rows per
+// transform (Re and Im of X to rows 2b and 2b + 1 of nreal real rows).
 // Every pass of the schedule over W rows of n points, A -> B -> A ...; returns the buffer that
 // holds the result (every thread's writes visible after the closing barrier).
 template <int DIR>
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kMixedThreads)
     k_mixed(const void* in_, void* out_, int64_t nrows, int n, int W, MixedSched sch,
             const float2* __restrict__ tw, const float2* __restrict__ ph, int shift_in,
             int shift_out, float scale, int mmax, int mmajor, uint32_t wmagic,
-            uint32_t kmagic, int tn1) {
+            uint32_t kmagic, int tn1, int64_t nreal) {
     constexpr bool PAIR = MODE == BLU_R2C2 || MODE == BLU_C2R2;
     constexpr bool SYN = MODE == BLU_C2R || MODE == BLU_C2R2;
     extern __shared__ float2 smem[];
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kMixedThreads)
         const int64_t tr = tr0 + w;
         float2 a = make_float2(0.f, 0.f);
         if (tr < ntr) {
-            if constexpr (MODE == kMixedRowsT) {
+            if constexpr (MODE == kMixedRowsT || MODE == kMixedRowsT2) {
                 a = ldg_stream(static_cast<const float2*>(in_) + tr * n + e);
             } else if constexpr (MODE == BLU_C2C) {
                 a = ldg_stream(static_cast<const float2*>(in_) + tr * n + e);
@@ -260,7 +262,29 @@ __global__ void __launch_bounds__(kMixedThreads)
     A = mixed_passes<DIR>(A, B, n, W, sch, tw);
 
     // ---- store from A ----
-    if constexpr (MODE == kMixedRowsT) {
+    if constexpr (MODE == kMixedRowsT2) {
+        // synthesis of two real rows per transform: Re y -> row 2b, Im y -> row 2b + 1 of the
+        // nreal rows, at k1 + N1*k2 (tn1 = N1)
+        const int64_t nfull = (int64_t)tn1 * n;
+        const int64_t b0 = tr0 / tn1;
+        const int k10 = (int)(tr0 - b0 * tn1);
+#pragma unroll 4
+        for (int idx = tid; idx < W * n; idx += kMixedThreads) {
+            const int k = mdiv(idx, wmagic), w = idx - k * W;
+            const int64_t tr = tr0 + w;
+            if (tr >= ntr) continue;
+            int k1 = k10 + w;
+            int64_t b = b0;
+            while (k1 >= tn1) {
+                k1 -= tn1;
+                ++b;
+            }
+            const float2 v = A[w * n + k];
+            float* xr = static_cast<float*>(out_) + 2 * b * nfull + k1 + (int64_t)tn1 * k;
+            __stcs(xr, v.x);
+            if (2 * b + 1 < nreal) __stcs(xr + nfull, v.y);
+        }
+    } else if constexpr (MODE == kMixedRowsT) {
         // consecutive threads take consecutive rows k1 (adjacent outputs) when W > 1
         const int64_t nfull = (int64_t)tn1 * n;
         const int64_t b0 = tr0 / tn1;  // transform and k1 of the CTA's first row
@@ -338,29 +362,56 @@ __global__ void __launch_bounds__(kMixedThreads)
 // load) into C rows of N1 points in shared memory, runs the N1-point passes, and writes output
 // (k1, n2) times w_n^{n2*k1} to out[b*n + k1*N2 + n2].  w_n^q = hi[q >> lobits] * lo[q & mask]
 // (plan tables, (cos, sin) of the positive angle, the sign applied at use).
-template <int DIR>
+// MODE BLU_C2C: complex rows (in: [batch][n] complex64).  Band-limited real rows, two per
+// transform b (rows 2b, 2b+1 of nrows): BLU_R2C2 loads y = x1 + i x2 (in: [nrows][n] float32);
+// BLU_C2R2 assembles Y_j = X1_j + i X2_j from the two Hermitian spectra (in: the spectrum, in
+// the plan's layout; X_0 and a Nyquist bin real, X_{n-m} = conj F_m).
+template <int MODE, int DIR>
 __global__ void __launch_bounds__(kMixedThreads)
-    k_mixed_cols(const float2* in, float2* out, int n1, int n2, int C, uint32_t cmagic,
+    k_mixed_cols(const void* in_, float2* out, int n1, int n2, int C, uint32_t cmagic,
                  int64_t tiles, MixedSched sch, const float2* __restrict__ tw,
                  const float2* __restrict__ hi, const float2* __restrict__ lo, int lobits,
-                 const float2* __restrict__ ph, int shift_in) {
+                 const float2* __restrict__ ph, int shift_in, int64_t nrows, int mmax,
+                 int mmajor) {
     extern __shared__ float2 smem[];
     float2* A = smem;
     float2* B = smem + C * n1;
     const int64_t b = blockIdx.x / tiles;
     const int c0 = (int)(blockIdx.x - b * tiles) * C;
     const int64_t n = (int64_t)n1 * n2;
-    const float2* x = in + b * n;
     float2* y = out + b * n;
     const int tid = (int)threadIdx.x;
+    const int64_t r1 = 2 * b;  // real modes: the transform's first row
+    const bool has2 = r1 + 1 < nrows;
 #pragma unroll 4
     for (int idx = tid; idx < C * n1; idx += kMixedThreads) {
         const int r = mdiv(idx, cmagic), c = idx - r * C;
         float2 a = make_float2(0.f, 0.f);
         if (c0 + c < n2) {
             const int64_t j = (int64_t)r * n2 + c0 + c;
-            a = ldg_stream(x + j);
-            if (shift_in) a = ctw<+1>(a, __ldg(ph + j));
+            if constexpr (MODE == BLU_C2C) {
+                a = ldg_stream(static_cast<const float2*>(in_) + b * n + j);
+                if (shift_in) a = ctw<+1>(a, __ldg(ph + j));
+            } else if constexpr (MODE == BLU_R2C2) {
+                const float* xf = static_cast<const float*>(in_) + r1 * n + j;
+                a.x = __ldcs(xf);
+                if (has2) a.y = __ldcs(xf + n);
+            } else if (j <= mmax || j >= n - mmax) {  // BLU_C2R2
+                const float2* F = static_cast<const float2*>(in_);
+                const int64_t m = j <= mmax ? j : n - j;
+                float2 f1 = ldg_stream(F + (mmajor ? m * nrows + r1 : r1 * (mmax + 1) + m));
+                float2 f2 = make_float2(0.f, 0.f);
+                if (has2)
+                    f2 = ldg_stream(F + (mmajor ? m * nrows + r1 + 1 : (r1 + 1) * (mmax + 1) + m));
+                if (j == 0 || 2 * j == n) {  // X_0 and a Nyquist bin are real
+                    f1.y = 0.f;
+                    f2.y = 0.f;
+                } else if (j > mmax) {  // mirrored bin: conj
+                    f1.y = -f1.y;
+                    f2.y = -f2.y;
+                }
+                a = make_float2(f1.x - f2.y, f1.y + f2.x);
+            }
         }
         A[c * n1 + r] = a;
     }
@@ -377,12 +428,13 @@ __global__ void __launch_bounds__(kMixedThreads)
     }
 }
 
-template <int DIR>
-cudaError_t launch_mixed_cols(const float2* in, float2* out, int64_t batch, int n1, int n2,
+// batch: transforms (real modes: (nrows + 1) / 2).
+template <int MODE, int DIR>
+cudaError_t launch_mixed_cols(const void* in, float2* out, int64_t batch, int n1, int n2,
                               const MixedSched& sch, const float2* tw, const float2* hi,
                               const float2* lo, int lobits, const float2* ph, int shift_in,
-                              cudaStream_t stream) {
-    auto kern = k_mixed_cols<DIR>;
+                              int64_t nrows, int mmax, int mmajor, cudaStream_t stream) {
+    auto kern = k_mixed_cols<MODE, DIR>;
     static LaunchCache cache;
     LaunchGeom geo;
     cudaError_t e = cache.get(
@@ -400,14 +452,44 @@ cudaError_t launch_mixed_cols(const float2* in, float2* out, int64_t batch, int 
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kMixedThreads, mixed_cols_smem_bytes(n1), stream>>>(
         in, out, n1, n2, C, div_magic((uint32_t)C), tiles, sch, tw, hi, lo, lobits, ph,
-        shift_in);
+        shift_in, nrows, mmax, mmajor);
     return cudaGetLastError();
+}
+
+// The unpack after the analysis of two real rows per transform: Y = the n-point spectra
+// [ntr][n] of y = x1 + i x2; bins m <= mmax of both rows, X1_m = (Y_m + conj Y_{n-m})/2,
+// X2_m = (Y_m - conj Y_{n-m})/(2i) (Mota §2.6 Eq. 17-18), bins 0 and n/2 real, into the
+// spectrum layout.  Grid: (m blocks, transforms).
+__global__ void __launch_bounds__(kMixedThreads)
+    k_mixed_unpack(const float2* __restrict__ Y, float2* F, int64_t nrows, int n, int mmax,
+                   int mmajor) {
+    const int64_t ntr = (nrows + 1) / 2;
+    for (int64_t t = blockIdx.y; t < ntr; t += gridDim.y) {
+        const float2* yr = Y + t * n;
+        const int64_t r1 = 2 * t;
+        const bool has2 = r1 + 1 < nrows;
+        for (int m = blockIdx.x * kMixedThreads + (int)threadIdx.x; m <= mmax;
+             m += gridDim.x * kMixedThreads) {
+            const float2 ym = ldg_stream(yr + m), yn = ldg_stream(yr + (m == 0 ? 0 : n - m));
+            float2 f1 = make_float2(0.5f * (ym.x + yn.x), 0.5f * (ym.y - yn.y));
+            float2 f2 = make_float2(0.5f * (ym.y + yn.y), 0.5f * (yn.x - ym.x));
+            if (m == 0 || 2 * m == n) {  // real bins: drop the rounding residue
+                f1.y = 0.f;
+                f2.y = 0.f;
+            }
+            stg_stream(F + (mmajor ? (int64_t)m * nrows + r1 : r1 * (mmax + 1) + m), f1);
+            if (has2)
+                stg_stream(F + (mmajor ? (int64_t)m * nrows + r1 + 1 : (r1 + 1) * (mmax + 1) + m),
+                           f2);
+        }
+    }
 }
 
 template <int MODE, int DIR>
 cudaError_t launch_mixed(const void* in, void* out, int64_t nrows, int n, const MixedSched& sch,
                          const float2* tw, const float2* ph, int shift_in, int shift_out,
-                         float scale, int mmax, int mmajor, int tn1, cudaStream_t stream) {
+                         float scale, int mmax, int mmajor, int tn1, cudaStream_t stream,
+                         int64_t nreal = 0) {
     if (n < 2 || n > kMaxMixedN) return cudaErrorInvalidValue;
     auto kern = k_mixed<MODE, DIR>;
     static LaunchCache cache;
@@ -427,7 +509,7 @@ cudaError_t launch_mixed(const void* in, void* out, int64_t nrows, int n, const 
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     kern<<<(unsigned)grid, kMixedThreads, mixed_smem_bytes(n), stream>>>(
         in, out, nrows, n, W, sch, tw, ph, shift_in, shift_out, scale, mmax, mmajor,
-        div_magic((uint32_t)W), div_magic((uint32_t)(mmax + 1)), tn1);
+        div_magic((uint32_t)W), div_magic((uint32_t)(mmax + 1)), tn1, nreal);
     return cudaGetLastError();
 }
 

@@ -78,10 +78,11 @@ enum {
  *             rows, dims 1; for real rows this is the any-nphi role of the direct-sum 'dft'
  *             mode of fourier.ts).  Lengths n <= 8192 whose prime factors are 2, 3, 5 and 7
  *             run mixed-radix Stockham passes (radices 2, 3, 4, 5, 7, 8) in one kernel (the
- *             mixed-radix extension of the radix-2^k passes, Mota §2.3); complex rows of such
+ *             mixed-radix extension of the radix-2^k passes, Mota §2.3); rows of such
  *             lengths above 8192 run two mixed-radix passes, n = N1*N2 (columns with the
  *             four-step twiddle, then rows with a transposed store, through a plan workspace
- *             of batch*n complex64); every other length is computed as the chirp-z (Bluestein)
+ *             of batch*n complex64; real rows two per transform, the analysis with a third,
+ *             unpack pass); every other length is computed as the chirp-z (Bluestein)
  *             transform X_k = c_k sum_j (x_j c_j) conj(c_{k-j}), c_j = exp(s*pi*i*j^2/n),
  *             through power-of-two FFTs of length m >= 2n - 1 (the same unnormalised DFT of
  *             Mota, "High Performance Fourier Transforms on GPUs with GLSL", 2.2 Eq. 5, for

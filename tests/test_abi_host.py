@@ -92,17 +92,21 @@ def test_smooth_lengths_take_the_mixed_radix_path(n, radix, monkeypatch):
                                       (100000, 250, 400), (531441, 243, 2187),
                                       (823543, 343, 2401), (1000000, 500, 2000)])
 def test_long_smooth_lengths_take_the_mixed_fourstep_path(n, n1, n2, monkeypatch):
-    """Complex rows above 8192 points whose prime factors are 2, 3, 5, 7 take two mixed-radix
-    passes, split n = N1*N2 with N1 the largest divisor up to min(512, sqrt(n)) that leaves
-    N2 <= 8192; real rows of these lengths, and the forced chirp-z route, take the multi-pass
-    chirp-z path."""
+    """Rows above 8192 points whose prime factors are 2, 3, 5, 7 take two mixed-radix passes
+    (real rows two per transform, the analysis with a third, unpack pass), split n = N1*N2
+    with N1 the largest divisor up to min(512, sqrt(n)) that leaves N2 <= 8192; the forced
+    chirp-z route takes the multi-pass chirp-z path."""
     d = fx.query(n, 3)
     assert "path=mixed_fourstep" in d and f"n1={n1} n2={n2} " in d and "kernels=2" in d
     assert n1 * n2 == n and n1 <= 512 and n2 <= 8192 and n1 * n1 <= n
     assert q(n, shift=1) == fx.FFT_OK
-    assert "path=bluestein_multipass" in fx.query(n, 3, layout=1)
+    d = fx.query(n, 3, layout=1)
+    assert "path=mixed_fourstep" in d and "rows_per_transform=2" in d and "kernels=3" in d
+    d = fx.query(n, 3, layout=2, direction=1)
+    assert "path=mixed_fourstep" in d and "synthesis" in d and "kernels=2" in d
     monkeypatch.setenv("GBFFT_FORCE_PATH", "chirpz")
     assert "path=bluestein_multipass" in fx.query(n, 3)
+    assert "path=bluestein_multipass" in fx.query(n, 3, layout=1)
 
 
 @pytest.mark.parametrize("n,m", [(8193, 1 << 15), (12289, 1 << 15), (16385, 1 << 16),

@@ -56,12 +56,12 @@ def mixed_split_exists(n):
 
 
 def expected_path(n, real=False):
-    """The path prefix the planner must choose: mixed-radix (one pass up to 8192 points, two
-    passes above for complex rows) for lengths whose prime factors are 2, 3, 5, 7, chirp-z
-    otherwise or when forced."""
+    """The path prefix the planner must choose: mixed-radix (one pass up to 8192 points, the
+    four-step above) for lengths whose prime factors are 2, 3, 5, 7, chirp-z otherwise or when
+    forced; the same for complex and real rows."""
     if os.environ.get("GBFFT_FORCE_PATH") == "chirpz" or not smooth(n):
         return "path=bluestein"
-    if n <= 8192 or (not real and n <= 1 << 20 and mixed_split_exists(n)):
+    if n <= 8192 or (n <= 1 << 20 and mixed_split_exists(n)):
         return "path=mixed"
     return "path=bluestein"
 
@@ -292,11 +292,14 @@ def test_long_any_length_round_trip_and_tones(route):
 
 
 @pytest.mark.parametrize("n,mmaxes", [(10000, (0, 3333, 4999, 5000)), (10001, (1, 5000)),
-                                      (100000, (0, 1000))])
+                                      (100000, (0, 1000)), (3 ** 9, (1, 9841))])
 @pytest.mark.parametrize("layout", ["rowmajor", "mmajor"])
-def test_long_real_rows(n, mmaxes, layout):
-    """Band-limited real rows above 8192 points (two rows per chirp-z transform), odd and
-    even row counts, against the oracle's direct analysis and synthesis sums."""
+def test_long_real_rows(n, mmaxes, layout, route):
+    """Band-limited real rows above 8192 points, two rows per transform (the mixed-radix
+    four-step for lengths with prime factors 2, 3, 5, 7, and forced onto the chirp-z; the
+    chirp-z otherwise), odd and even row counts, against the oracle's direct analysis and
+    synthesis sums."""
+    skip_same(n, route)
     for i, mmax in enumerate(mmaxes):
         rows = (3, 4)[i % 2]
         F = wl().spectrum(7800 + n + i, rows, mmax)
