@@ -342,13 +342,15 @@ std::string describe_spec(const PlanSpec& s, int64_t mmax, int real_pair = 0) {
                 snprintf(what, sizeof what, "%s shift=%d", dir, s.shift);
             std::string rs;
             for (int p = 0; p < s.nmix; ++p) rs += (p ? "x" : "") + std::to_string(s.mix_radix[p]);
+            const int64_t ntr = real && real_pair ? (s.batch + 1) / 2 : s.batch;
+            const bool small = mixed_small_cta((int)s.n, ntr);
             snprintf(buf, sizeof buf,
                      "path=mixed n=%lld batch=%lld %s%s radix=%s kernels=1 threads=%d "
                      "rows_per_cta=%d smem=%zu",
                      (long long)s.n, (long long)s.batch, what,
                      real && real_pair ? " rows_per_transform=2" : "", rs.c_str(),
-                     kMixedThreadsHost, mixed_rows_per_cta((int)s.n),
-                     mixed_smem_bytes((int)s.n));
+                     mixed_threads_for(small), mixed_rows_for((int)s.n, small),
+                     mixed_smem_bytes_for((int)s.n, small));
             break;
         }
         case PATH_MIXED_FS: {

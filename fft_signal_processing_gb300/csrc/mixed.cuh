@@ -135,14 +135,15 @@ __device__ __forceinline__ int mdiv(int x, uint32_t magic) {
     return magic ? (int)__umulhi((uint32_t)x, magic) : x;
 }
 
-// One Stockham pass of radix R over the CTA's W rows (row stride n in both buffers).
-template <int R, int DIR>
+// One Stockham pass of radix R over the CTA's W rows (row stride n in both buffers), by a CTA
+// of THREADS threads.
+template <int R, int DIR, int THREADS>
 __device__ __forceinline__ void mixed_pass(const float2* A, float2* B, int n, int W, int Ns,
                                            uint32_t qmagic, uint32_t smagic,
                                            const float2* __restrict__ twp) {
     const int q = n / R;  // butterflies per row
     const int total = W * q;
-    for (int idx = (int)threadIdx.x; idx < total; idx += kMixedThreads) {
+    for (int idx = (int)threadIdx.x; idx < total; idx += THREADS) {
         const int w = mdiv(idx, qmagic);
         const int j = idx - w * q;
         const float2* a = A + w * n;
@@ -170,7 +171,7 @@ __device__ __forceinline__ void mixed_pass(const float2* A, float2* B, int n, in
 // transform (Re and Im of X to rows 2b and 2b + 1 of nreal real rows).
 // Every pass of the schedule over W rows of n points, A -> B -> A ...; returns the buffer that
 // holds the result (every thread's writes visible after the closing barrier).
-template <int DIR>
+template <int DIR, int THREADS>
 __device__ __forceinline__ float2* mixed_passes(float2* A, float2* B, int n, int W,
                                                 const MixedSched& sch,
                                                 const float2* __restrict__ tw) {
@@ -179,12 +180,12 @@ __device__ __forceinline__ float2* mixed_passes(float2* A, float2* B, int n, int
         const int ns = sch.span[p];
         const uint32_t qm = sch.qmagic[p], sm = sch.smagic[p];
         switch (sch.radix[p]) {
-            case 2: mixed_pass<2, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 3: mixed_pass<3, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 4: mixed_pass<4, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 5: mixed_pass<5, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            case 7: mixed_pass<7, DIR>(A, B, n, W, ns, qm, sm, twp); break;
-            default: mixed_pass<8, DIR>(A, B, n, W, ns, qm, sm, twp); break;
+            case 2: mixed_pass<2, DIR, THREADS>(A, B, n, W, ns, qm, sm, twp); break;
+            case 3: mixed_pass<3, DIR, THREADS>(A, B, n, W, ns, qm, sm, twp); break;
+            case 4: mixed_pass<4, DIR, THREADS>(A, B, n, W, ns, qm, sm, twp); break;
+            case 5: mixed_pass<5, DIR, THREADS>(A, B, n, W, ns, qm, sm, twp); break;
+            case 7: mixed_pass<7, DIR, THREADS>(A, B, n, W, ns, qm, sm, twp); break;
+            default: mixed_pass<8, DIR, THREADS>(A, B, n, W, ns, qm, sm, twp); break;
         }
         __syncthreads();
         float2* t = A;
@@ -194,8 +195,8 @@ __device__ __forceinline__ float2* mixed_passes(float2* A, float2* B, int n, int
     return A;
 }
 
-template <int MODE, int DIR>
-__global__ void __launch_bounds__(kMixedThreads)
+template <int MODE, int DIR, int THREADS>
+__global__ void __launch_bounds__(THREADS)
     k_mixed(const void* in_, void* out_, int64_t nrows, int n, int W, MixedSched sch,
             const float2* __restrict__ tw, const float2* __restrict__ ph, int shift_in,
             int shift_out, float scale, int mmax, int mmajor, uint32_t wmagic,
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kMixedThreads)
     const bool wfast_in = SYN && mmajor;
     const uint32_t nm = sch.nmagic;
 #pragma unroll 4
-    for (int idx = tid; idx < W * n; idx += kMixedThreads) {
+    for (int idx = tid; idx < W * n; idx += THREADS) {
         int w, e;
         if (wfast_in) {
             e = mdiv(idx, wmagic);
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kMixedThreads)
     }
     __syncthreads();
 
-    A = mixed_passes<DIR>(A, B, n, W, sch, tw);
+    A = mixed_passes<DIR, THREADS>(A, B, n, W, sch, tw);
 
     // ---- store from A ----
     if constexpr (MODE == kMixedRowsT2) {
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kMixedThreads)
         const int64_t b0 = tr0 / tn1;
         const int k10 = (int)(tr0 - b0 * tn1);
 #pragma unroll 4
-        for (int idx = tid; idx < W * n; idx += kMixedThreads) {
+        for (int idx = tid; idx < W * n; idx += THREADS) {
             const int k = mdiv(idx, wmagic), w = idx - k * W;
             const int64_t tr = tr0 + w;
             if (tr >= ntr) continue;
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(kMixedThreads)
         const int64_t b0 = tr0 / tn1;  // transform and k1 of the CTA's first row
         const int k10 = (int)(tr0 - b0 * tn1);
 #pragma unroll 4
-        for (int idx = tid; idx < W * n; idx += kMixedThreads) {
+        for (int idx = tid; idx < W * n; idx += THREADS) {
             const int k = mdiv(idx, wmagic), w = idx - k * W;
             const int64_t tr = tr0 + w;
             if (tr >= ntr) continue;
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kMixedThreads)
         }
     } else if constexpr (MODE == BLU_C2C || MODE == BLU_C2R || MODE == BLU_C2R2) {
 #pragma unroll 4
-        for (int idx = tid; idx < W * n; idx += kMixedThreads) {
+        for (int idx = tid; idx < W * n; idx += THREADS) {
             const int w = mdiv(idx, nm), k = idx - w * n;
             const int64_t tr = tr0 + w;
             if (tr >= ntr) continue;
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kMixedThreads)
     } else {  // analysis: bins m <= mmax into the spectrum layout (w fastest when m-major)
         const int nk = mmax + 1;
         float2* F = static_cast<float2*>(out_);
-        for (int idx = tid; idx < W * nk; idx += kMixedThreads) {
+        for (int idx = tid; idx < W * nk; idx += THREADS) {
             const int q = mdiv(idx, mmajor ? wmagic : kmagic);
             const int w = mmajor ? idx - q * W : q;
             const int m = mmajor ? q : idx - q * nk;
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(kMixedThreads)
         A[c * n1 + r] = a;
     }
     __syncthreads();
-    A = mixed_passes<DIR>(A, B, n1, C, sch, tw);
+    A = mixed_passes<DIR, kMixedThreads>(A, B, n1, C, sch, tw);
     const uint32_t lomask = (1u << lobits) - 1u;
 #pragma unroll 4
     for (int idx = tid; idx < C * n1; idx += kMixedThreads) {
@@ -491,23 +492,31 @@ cudaError_t launch_mixed(const void* in, void* out, int64_t nrows, int n, const 
                          float scale, int mmax, int mmajor, int tn1, cudaStream_t stream,
                          int64_t nreal = 0) {
     if (n < 2 || n > kMaxMixedN) return cudaErrorInvalidValue;
-    auto kern = k_mixed<MODE, DIR>;
+    const bool pair = MODE == BLU_R2C2 || MODE == BLU_C2R2;
+    const int64_t ntr = pair ? (nrows + 1) / 2 : nrows;
+    constexpr bool onepass = MODE != kMixedRowsT && MODE != kMixedRowsT2;
+    const bool small = onepass && mixed_small_cta(n, ntr);
+    auto kern = small ? k_mixed<MODE, DIR, kMixedSmallThreads> : k_mixed<MODE, DIR, kMixedThreads>;
     static LaunchCache cache;
     LaunchGeom geo;
     cudaError_t e = cache.get(
         [&](int, LaunchGeom*) {
-            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)mixed_smem_bytes(kMaxMixedN));
+            cudaError_t r = cudaFuncSetAttribute(k_mixed<MODE, DIR, kMixedThreads>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)mixed_smem_bytes(kMaxMixedN));
+            if (r != cudaSuccess || !onepass) return r;
+            return cudaFuncSetAttribute(k_mixed<MODE, DIR, kMixedSmallThreads>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)mixed_smem_bytes_for(1024, true));
         },
         &geo);
     if (e != cudaSuccess) return e;
-    const int W = mixed_rows_per_cta(n);
-    const bool pair = MODE == BLU_R2C2 || MODE == BLU_C2R2;
-    const int64_t ntr = pair ? (nrows + 1) / 2 : nrows;
+    const int W = mixed_rows_for(n, small);
     const int64_t grid = (ntr + W - 1) / W;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, kMixedThreads, mixed_smem_bytes(n), stream>>>(
+    kern<<<(unsigned)grid, small ? kMixedSmallThreads : kMixedThreads,
+           mixed_smem_bytes_for(n, small), stream>>>(
         in, out, nrows, n, W, sch, tw, ph, shift_in, shift_out, scale, mmax, mmajor,
         div_magic((uint32_t)W), div_magic((uint32_t)(mmax + 1)), tn1, nreal);
     return cudaGetLastError();

@@ -157,6 +157,60 @@ def test_any_length_full_batch_sampled():
     assert_parity(ys, oracle.transform(x[rows], -1), n, "n=1000 full batch")
 
 
+@pytest.mark.parametrize("n", [12, 100, 1000])
+@pytest.mark.parametrize("direction,shift", [(-1, False), (1, True)])
+def test_mixed_small_shape_large_batches(n, direction, shift):
+    """Batches of at least 8192 rows of at most 1024 points take the mixed-radix kernel's
+    128-thread shape: ragged against its rows per CTA, sampled rows against the oracle."""
+    m = fx()
+    batch = 8192 + 37
+    p = m.Plan(n, batch, 1, direction, shift=shift)
+    assert "path=mixed" in p.describe() and "threads=128" in p.describe()
+    x = wl().normal(7320 + n, batch, n)
+    y = p.c2c(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    p.check()
+    rng = np.random.default_rng(n)
+    rows = np.array(sorted({0, batch - 1, *rng.integers(0, batch, 30).tolist()}))
+    ys = y[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_parity(ys, oracle.transform(x[rows], direction, 1, shift), n, f"small shape n={n}")
+
+
+@pytest.mark.parametrize("pairing", [False, True])
+def test_mixed_small_shape_real_rows(pairing):
+    """Real rows of 100 points, 16384 + 5 of them (at least 8192 transforms either way):
+    synthesis then analysis on the 128-thread shape, sampled rows against the direct sums."""
+    m = fx()
+    n, rows, mmax = 100, 16389, 50
+    syn = m.Plan(n, rows, 1, m.INVERSE, layout=m.LAYOUT_REAL_MMAJOR, mmax=mmax, pairing=pairing)
+    ana = m.Plan(n, rows, 1, m.FORWARD, layout=m.LAYOUT_REAL_ROWMAJOR, mmax=mmax, pairing=pairing)
+    assert "threads=128" in syn.describe() and "threads=128" in ana.describe()
+    F = wl().spectrum(7330, rows, mmax)
+    x = syn.c2r(torch.from_numpy(np.ascontiguousarray(oracle.to_mmajor(F), dtype=np.complex64)).cuda())
+    G = ana.r2c(x)
+    torch.cuda.synchronize()
+    syn.check()
+    ana.check()
+    pick = np.array(sorted({0, rows - 1, *np.random.default_rng(7330).integers(0, rows, 30).tolist()}))
+    xs = x.cpu().numpy()
+    ref_x = oracle.c2r_direct(F[pick], n)
+    scale_x = np.sqrt(np.mean(ref_x ** 2, axis=1))
+    part = pick ^ 1  # the other row of each pair (rows 2p, 2p+1 share one transform)
+    alone = part >= rows  # the last row of an odd count shares its transform with no row
+    part = np.minimum(part, rows - 1)
+    if pairing:  # a row's error is set by its pair
+        other = np.sqrt(np.mean(oracle.c2r_direct(F[part], n) ** 2, axis=1))
+        scale_x = np.where(alone, scale_x, np.hypot(scale_x, other))
+    assert_parity(xs[pick], ref_x, n, f"small shape synthesis pairing={pairing}", scale=scale_x)
+    ref_G = oracle.r2c_direct(xs[pick].astype(np.float64), mmax)
+    scale_G = np.linalg.norm(xs[pick].astype(np.float64), axis=1)
+    if pairing:
+        other = np.linalg.norm(xs[part].astype(np.float64), axis=1)
+        scale_G = np.where(alone, scale_G, np.hypot(scale_G, other))
+    assert_parity(G.cpu().numpy()[pick], ref_G, mmax + 1, f"small shape analysis pairing={pairing}",
+                  scale=scale_G)
+
+
 # ---- band-limited real rows of any length (the any-nphi 'dft' mode) --------------------------
 LAYOUTS = {"rowmajor": 1, "mmajor": 2}
 
