@@ -213,8 +213,18 @@ __global__ void __launch_bounds__(THREADS)
     // ---- load: W transforms' inputs into A (w fastest for the m-major spectrum gathers) ----
     const bool wfast_in = SYN && mmajor;
     const uint32_t nm = sch.nmagic;
+    // complex rows without a load factor: the CTA's rows are one contiguous run
+    constexpr bool CONTIG = MODE == BLU_C2C || MODE == kMixedRowsT || MODE == kMixedRowsT2;
+    const bool linear_in = CONTIG && !(MODE == BLU_C2C && shift_in);
+    const int cnt = (int)((ntr - tr0 < W ? ntr - tr0 : W) * n);  // points of rows that exist
+    if (linear_in) {
+        const float2* src = static_cast<const float2*>(in_) + tr0 * n;
 #pragma unroll 4
-    for (int idx = tid; idx < W * n; idx += THREADS) {
+        for (int i = tid; i < W * n; i += THREADS)
+            A[i] = i < cnt ? ldg_stream(src + i) : make_float2(0.f, 0.f);
+    }
+#pragma unroll 4
+    for (int idx = linear_in ? W * n : tid; idx < W * n; idx += THREADS) {
         int w, e;
         if (wfast_in) {
             e = mdiv(idx, wmagic);
@@ -308,8 +318,16 @@ __global__ void __launch_bounds__(THREADS)
                        make_float2(y.x * scale, y.y * scale));
         }
     } else if constexpr (MODE == BLU_C2C || MODE == BLU_C2R || MODE == BLU_C2R2) {
+        if (MODE == BLU_C2C && !shift_out) {  // one contiguous run, as on the load
+            float2* dst = static_cast<float2*>(out_) + tr0 * n;
 #pragma unroll 4
-        for (int idx = tid; idx < W * n; idx += THREADS) {
+            for (int i = tid; i < cnt; i += THREADS) {
+                const float2 y = A[i];
+                stg_stream(dst + i, make_float2(y.x * scale, y.y * scale));
+            }
+        }
+#pragma unroll 4
+        for (int idx = MODE == BLU_C2C && !shift_out ? W * n : tid; idx < W * n; idx += THREADS) {
             const int w = mdiv(idx, nm), k = idx - w * n;
             const int64_t tr = tr0 + w;
             if (tr >= ntr) continue;
