@@ -213,24 +213,15 @@ __global__ void __launch_bounds__(THREADS)
     // ---- load: W transforms' inputs into A (w fastest for the m-major spectrum gathers) ----
     const bool wfast_in = SYN && mmajor;
     const uint32_t nm = sch.nmagic;
-    // rows without a load factor (complex rows, one real row per transform): the CTA's rows
-    // are one contiguous run
-    constexpr bool CONTIG = MODE == BLU_C2C || MODE == kMixedRowsT || MODE == kMixedRowsT2 ||
-                            MODE == BLU_R2C;
+    // complex rows without a load factor: the CTA's rows are one contiguous run
+    constexpr bool CONTIG = MODE == BLU_C2C || MODE == kMixedRowsT || MODE == kMixedRowsT2;
     const bool linear_in = CONTIG && !(MODE == BLU_C2C && shift_in);
     const int cnt = (int)((ntr - tr0 < W ? ntr - tr0 : W) * n);  // points of rows that exist
     if (linear_in) {
-        if constexpr (MODE == BLU_R2C) {
-            const float* src = static_cast<const float*>(in_) + tr0 * n;
+        const float2* src = static_cast<const float2*>(in_) + tr0 * n;
 #pragma unroll 4
-            for (int i = tid; i < W * n; i += THREADS)
-                A[i] = make_float2(i < cnt ? __ldcs(src + i) : 0.f, 0.f);
-        } else {
-            const float2* src = static_cast<const float2*>(in_) + tr0 * n;
-#pragma unroll 4
-            for (int i = tid; i < W * n; i += THREADS)
-                A[i] = i < cnt ? ldg_stream(src + i) : make_float2(0.f, 0.f);
-        }
+        for (int i = tid; i < W * n; i += THREADS)
+            A[i] = i < cnt ? ldg_stream(src + i) : make_float2(0.f, 0.f);
     }
 #pragma unroll 4
     for (int idx = linear_in ? W * n : tid; idx < W * n; idx += THREADS) {
@@ -327,25 +318,16 @@ __global__ void __launch_bounds__(THREADS)
                        make_float2(y.x * scale, y.y * scale));
         }
     } else if constexpr (MODE == BLU_C2C || MODE == BLU_C2R || MODE == BLU_C2R2) {
-        // one contiguous run, as on the load (complex rows without a store factor; one real
-        // row per transform)
-        const bool linear_out = (MODE == BLU_C2C && !shift_out) || MODE == BLU_C2R;
-        if (linear_out) {
-            if constexpr (MODE == BLU_C2R) {
-                float* dst = static_cast<float*>(out_) + tr0 * n;
+        if (MODE == BLU_C2C && !shift_out) {  // one contiguous run, as on the load
+            float2* dst = static_cast<float2*>(out_) + tr0 * n;
 #pragma unroll 4
-                for (int i = tid; i < cnt; i += THREADS) __stcs(dst + i, A[i].x);
-            } else {
-                float2* dst = static_cast<float2*>(out_) + tr0 * n;
-#pragma unroll 4
-                for (int i = tid; i < cnt; i += THREADS) {
-                    const float2 y = A[i];
-                    stg_stream(dst + i, make_float2(y.x * scale, y.y * scale));
-                }
+            for (int i = tid; i < cnt; i += THREADS) {
+                const float2 y = A[i];
+                stg_stream(dst + i, make_float2(y.x * scale, y.y * scale));
             }
         }
 #pragma unroll 4
-        for (int idx = linear_out ? W * n : tid; idx < W * n; idx += THREADS) {
+        for (int idx = MODE == BLU_C2C && !shift_out ? W * n : tid; idx < W * n; idx += THREADS) {
             const int w = mdiv(idx, nm), k = idx - w * n;
             const int64_t tr = tr0 + w;
             if (tr >= ntr) continue;
