@@ -1,5 +1,12 @@
 // Entry points of the mixed-radix four-step transform for band-limited real rows (two rows per
-// transform), next to the complex entry points declared in kernels.h.
+// transform), next to the complex entry points declared in kernels.h, and the launch shape of
+// the one-pass kernel.
+//
+// Rows of up to 2^20 points whose prime factors are 2, 3, 5 and 7 run the mixed-radix passes
+// of mixed.cuh as a four-step transform n = N1*N2: k_mixed_cols transforms the columns of each
+// [N1][N2] matrix with the twiddle w_n^{n2*k1} on its store, then k_mixed in mode kMixedRowsT
+// (or kMixedRowsT2 for the synthesis of real rows) transforms the rows with a transposed store;
+// the analysis of real rows ends with k_mixed_unpack.
 #pragma once
 
 #include "kernels.h"

@@ -250,3 +250,47 @@ def test_rectangular_2d_plans(ny, nx):
     assert L.fft_plan_query_2d(nx, 0, 1, -1, 0, None, 0) == fx.FFT_ERR_UNSUPPORTED_SIZE
     assert L.fft_plan_query_2d(nx, 8192, 1, -1, 0, None, 0) == fx.FFT_ERR_UNSUPPORTED_SIZE
     assert L.fft_plan_create_2d(nx, ny, 1, -1, 0, None) == fx.FFT_ERR_INVALID_ARG
+
+
+def test_every_smooth_length_plans_a_valid_mixed_schedule():
+    """Every length up to 2^20 whose prime factors are 2, 3, 5 and 7 (and is not a power of
+    two) plans the mixed-radix path: one pass up to 8192 points with radices from
+    {2, 3, 4, 5, 7, 8} whose product is n (odd radices first, then 8s and one 4 or 2), the
+    four-step above with n1*n2 = n, n1 <= min(512, sqrt(n)), n2 <= 8192 and both factors
+    scheduled the same way; every other length takes a chirp-z path."""
+    def smooth(v):
+        for f in (2, 3, 5, 7):
+            while v % f == 0:
+                v //= f
+        return v == 1
+
+    def check_radix(text, m):
+        rs = [int(r) for r in text.split("x")]
+        prod = 1
+        for r in rs:
+            prod *= r
+        assert prod == m and all(r in (2, 3, 4, 5, 7, 8) for r in rs) and len(rs) <= 16
+        odd = [r for r in rs if r % 2]
+        assert rs[:len(odd)] == odd  # odd radices first
+        even = rs[len(odd):]
+        assert all(r == 8 for r in even[:-1]) and even.count(4) + even.count(2) <= 1
+
+    seen = 0
+    for n in range(3, (1 << 20) + 1):
+        if n & (n - 1) == 0 or not smooth(n):
+            continue
+        d = fx.query(n, 2)
+        seen += 1
+        if n <= 8192:
+            assert "path=mixed " in d, (n, d)
+            check_radix(d.split("radix=")[1].split()[0], n)
+        else:
+            assert "path=mixed_fourstep" in d, (n, d)
+            n1 = int(d.split("n1=")[1].split()[0])
+            n2 = int(d.split("n2=")[1].split()[0])
+            assert n1 * n2 == n and n1 <= 512 and n1 * n1 <= n and n2 <= 8192, (n, n1, n2)
+            check_radix(d.split("pass1=columns(radix=")[1].split()[0], n1)
+            check_radix(d.split("pass2=rows_transposed(radix=")[1].split()[0], n2)
+    assert seen > 1000
+    for n in (11, 13 * 8, 1001, 8191, 8193, 12289, 99991):
+        assert "path=bluestein" in fx.query(n, 2)
