@@ -25,9 +25,10 @@ the roofline of the dominant kernel, measured live with CUDA events on the launc
 library), on a bounded sample of the same workload, on the host cores.
 
 Timing rules: W >= 3 untimed warm-up steps; K timed steps bracketed by a barrier and a device
-synchronisation; inputs are larger than L2 for the default workload (smaller ones flush L2
-between steps by writing a 512 MiB buffer, outside the timed kernel windows); nvidia-smi clocks
-are sampled during the timed region.
+synchronisation, the K-step window repeated (the same count on every rank) until --min-seconds
+(default 1 s) has passed, the median per-step time reported; inputs are larger than L2 for the
+default workload (smaller ones flush L2 between steps by writing a 512 MiB buffer, outside the
+timed kernel windows); nvidia-smi clocks are sampled during the timed region.
 """
 import argparse
 import hashlib
