@@ -263,7 +263,7 @@ def test_rectangular_2d_matches_numpy_and_separability(ny, nx):
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 6, 7, 12, 30, 97, 100, 210, 1000, 1024, 3 * 5 * 7 * 11,
-                               2 * 8191, 60000])
+                               2 * 8191, 60000, 100000, 3 ** 12, 10 ** 6, (1 << 20) - 1])
 @pytest.mark.parametrize("sign", [-1, 1])
 def test_mixed_radix_fft_any_length(n, sign):
     """The mixed-radix FFT against numpy's FFT (a library routine) at composite, prime and
