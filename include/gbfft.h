@@ -302,7 +302,8 @@ int fft_plan_destroy(fft_plan plan);
  * ignored) to synchronise `stream`, read and clear the word, and get FFT_ERR_TIMEOUT if any
  * earlier call on the current device timed out (FFT_OK otherwise).
  * Returns FFT_OK, FFT_ERR_INVALID_ARG, FFT_ERR_UNSUPPORTED_SIZE, FFT_ERR_MISALIGNED or
- * FFT_ERR_CUDA; the status form (n == 0) returns FFT_OK, FFT_ERR_TIMEOUT or FFT_ERR_CUDA.
+ * FFT_ERR_CUDA; the status form (n == 0) returns FFT_OK, FFT_ERR_TIMEOUT, FFT_ERR_BOUNDS
+ * (checked build only) or FFT_ERR_CUDA.
  */
 int fft_exec_c2c_noalloc(int64_t n, int64_t batch, int direction, int shift, const void* in,
                          void* out, void* stream);
